@@ -124,13 +124,19 @@ static float bf16_bits_to_float(uint16_t h) {
 
 /* q8 = E4M3_RNE_sat(fl32(q / q_descale)).  The quotient is formed in double
  * and rounded once to float, which equals the correctly rounded fp32 quotient
- * (double carries more than 2*24+2 bits). */
+ * (double carries more than 2*24+2 bits).  A NaN quotient (NaN input, 0/0,
+ * inf/inf) encodes as 0x7F carrying the sign bit of the input q: the sign of
+ * a NaN produced by a division is not fixed by IEEE 754, so the input's sign
+ * is the one kept. */
 void or_quantize_q(const uint16_t* q_bf16, int64_t n, float q_descale, uint8_t* out) {
   int64_t i;
   for (i = 0; i < n; ++i) {
     float x = bf16_bits_to_float(q_bf16[i]);
     float v = (float)((double)x / (double)q_descale);
-    out[i] = or_e4m3_encode(v);
+    if (isnan(v))
+      out[i] = (uint8_t)(0x7F | ((q_bf16[i] >> 8) & 0x80));
+    else
+      out[i] = or_e4m3_encode(v);
   }
 }
 

@@ -164,6 +164,15 @@ def test_quantize_q_division_not_reciprocal_multiply():
         assert oracle.quantize_q(np.array([b]), float(d))[0] == want
 
 
+def test_quantize_q_nan_quotient_keeps_input_sign():
+    bits = np.array([0x7FC1, 0xFFC1, 0x7F81, 0xFF81], np.uint16)       # +-qNaN, +-sNaN payloads
+    assert list(oracle.quantize_q(bits, 0.5)) == [0x7F, 0xFF, 0x7F, 0xFF]
+    zeros = np.array([0x0000, 0x8000], np.uint16)                     # 0 / 0 and -0 / 0
+    assert list(oracle.quantize_q(zeros, 0.0)) == [0x7F, 0xFF]
+    infs = np.array([0x7F80, 0xFF80], np.uint16)                      # +-inf / finite saturates
+    assert list(oracle.quantize_q(infs, 3.0)) == [0x7E, 0xFE]
+
+
 # ------------------------------------------------------------------ masks
 
 def _golden_ranges():
