@@ -1,0 +1,184 @@
+"""Paged FP8 (E4M3) KV-cache attention for GB300 (sm_103a).
+
+Thin ctypes binding over the C ABI in ``include/fp8pa.h`` (library
+``_lib/libfp8pa.so``, built in-tree by ``build()``).  The functions here only
+marshal torch tensors into pointers and sizes; every step of the computation
+runs in the library's CUDA kernels.  There is no CPU fallback: if the library
+is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "build", "load_library", "library_path", "quantize_q_fp8", "fp8_paged_attn_fwd", "workspace_size",
+    "num_splits", "get_device_status", "reset_device_status", "set_wait_limit", "FP8PA_BF16", "FP8PA_E4M3",
+    "DEV_BAD_PAGE", "DEV_TIMEOUT", "DEV_BAD_LENGTH", "PAGE_SIZE", "Fp8paError",
+]
+
+FP8PA_BF16 = 0
+FP8PA_E4M3 = 1
+DEV_BAD_PAGE = 1
+DEV_TIMEOUT = 2
+DEV_BAD_LENGTH = 4
+PAGE_SIZE = 64
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Fp8paError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"fp8pa status {status}: {message}")
+        self.status = status
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library for sm_103a (in-tree)."""
+    return _build.build(force=force)
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Load libfp8pa.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not _build.up_to_date():
+            _build.build()
+        lib = ctypes.CDLL(_build.LIB_PATH)
+        c = ctypes
+        lib.quantize_q_fp8.restype = c.c_int
+        lib.quantize_q_fp8.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_longlong, c.c_void_p]
+        lib.fp8pa_workspace_size.restype = c.c_size_t
+        lib.fp8pa_workspace_size.argtypes = [c.c_int] * 9
+        lib.fp8pa_num_splits.restype = c.c_int
+        lib.fp8pa_num_splits.argtypes = [c.c_int] * 9
+        lib.fp8_paged_attn_fwd.restype = c.c_int
+        lib.fp8_paged_attn_fwd.argtypes = [
+            c.c_void_p, c.c_int, c.c_void_p, c.c_void_p, c.c_int, c.c_void_p, c.c_int, c.c_void_p, c.c_void_p,
+            c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p, c.c_int,
+            c.c_int, c.c_float, c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_size_t, c.c_void_p, c.c_void_p,
+            c.c_void_p,
+        ]
+        lib.fp8pa_get_device_status.restype = c.c_int
+        lib.fp8pa_get_device_status.argtypes = [c.c_void_p, c.c_void_p]
+        lib.fp8pa_reset_device_status.restype = c.c_int
+        lib.fp8pa_reset_device_status.argtypes = [c.c_void_p]
+        lib.fp8pa_last_error.restype = c.c_char_p
+        lib.fp8pa_last_error.argtypes = []
+        lib.fp8pa_set_wait_limit.restype = None
+        lib.fp8pa_set_wait_limit.argtypes = [c.c_uint]
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        msg = load_library().fp8pa_last_error().decode(errors="replace")
+        raise Fp8paError(rc, msg)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def workspace_size(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq,
+                   window_left=-1, num_splits=0) -> int:
+    return int(load_library().fp8pa_workspace_size(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv,
+                                                   head_dim, max_pages_per_seq, window_left, num_splits))
+
+
+def num_splits(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq,
+               window_left=-1, num_splits=0) -> int:
+    return int(load_library().fp8pa_num_splits(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim,
+                                               max_pages_per_seq, window_left, num_splits))
+
+
+def quantize_q_fp8(q: torch.Tensor, q_descale: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+    """E4M3 codes (uint8) of a bf16 tensor: RNE_sat(fl32(q / q_descale))."""
+    lib = load_library()
+    if q.dtype != torch.bfloat16 or not q.is_cuda or not q.is_contiguous():
+        raise ValueError("q must be a contiguous CUDA bfloat16 tensor")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.uint8, device=q.device)
+    _check(lib.quantize_q_fp8(_ptr(q), _ptr(out), _ptr(q_descale), q.numel(), _stream_ptr(stream)))
+    return out
+
+
+def fp8_paged_attn_fwd(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q, q_descale,
+                       k_descale, v_descale, softmax_scale, window_left=-1, causal=True, num_splits=0,
+                       out=None, lse=None, workspace=None, descale_batch_stride=0, descale_head_stride=0,
+                       stream=None, return_lse=True):
+    """Attention over a paged E4M3 KV cache.
+
+    q: [total_q, Hq, D] bf16, or uint8 E4M3 codes (FP8-MMA path);
+    k_cache, v_cache: uint8 [num_pages, 64, Hkv, D]; block_table int32 [B, max_pages];
+    cu_seqlens_q int32 [B+1]; seqused_k int32 [B]; descales: f32 device tensors.
+    Returns (out bf16 [total_q, Hq, D], lse f32 [Hq, total_q] or None).
+    """
+    lib = load_library()
+    if q.dtype == torch.bfloat16:
+        q_dtype = FP8PA_BF16
+    elif q.dtype in (torch.uint8, torch.float8_e4m3fn):
+        q_dtype = FP8PA_E4M3
+    else:
+        raise ValueError(f"unsupported q dtype {q.dtype}")
+    total_q, hq, d = q.shape
+    num_pages, page, hkv, d2 = k_cache.shape
+    if page != PAGE_SIZE or d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache / v_cache must be [num_pages, 64, Hkv, D] with D equal to q's head dim")
+    batch, max_pages = block_table.shape
+    if out is None:
+        out = torch.empty((total_q, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((hq, total_q), dtype=torch.float32, device=q.device)
+    need = workspace_size(batch, total_q, max_seqlen_q, hq, hkv, d, max_pages, window_left, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("block_table", block_table),
+                    ("cu_seqlens_q", cu_seqlens_q), ("seqused_k", seqused_k), ("out", out)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    _check(lib.fp8_paged_attn_fwd(
+        _ptr(q), q_dtype, _ptr(k_cache), _ptr(v_cache), num_pages, _ptr(block_table), max_pages,
+        _ptr(cu_seqlens_q), _ptr(seqused_k), batch, total_q, max_seqlen_q, hq, hkv, d, _ptr(q_descale),
+        _ptr(k_descale), _ptr(v_descale), descale_batch_stride, descale_head_stride, float(softmax_scale),
+        int(window_left), int(bool(causal)), int(num_splits), _ptr(workspace), workspace.numel(), _ptr(out),
+        _ptr(lse), _stream_ptr(stream)))
+    return out, lse
+
+
+def get_device_status(stream=None) -> int:
+    """Status bits accumulated on the current device (synchronizes the stream)."""
+    lib = load_library()
+    host = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(lib.fp8pa_get_device_status(host.data_ptr(), _stream_ptr(s)))
+    s.synchronize()
+    return int(host.item()) & 0xFFFFFFFF
+
+
+def reset_device_status(stream=None):
+    _check(load_library().fp8pa_reset_device_status(_stream_ptr(stream)))
+
+
+def set_wait_limit(max_iterations: int):
+    """Test hook: cap every bounded pipeline wait (0 restores the default)."""
+    load_library().fp8pa_set_wait_limit(int(max_iterations))

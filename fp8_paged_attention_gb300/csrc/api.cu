@@ -1,0 +1,413 @@
+// C ABI of the library: argument checks, split choice, workspace layout,
+// TMA descriptors and kernel launches.  Nothing here allocates device memory,
+// synchronizes, or reads device memory on the host.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "fp8pa.h"
+#include "kernels.h"
+
+namespace fp8pa {
+cudaError_t launch_attn_fp8_d256(int, const AttnParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                 int, cudaStream_t);
+cudaError_t launch_attn_fp8_d512(int, const AttnParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                 int, cudaStream_t);
+cudaError_t launch_attn_bf16_d512(int, const AttnParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                  int, cudaStream_t);
+int smem_attn_fp8_d256(int);
+int smem_attn_fp8_d512(int);
+int smem_attn_bf16_d512(int);
+
+cudaError_t launch_attn(int head_dim, bool fp8_q, int rows, const AttnParams& p, const CUtensorMap& tm_q,
+                        const CUtensorMap& tm_k, const CUtensorMap& tm_v, int grid, cudaStream_t stream) {
+  if (head_dim == 256 && fp8_q) return launch_attn_fp8_d256(rows, p, tm_q, tm_k, tm_v, grid, stream);
+  if (head_dim == 512 && fp8_q) return launch_attn_fp8_d512(rows, p, tm_q, tm_k, tm_v, grid, stream);
+  if (head_dim == 512 && !fp8_q) return launch_attn_bf16_d512(rows, p, tm_q, tm_k, tm_v, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+int attn_smem_bytes(int head_dim, bool fp8_q, int rows) {
+  if (head_dim == 256 && fp8_q) return smem_attn_fp8_d256(rows);
+  if (head_dim == 512 && fp8_q) return smem_attn_fp8_d512(rows);
+  if (head_dim == 512 && !fp8_q) return smem_attn_bf16_d512(rows);
+  return 0;
+}
+}  // namespace fp8pa
+
+using namespace fp8pa;
+
+namespace {
+
+__device__ unsigned int g_status;
+
+thread_local char g_err[512] = "";
+std::atomic<unsigned> g_wait_limit{0};
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(FP8PA_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+constexpr int kDefaultSms = 152;  // GB300; used when no device is visible (host-only sizing)
+
+int device_sms() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return kDefaultSms;
+  }
+  int v = cache[dev].load();
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+      cudaGetLastError();
+      return kDefaultSms;
+    }
+    cache[dev].store(v);
+  }
+  return v;
+}
+
+unsigned* status_ptr() {
+  static std::atomic<unsigned*> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned* p = cache[dev].load();
+  if (!p) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status) != cudaSuccess) return nullptr;
+    p = static_cast<unsigned*>(addr);
+    cache[dev].store(p);
+  }
+  return p;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Everything about a call that follows from host-known sizes.
+struct CallPlan {
+  int group;
+  int num_classes;
+  ClassInfo cls[2];
+  int splits;
+  size_t items_max[2];
+  size_t off_work[2], off_opart, off_lsepart, total;
+};
+
+int check_shape(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int head_dim, int max_pages,
+                int window_left, int num_splits) {
+  if (batch < 0 || total_q < 0 || max_seqlen_q < 0)
+    return fail(FP8PA_EINVAL, "batch, total_q and max_seqlen_q must be >= 0 (got %d, %d, %d)", batch, total_q,
+                max_seqlen_q);
+  if (total_q > 0 && max_seqlen_q < 1) return fail(FP8PA_EINVAL, "max_seqlen_q must be >= 1 when total_q > 0");
+  if (max_seqlen_q > total_q && total_q > 0)
+    return fail(FP8PA_EINVAL, "max_seqlen_q (%d) exceeds total_q (%d)", max_seqlen_q, total_q);
+  if (hkv <= 0 || hq <= 0) return fail(FP8PA_EINVAL, "num_heads_q and num_heads_kv must be > 0");
+  if (hq % hkv != 0)
+    return fail(FP8PA_EUNSUPPORTED, "num_heads_q (%d) must be a multiple of num_heads_kv (%d)", hq, hkv);
+  const int g = hq / hkv;
+  if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16)
+    return fail(FP8PA_EUNSUPPORTED, "query heads per KV head = %d; supported: 1, 2, 4, 8, 16", g);
+  if (head_dim != 256 && head_dim != 512)
+    return fail(FP8PA_EUNSUPPORTED, "head_dim %d is not supported (supported: 256 with E4M3 Q, 512 with BF16 or E4M3 Q)",
+                head_dim);
+  if (max_pages < 1) return fail(FP8PA_EINVAL, "max_pages_per_seq must be >= 1");
+  if ((long long)max_pages * kPage > 0x7FFFFFFFLL) return fail(FP8PA_EINVAL, "max_pages_per_seq too large");
+  if (window_left < -1) return fail(FP8PA_EINVAL, "window_left must be >= -1 (got %d)", window_left);
+  if (num_splits < 0 || num_splits > 256) return fail(FP8PA_EINVAL, "num_splits must be in [0, 256] (got %d)", num_splits);
+  if ((long long)total_q * hq > 0x7FFFFFFFLL) return fail(FP8PA_EINVAL, "total_q * num_heads_q too large");
+  return FP8PA_OK;
+}
+
+int auto_splits(const CallPlan& pl, int batch, int hkv, int max_pages, int window_left, int max_lq0, int sms) {
+  const long long units = (long long)hkv * batch;
+  if (units <= 0) return 1;
+  long long pages = max_pages;
+  if (window_left >= 0) pages = std::min<long long>(pages, (window_left + max_lq0 - 1) / kPage + 2);
+  const long long tiles = (pages + 1) / 2;
+  long long s = (8LL * sms + units - 1) / units;
+  s = std::min<long long>(s, std::max<long long>(1, tiles / 4));
+  s = std::max<long long>(1, std::min<long long>(s, 64));
+  (void)pl;
+  return (int)s;
+}
+
+int make_plan(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int head_dim, int max_pages,
+              int window_left, int num_splits, CallPlan& pl) {
+  int rc = check_shape(batch, total_q, max_seqlen_q, hq, hkv, head_dim, max_pages, window_left, num_splits);
+  if (rc) return rc;
+  const int g = hq / hkv;
+  pl.group = g;
+  const long long rmax = (long long)max_seqlen_q * g;
+  int lq0_max;
+  if (rmax <= 32) {
+    pl.num_classes = 1;
+    pl.cls[0] = ClassInfo{1, std::max(1, max_seqlen_q), rmax <= 16 ? 16 : 32, 1};
+    lq0_max = std::max(1, max_seqlen_q);
+  } else {
+    lq0_max = 16 / g;
+    if (lq0_max >= 1) {
+      pl.num_classes = 2;
+      pl.cls[0] = ClassInfo{1, lq0_max, 16, 1};
+      pl.cls[1] = ClassInfo{lq0_max + 1, max_seqlen_q, 64, 1};
+    } else {
+      pl.num_classes = 2;  // class 0 empty
+      pl.cls[0] = ClassInfo{1, 0, 16, 1};
+      pl.cls[1] = ClassInfo{1, max_seqlen_q, 64, 1};
+      lq0_max = 1;
+    }
+  }
+  pl.splits = num_splits > 0 ? num_splits
+                             : auto_splits(pl, batch, hkv, max_pages, window_left, lq0_max, device_sms());
+  pl.cls[0].max_splits = pl.splits;
+  // workspace layout: [counts][class-0 items][class-1 items][o_part][lse_part]
+  pl.items_max[0] = (size_t)hkv * batch * pl.splits;
+  pl.items_max[1] =
+      pl.num_classes > 1 ? (size_t)hkv * ((size_t)((long long)total_q * g + 63) / 64 + (size_t)batch) : 0;
+  size_t off = 256;
+  for (int k = 0; k < 2; ++k) {
+    pl.off_work[k] = off;
+    off = round_up(off + pl.items_max[k] * sizeof(int4), 256);
+  }
+  pl.off_opart = off;
+  if (pl.splits > 1) off = round_up(off + (size_t)pl.splits * total_q * hq * head_dim * sizeof(float), 256);
+  pl.off_lsepart = off;
+  if (pl.splits > 1) off = round_up(off + (size_t)pl.splits * hq * total_q * sizeof(float), 256);
+  pl.total = off;
+  return FP8PA_OK;
+}
+
+int encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+               const cuuint64_t* strides, const cuuint32_t* box, const char* what) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FP8PA_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, dt, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FP8PA_ECUDA, "cuTensorMapEncodeTiled failed for %s (CUresult %d)", what, (int)r);
+  return FP8PA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fp8pa_last_error(void) { return g_err; }
+
+void fp8pa_set_wait_limit(unsigned int max_iterations) { g_wait_limit.store(max_iterations); }
+
+int quantize_q_fp8(const void* q_bf16, void* q_e4m3, const float* q_descale, long long n_elems,
+                   fp8pa_stream_t stream) {
+  if (n_elems < 0) return fail(FP8PA_EINVAL, "n_elems must be >= 0 (got %lld)", n_elems);
+  if (n_elems == 0) return FP8PA_OK;
+  if (!q_bf16 || !q_e4m3 || !q_descale) return fail(FP8PA_EINVAL, "quantize_q_fp8: null pointer");
+  cudaError_t e = launch_quantize_q(q_bf16, q_e4m3, q_descale, n_elems, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize_q_fp8 launch");
+  return FP8PA_OK;
+}
+
+size_t fp8pa_workspace_size(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv,
+                            int head_dim, int max_pages_per_seq, int window_left, int num_splits) {
+  CallPlan pl;
+  if (make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq, window_left,
+                num_splits, pl))
+    return 0;
+  return pl.total;
+}
+
+int fp8pa_num_splits(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
+                     int max_pages_per_seq, int window_left, int num_splits) {
+  CallPlan pl;
+  if (make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq, window_left,
+                num_splits, pl))
+    return 0;
+  return pl.splits;
+}
+
+int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* v_cache, int num_pages,
+                       const int32_t* block_table, int max_pages_per_seq, const int32_t* cu_seqlens_q,
+                       const int32_t* seqused_k, int batch, int total_q, int max_seqlen_q, int num_heads_q,
+                       int num_heads_kv, int head_dim, const float* q_descale, const float* k_descale,
+                       const float* v_descale, int descale_batch_stride, int descale_head_stride,
+                       float softmax_scale, int window_left, int causal, int num_splits, void* workspace,
+                       size_t workspace_bytes, void* out, float* lse, fp8pa_stream_t stream) {
+  if (q_dtype != FP8PA_BF16 && q_dtype != FP8PA_E4M3)
+    return fail(FP8PA_EINVAL, "q_dtype must be FP8PA_BF16 (0) or FP8PA_E4M3 (1), got %d", q_dtype);
+  const bool fp8_q = q_dtype == FP8PA_E4M3;
+  CallPlan pl;
+  int rc = make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq,
+                     window_left, num_splits, pl);
+  if (rc) return rc;
+  if (head_dim == 256 && !fp8_q)
+    return fail(FP8PA_EUNSUPPORTED,
+                "q dtype bfloat16 with k/v dtype float8_e4m3fn at head_size 256 is not supported "
+                "(head_size 256 takes E4M3 Q; quantize it with quantize_q_fp8)");
+  if (causal != 0 && causal != 1) return fail(FP8PA_EINVAL, "causal must be 0 or 1 (got %d)", causal);
+  if (!std::isfinite(softmax_scale)) return fail(FP8PA_EINVAL, "softmax_scale must be finite");
+  if (descale_batch_stride < 0 || descale_head_stride < 0) return fail(FP8PA_EINVAL, "descale strides must be >= 0");
+  if (batch == 0 || total_q == 0) return FP8PA_OK;
+  if (num_pages < 1) return fail(FP8PA_EINVAL, "num_pages must be >= 1 (got %d)", num_pages);
+  if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !seqused_k || !k_descale || !v_descale || !out ||
+      (fp8_q && !q_descale))
+    return fail(FP8PA_EINVAL, "null pointer argument");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return fail(FP8PA_EINVAL, "q, k_cache, v_cache and out must be 16-byte aligned");
+  if (workspace_bytes < pl.total)
+    return fail(FP8PA_EINVAL, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, pl.total);
+  if (!workspace || !aligned(workspace, 256)) return fail(FP8PA_EINVAL, "workspace must be non-null and 256-byte aligned");
+
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned* status = status_ptr();
+  if (!status) return fail(FP8PA_ECUDA, "cannot resolve the device status word");
+  const int sms = device_sms();
+  const int g = pl.group;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* counts = reinterpret_cast<int*>(ws);
+
+  // TMA descriptors: K/V page tiles (128 bytes of head dim x 64 slots of one KV head of one page)
+  CUtensorMap tm_k, tm_v, tm_q[2];
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads_kv, (cuuint64_t)kPage,
+                                (cuuint64_t)num_pages};
+    const cuuint64_t strides[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads_kv * head_dim,
+                                   (cuuint64_t)kPage * num_heads_kv * head_dim};
+    const cuuint32_t box[4] = {128, 1, (cuuint32_t)kPage, 1};
+    if ((rc = encode_map(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, k_cache, dims, strides, box, "k_cache"))) return rc;
+    if ((rc = encode_map(&tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, v_cache, dims, strides, box, "v_cache"))) return rc;
+  }
+  const int esz = fp8_q ? 1 : 2;
+  for (int k = 0; k < pl.num_classes; ++k) {
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads_q, (cuuint64_t)total_q};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * esz, (cuuint64_t)num_heads_q * head_dim * esz};
+    const cuuint32_t box[3] = {(cuuint32_t)(128 / esz), (cuuint32_t)g, (cuuint32_t)(pl.cls[k].rows / g)};
+    if ((rc = encode_map(&tm_q[k], fp8_q ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q,
+                         dims, strides, box, "q")))
+      return rc;
+  }
+
+  PlanParams pp{};
+  pp.cu_seqlens_q = cu_seqlens_q;
+  pp.seqused_k = seqused_k;
+  pp.batch = batch;
+  pp.total_q = total_q;
+  pp.group = g;
+  pp.hkv = num_heads_kv;
+  pp.max_pages = max_pages_per_seq;
+  pp.window_left = window_left;
+  pp.causal = causal;
+  pp.num_classes = pl.num_classes;
+  for (int k = 0; k < 2; ++k) {
+    pp.cls[k] = pl.cls[k];
+    pp.work[k] = reinterpret_cast<int4*>(ws + pl.off_work[k]);
+  }
+  pp.counts = counts;
+  pp.status = status;
+  cudaError_t e = launch_plan(pp, st);
+  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+
+  AttnParams p{};
+  p.block_table = block_table;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.seqused_k = seqused_k;
+  p.q_descale = q_descale;
+  p.k_descale = k_descale;
+  p.v_descale = v_descale;
+  p.descale_b = descale_batch_stride;
+  p.descale_h = descale_head_stride;
+  p.batch = batch;
+  p.total_q = total_q;
+  p.hq = num_heads_q;
+  p.hkv = num_heads_kv;
+  p.group = g;
+  p.head_dim = head_dim;
+  p.max_pages = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.softmax_scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.window_left = window_left;
+  p.causal = causal;
+  p.out = out;
+  p.lse = lse;
+  p.o_part = reinterpret_cast<float*>(ws + pl.off_opart);
+  p.lse_part = reinterpret_cast<float*>(ws + pl.off_lsepart);
+  p.status = status;
+  const unsigned wl = g_wait_limit.load();
+  p.wait_limit = wl ? wl : kDefaultWaitLimit;
+  for (int k = 0; k < pl.num_classes; ++k) {
+    if (pl.cls[k].lq_max < pl.cls[k].lq_min) continue;
+    p.cls = pl.cls[k];
+    p.work = reinterpret_cast<const int4*>(ws + pl.off_work[k]);
+    p.work_count = counts + k;
+    const int grid = (int)std::min<size_t>((size_t)sms, std::max<size_t>(1, pl.items_max[k]));
+    e = launch_attn(head_dim, fp8_q, pl.cls[k].rows, p, tm_q[k], tm_k, tm_v, grid, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  }
+  if (pl.splits > 1) {
+    CombineParams cp{};
+    cp.cu_seqlens_q = cu_seqlens_q;
+    cp.seqused_k = seqused_k;
+    cp.batch = batch;
+    cp.total_q = total_q;
+    cp.hq = num_heads_q;
+    cp.group = g;
+    cp.head_dim = head_dim;
+    cp.max_pages = max_pages_per_seq;
+    cp.window_left = window_left;
+    cp.causal = causal;
+    cp.cls = pl.cls[0];
+    cp.o_part = p.o_part;
+    cp.lse_part = p.lse_part;
+    cp.out = out;
+    cp.lse = lse;
+    e = launch_combine(cp, st);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  }
+  return FP8PA_OK;
+}
+
+int fp8pa_get_device_status(unsigned int* host_status, fp8pa_stream_t stream) {
+  if (!host_status) return fail(FP8PA_EINVAL, "null host_status");
+  cudaError_t e = cudaMemcpyFromSymbolAsync(host_status, g_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost,
+                                            (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "status copy");
+  return FP8PA_OK;
+}
+
+int fp8pa_reset_device_status(fp8pa_stream_t stream) {
+  unsigned* p = status_ptr();
+  if (!p) return fail(FP8PA_ECUDA, "cannot resolve the device status word");
+  cudaError_t e = cudaMemsetAsync(p, 0, sizeof(unsigned), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "status reset");
+  return FP8PA_OK;
+}
+
+}  // extern "C"

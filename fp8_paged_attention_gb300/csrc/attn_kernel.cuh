@@ -1,0 +1,711 @@
+// Paged FP8-KV attention forward, sm_103a.
+//
+// One persistent CTA per SM walks a device-built list of work items (sequence,
+// KV head, tile of packed query rows, key split).  Per item the CTA streams the
+// item's 64-token K/V pages through shared memory and keeps the running output
+// in tensor memory:
+//
+//   S^T[key, row] = K[key, :] . Q[row, :]        tcgen05.mma, M = 128 keys, N = rows
+//   P = exp2(S * scale * log2 e - m)              online softmax, one thread per key
+//   O^T[d, row] += V[key, d]^T P^T[key, row]     tcgen05.mma, M = 128 dims, K = keys
+//
+// Rows pack (query token, query head of the KV group) pairs token-major, so GQA
+// shares every K/V page among all heads of its group and all query tokens of
+// the tile.  Keys sit on the 128 TMEM lanes; each softmax thread owns one key.
+//
+// Warp roles: warp 0 issues TMA loads (Q tile, then K/V page tiles in the
+// order the MMAs consume them), warp 1 allocates tensor memory and issues the
+// MMAs from one thread, warps 2-5 run the softmax, the O rescale and the
+// epilogue.  On the BF16-Q path warps 6-9 turn each E4M3 K/V stage into BF16
+// operand tiles (exact: every E4M3 value is a BF16 value).
+//
+// FP8 path (E4M3 Q): QK^T and PV are kind::f8f6f4 MMAs.  P is requantized to
+// E4M3 after a 2^8 pre-scale (P' = 2^(x - m + 8) in [0, 256], keeping small
+// weights out of E4M3's subnormal range) as a pair on one scale:
+// hi = e4m3(P'), lo = e4m3(P' - hi); both PV MMAs accumulate into the same
+// TMEM O, so P carries about 8 significant bits instead of E4M3's 4.  The row
+// sum accumulates hi + lo, so O / l is an exact convex combination of the V
+// rows the MMAs saw.  BF16 path: kind::f16 MMAs, P in BF16.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fp8pa {
+
+template <int D, bool kFP8, int N>
+struct AttnCfg {
+  static_assert(D == 256 || D == 512, "head dim");
+  static_assert(N == 16 || N == 32 || N == 64, "rows per tile");
+  static constexpr int kDC = D / 128;                    // 128-byte chunks of an E4M3 row
+  static constexpr int kQChunkElems = kFP8 ? 128 : 64;   // Q elements per 128-byte chunk
+  static constexpr int kQChunks = D / kQChunkElems;
+  static constexpr int kQBytes = kQChunks * N * 128;
+  // P^T for 128 keys: FP8 path = E4M3 hi term then E4M3 lo term (N x 128 bytes each)
+  static constexpr int kPBytes = kFP8 ? 2 * N * 128 : N * 256;
+  static constexpr int kBfSlotBytes = 32768;             // BF16 tile of 128 keys x 128 dims
+  static constexpr int kThreads = kFP8 ? 192 : 320;
+  static constexpr int kSmemLimit = 232448;              // opt-in maximum per block
+  // barriers (< 1 KB) + per-row softmax state: red[2][4][N], lred[4][N], 4 x [N] floats
+  static constexpr int kCtrlBytes = 1024 + 64 * N + 64;
+  static constexpr int kQBufs = kFP8 ? ((2 * kQBytes <= 65536) ? 2 : 1) : ((2 * kQBytes <= 32768) ? 2 : 1);
+  static constexpr int kBfSlots = kFP8 ? 0 : 2;
+  static constexpr int kFixed = kQBufs * kQBytes + 2 * kPBytes + kBfSlots * kBfSlotBytes + kCtrlBytes + 1024;
+  static constexpr int kStages = (kSmemLimit - kFixed) / kStageBytes > 16 ? 16 : (kSmemLimit - kFixed) / kStageBytes;
+  static_assert(kStages >= 2, "smem");
+  static constexpr int kSmemBytes = kFixed + kStages * kStageBytes;
+  static constexpr int kTmemUsed = 2 * N + kDC * N;
+  static constexpr uint32_t kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
+                                        : kTmemUsed <= 256 ? 256 : 512;
+  static constexpr float kPShift = kFP8 ? 8.0f : 0.0f;
+};
+
+namespace detail {
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Max over the warp; floats ordered through their sign-magnitude integer image.
+__device__ __forceinline__ float warp_max(float v) {
+  int i = __float_as_int(v);
+  int key = i >= 0 ? i : (i ^ 0x7FFFFFFF);
+  int r = __reduce_max_sync(0xFFFFFFFFu, key);
+  return __int_as_float(r >= 0 ? r : (r ^ 0x7FFFFFFF));
+}
+
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t res;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(res)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return res != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: gives up after `lim` rounds, after about two seconds of wall
+// clock, or once another role has flagged an abort.
+__device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, uint32_t lim, volatile int* abort_flag) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0; i < lim; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 31u) {
+      if (*abort_flag) return false;
+      const uint64_t t = global_ns();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > 2000000000ull) return false;
+    }
+  }
+  return false;
+}
+
+__device__ __forceinline__ void flag_timeout(const AttnParams& p, volatile int* abort_flag) {
+  *abort_flag = 1;
+  atomicOr(p.status, kDevTimeout);
+}
+
+// Physical page of logical page `pg`, or an out-of-range page id (the TMA then
+// fills zeros) for pages past the item's last visible key or bad table entries.
+__device__ __forceinline__ int page_id(const AttnParams& p, const Item& it, int pg) {
+  if (pg > it.hi_max / kPage) return p.num_pages;
+  int phys = p.block_table[(size_t)it.b * p.max_pages + pg];
+  if ((unsigned)phys >= (unsigned)p.num_pages) {
+    atomicOr(p.status, kDevBadPage);
+    return p.num_pages;
+  }
+  return phys;
+}
+
+__device__ __forceinline__ float load_descale(const float* d, const AttnParams& p, const Item& it) {
+  return d[(size_t)it.b * p.descale_b + (size_t)it.hk * p.descale_h];
+}
+
+// Stage position of V tile u (0-based within the item) in the item's stream
+// K(0), [K(1), V(0)], [K(2), V(1)], ..., [K(n-1), V(n-2)], V(n-1), in stages.
+__device__ __forceinline__ uint32_t v_stage_offset(int u, int n, int dc) {
+  return (u < n - 1) ? (uint32_t)(2 * (u + 1) * dc) : (uint32_t)((2 * n - 1) * dc);
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2_bf16x2(uint16_t v) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
+  float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+  __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+}  // namespace detail
+
+template <int D, bool kFP8, int N>
+__global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+  using C = AttnCfg<D, kFP8, N>;
+  using namespace ptx;
+  using namespace detail;
+  constexpr int S = C::kStages;
+  constexpr int SB = C::kBfSlots;
+  constexpr int SBm = SB > 0 ? SB : 1;  // modulus for the BF16 operand ring (unused on the FP8 path)
+  constexpr int QB = C::kQBufs;
+  constexpr int DC = C::kDC;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* ring = smem;
+  uint8_t* bfbuf = ring + S * kStageBytes;
+  uint8_t* qbuf = bfbuf + SB * C::kBfSlotBytes;
+  uint8_t* pbuf = qbuf + QB * C::kQBytes;
+  uint8_t* ctrl = pbuf + 2 * C::kPBytes;
+  uint64_t* ring_full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* ring_empty = ring_full + S;
+  uint64_t* bf_full = ring_empty + S;
+  uint64_t* bf_empty = bf_full + (SB > 0 ? SB : 1);
+  uint64_t* q_full = bf_empty + (SB > 0 ? SB : 1);
+  uint64_t* q_empty = q_full + QB;
+  uint64_t* s_full = q_empty + QB;
+  uint64_t* s_empty = s_full + 2;
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* o_empty = pv_done + 2;
+  uint64_t* drain = o_empty + 1;
+  float* red = reinterpret_cast<float*>(drain + 1);  // [2][4][N] per-warp tile maxima
+  float* lred = red + 2 * 4 * N;                      // [4][N] per-warp row sums
+  float* m_s = lred + 4 * N;                          // [N] running max (log2 units)
+  float* a_s = m_s + N;                               // [N] rescale factor of this tile
+  float* msub_s = a_s + N;                            // [N] exponent offset of this tile
+  float* l_s = msub_s + N;                            // [N] final row sums
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(l_s + N);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&ring_full[i], 1);
+      mbar_init(&ring_empty[i], kFP8 ? 1 : 4);
+    }
+    for (int i = 0; i < SB; ++i) {
+      mbar_init(&bf_full[i], 4);
+      mbar_init(&bf_empty[i], 1);
+    }
+    for (int i = 0; i < QB; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(o_empty, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_items = *p.work_count;
+  const uint32_t lim = p.wait_limit;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t idx = 0, qit = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const Item it = decode_item(p, p.work[w]);
+        if (it.t1 <= it.t0) continue;
+        const int qb = qit % QB;
+        if (!(ok = pwait(&q_empty[qb], ((qit / QB) & 1) ^ 1, lim, abort_flag))) break;
+        mbar_arrive_expect_tx(&q_full[qb], C::kQBytes);
+        for (int c = 0; c < C::kQChunks; ++c)
+          tma_load_3d(qbuf + qb * C::kQBytes + c * N * 128, &tm_q, &q_full[qb], c * C::kQChunkElems,
+                      it.hk * p.group, it.q0 + it.row0 / p.group);
+        ++qit;
+        const int n = it.t1 - it.t0;
+        auto load_tile = [&](int u, const CUtensorMap* tm) -> bool {
+          const int pg = it.pg_lo + 2 * (it.t0 + u);
+          const int pa = page_id(p, it, pg), pb = page_id(p, it, pg + 1);
+          for (int c = 0; c < DC; ++c) {
+            const uint32_t slot = idx % S;
+            if (!pwait(&ring_empty[slot], ((idx / S) & 1) ^ 1, lim, abort_flag)) return false;
+            mbar_arrive_expect_tx(&ring_full[slot], kStageBytes);
+            uint8_t* dst = ring + slot * kStageBytes;
+            tma_load_4d(dst, tm, &ring_full[slot], c * 128, it.hk, 0, pa);
+            tma_load_4d(dst + kStageBytes / 2, tm, &ring_full[slot], c * 128, it.hk, 0, pb);
+            ++idx;
+          }
+          return true;
+        };
+        ok = load_tile(0, &tm_k);
+        for (int u = 1; u <= n && ok; ++u) {
+          if (u < n) ok = load_tile(u, &tm_k);
+          if (ok) ok = load_tile(u - 1, &tm_v);
+        }
+      }
+      if (!ok) flag_timeout(p, abort_flag);
+      // drain: every issued copy must land before the CTA may exit
+      for (uint32_t j = idx > (uint32_t)S ? idx - S : 0; j < idx; ++j)
+        mbar_wait(&ring_full[j % S], (j / S) & 1, kDrainWaitLimit);
+      for (uint32_t j = qit > (uint32_t)QB ? qit - QB : 0; j < qit; ++j)
+        mbar_wait(&q_full[j % QB], (j / QB) & 1, kDrainWaitLimit);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kFmt = kFP8 ? kFmtE4M3 : kFmtBF16;
+      constexpr uint32_t idesc_qk = make_idesc(kFmt, kKMajor, kKMajor, 128, N);
+      constexpr uint32_t idesc_pv = make_idesc(kFmt, kMNMajor, kMNMajor, 128, N);
+      uint32_t idx = 0, g = 0, qit = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const Item it = decode_item(p, p.work[w]);
+        if (it.t1 <= it.t0) continue;
+        const int qb = qit % QB;
+        if (!(ok = pwait(&q_full[qb], (qit / QB) & 1, lim, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t qaddr = smem_u32(qbuf + qb * C::kQBytes);
+        // S^T(gg) = K . Q^T into S buffer gg & 1
+        auto qk = [&](uint32_t gg) -> bool {
+          const uint32_t sb = gg & 1;
+          if (!pwait(&s_empty[sb], ((gg >> 1) & 1) ^ 1, lim, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + sb * N;
+          for (int c = 0; c < DC; ++c) {
+            const uint32_t slot = idx % (kFP8 ? S : SBm);
+            if (kFP8) {
+              if (!pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag)) return false;
+              tc_fence_after();
+              const uint32_t a0 = smem_u32(ring + slot * kStageBytes), b0 = qaddr + c * N * 128;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8f6f4(d_tmem, make_sdesc(a0 + kk * 32, 16, 1024, kLayoutSW128),
+                           make_sdesc(b0 + kk * 32, 16, 1024, kLayoutSW128), idesc_qk, (c | kk) != 0);
+              mma_commit(&ring_empty[slot]);
+            } else {
+              if (!pwait(&bf_full[slot], (idx / SBm) & 1, lim, abort_flag)) return false;
+              tc_fence_after();
+              const uint32_t a0 = smem_u32(bfbuf + slot * C::kBfSlotBytes);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_f16(d_tmem, make_sdesc(a0 + h * 16384 + kk * 32, 16, 1024, kLayoutSW128),
+                          make_sdesc(qaddr + (2 * c + h) * N * 128 + kk * 32, 16, 1024, kLayoutSW128), idesc_qk,
+                          (c | h | kk) != 0);
+              mma_commit(&bf_empty[slot]);
+            }
+            ++idx;
+          }
+          mma_commit(&s_full[sb]);
+          return true;
+        };
+        // O^T += V^T . P^T(gg)
+        auto pv = [&](uint32_t gg, bool first) -> bool {
+          const uint32_t pb = gg & 1;
+          if (!pwait(&p_full[pb], (gg >> 1) & 1, lim, abort_flag)) return false;
+          if (first && !pwait(o_empty, ((qit - 1) & 1) ^ 1, lim, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t paddr = smem_u32(pbuf + pb * C::kPBytes);
+          for (int c = 0; c < DC; ++c) {
+            const uint32_t d_tmem = tmem + 2 * N + c * N;
+            const uint32_t slot = idx % (kFP8 ? S : SBm);
+            if (kFP8) {
+              if (!pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag)) return false;
+              tc_fence_after();
+              const uint32_t a0 = smem_u32(ring + slot * kStageBytes);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t va = make_sdesc(a0 + kk * 4096, 16384, 1024, kLayoutSW128);
+                mma_f8f6f4(d_tmem, va, make_sdesc(paddr + kk * 512, 128, 2048, kLayoutNone), idesc_pv,
+                           !(first && kk == 0));
+                mma_f8f6f4(d_tmem, va, make_sdesc(paddr + N * 128 + kk * 512, 128, 2048, kLayoutNone), idesc_pv, 1);
+              }
+              mma_commit(&ring_empty[slot]);
+            } else {
+              if (!pwait(&bf_full[slot], (idx / SBm) & 1, lim, abort_flag)) return false;
+              tc_fence_after();
+              const uint32_t a0 = smem_u32(bfbuf + slot * C::kBfSlotBytes);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_f16(d_tmem, make_sdesc(a0 + kk * 2048, 16384, 1024, kLayoutSW128),
+                        make_sdesc(paddr + kk * 256, 128, 2048, kLayoutNone), idesc_pv, !(first && kk == 0));
+              mma_commit(&bf_empty[slot]);
+            }
+            ++idx;
+          }
+          mma_commit(&pv_done[pb]);
+          return true;
+        };
+        ++qit;  // pv() reads qit - 1 as this item's ordinal
+        const int n = it.t1 - it.t0;
+        ok = qk(g);
+        for (int u = 0; u < n && ok; ++u) {
+          if (u + 1 < n) ok = qk(g + u + 1);
+          if (!ok) break;
+          if (u + 1 == n) mma_commit(&q_empty[qb]);
+          ok = pv(g + u, u == 0);
+        }
+        g += n;
+      }
+      if (!ok) flag_timeout(p, abort_flag);
+      mma_commit(drain);
+      mbar_wait(drain, 0, kDrainWaitLimit);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------------ softmax / correction / epilogue
+    const int wt = threadIdx.x - 64;        // 0..127
+    const int quarter = warp & 3;           // TMEM lane quarter this warp may access
+    const int kl = quarter * 32 + lane;     // key (S) or head-dim (O) lane within the tile
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const float NEG_INF = __int_as_float(0xFF800000);
+    uint32_t g = 0, sbase = 0;
+    bool aborted = false;
+    for (int w = blockIdx.x; w < n_items && !aborted; w += gridDim.x) {
+      const Item it = decode_item(p, p.work[w]);
+      const int G = p.group;
+      const bool split_out = it.nsplit > 1;
+      auto row_tok = [&](int n) { return it.q0 + (it.row0 + n) / G; };
+      auto row_head = [&](int n) { return it.hk * G + (it.row0 + n) % G; };
+      if (it.t1 <= it.t0) {
+        // nothing visible: out = 0, lse = -inf
+        for (int n = 0; n < it.nrows; ++n) {
+          const size_t r = (size_t)row_tok(n) * p.hq + row_head(n);
+          for (int d = wt; d < D; d += 128) {
+            if (split_out)
+              p.o_part[((size_t)it.split * p.total_q * p.hq + r) * D + d] = 0.f;
+            else
+              reinterpret_cast<__nv_bfloat16*>(p.out)[r * D + d] = __float2bfloat16_rn(0.f);
+          }
+        }
+        if (wt < it.nrows) {
+          const size_t li = (size_t)row_head(wt) * p.total_q + row_tok(wt);
+          if (split_out)
+            p.lse_part[(size_t)it.split * p.hq * p.total_q + li] = NEG_INF;
+          else if (p.lse)
+            p.lse[li] = NEG_INF;
+        }
+        continue;
+      }
+      const int n_t = it.t1 - it.t0;
+      const float kd = load_descale(p.k_descale, p, it);
+      const float vd = load_descale(p.v_descale, p, it);
+      const float scale = p.softmax_scale_log2 * kd * (kFP8 ? *p.q_descale : 1.0f);
+      if (wt < N) m_s[wt] = NEG_INF;
+      float lt[N];
+#pragma unroll
+      for (int n = 0; n < N; ++n) lt[n] = 0.f;
+
+      for (int u = 0; u < n_t; ++u, ++g) {
+        const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
+        const int j = kb + kl;
+        const uint32_t sb = g & 1;
+        bool ok = pwait(&s_full[sb], (g >> 1) & 1, lim, abort_flag);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        float x[N];
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < N; c += 16) {
+            uint32_t r[16];
+            tmem_load16(tmem + lane_base + sb * N + c, r);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(r[i]) * scale;
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[sb]);
+          const bool interior = kb >= it.lo_max && kb + kTileKeys - 1 <= it.hi_min;
+          if (!interior) {
+#pragma unroll
+            for (int n = 0; n < N; ++n) {
+              int lo, hi;
+              visible_range(it.Lq, it.Lk, (it.row0 + n) / G, p.window_left, p.causal, lo, hi);
+              if (j < lo || j > hi) x[n] = NEG_INF;
+            }
+          }
+#pragma unroll
+          for (int n = 0; n < N; ++n)
+            if (n >= it.nrows) x[n] = NEG_INF;
+          float* rb = red + (g & 1) * 4 * N + quarter * N;
+#pragma unroll
+          for (int n = 0; n < N; ++n) {
+            const float mx = warp_max(x[n]);
+            if (lane == (n & 31)) rb[n] = mx;
+          }
+        } else {
+          flag_timeout(p, abort_flag);
+        }
+        if (bar_red_or(1, 128, !ok)) {
+          aborted = true;
+          break;
+        }
+        // row owners fold the four warp maxima into the running max
+        bool resc = false;
+        if (wt < N) {
+          const float* rr = red + (g & 1) * 4 * N;
+          const float tmax = fmaxf(fmaxf(rr[wt], rr[N + wt]), fmaxf(rr[2 * N + wt], rr[3 * N + wt]));
+          const float mo = m_s[wt];
+          const float mn = fmaxf(mo, tmax);
+          const float alpha = (mo == mn) ? 1.0f : ex2(mo - mn);
+          m_s[wt] = mn;
+          a_s[wt] = alpha;
+          msub_s[wt] = (mn == NEG_INF ? 0.0f : mn) - C::kPShift;
+          resc = alpha != 1.0f;
+        }
+        const bool rescale = bar_red_or(2, 128, resc);
+        // P = 2^(x - m + shift), quantized; thread-partial row sums of the quantized values
+        const uint32_t pb = g & 1;
+        ok = true;
+        if (g >= 2) ok = pwait(&pv_done[pb], ((g >> 1) - 1) & 1, lim, abort_flag);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (ok) {
+          uint8_t* pdst = pbuf + pb * C::kPBytes;
+          if (kFP8) {
+#pragma unroll
+            for (int blk = 0; blk < N / 16; ++blk) {
+              uint32_t hi_w[4], lo_w[4];
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t hw = 0, lw = 0;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                  const int n0 = blk * 16 + q4 * 4 + h2 * 2;
+                  const float p0 = ex2(x[n0] - msub_s[n0]);
+                  const float p1 = ex2(x[n0 + 1] - msub_s[n0 + 1]);
+                  const __nv_fp8x2_storage_t h8 =
+                      __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
+                  __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h8, __NV_E4M3);
+                  const float2 hv = __half22float2(*reinterpret_cast<__half2*>(&hr));
+                  // residuals are exact in f32 (p and hv agree in their leading bits)
+                  const __nv_fp8x2_storage_t l8 =
+                      __nv_cvt_float2_to_fp8x2(make_float2(p0 - hv.x, p1 - hv.y), __NV_SATFINITE, __NV_E4M3);
+                  __half2_raw lr = __nv_cvt_fp8x2_to_halfraw2(l8, __NV_E4M3);
+                  const float2 lv = __half22float2(*reinterpret_cast<__half2*>(&lr));
+                  if (rescale) {
+                    lt[n0] *= a_s[n0];
+                    lt[n0 + 1] *= a_s[n0 + 1];
+                  }
+                  lt[n0] += hv.x + lv.x;
+                  lt[n0 + 1] += hv.y + lv.y;
+                  hw |= (uint32_t)h8 << (16 * h2);
+                  lw |= (uint32_t)l8 << (16 * h2);
+                }
+                hi_w[q4] = hw;
+                lo_w[q4] = lw;
+              }
+              *reinterpret_cast<uint4*>(pdst + blk * 2048 + kl * 16) = make_uint4(hi_w[0], hi_w[1], hi_w[2], hi_w[3]);
+              *reinterpret_cast<uint4*>(pdst + N * 128 + blk * 2048 + kl * 16) =
+                  make_uint4(lo_w[0], lo_w[1], lo_w[2], lo_w[3]);
+            }
+          } else {
+#pragma unroll
+            for (int blk = 0; blk < N / 8; ++blk) {
+              uint32_t packed[4];
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const int n0 = blk * 8 + q4 * 2;
+                const float p0 = ex2(x[n0] - msub_s[n0]);
+                const float p1 = ex2(x[n0 + 1] - msub_s[n0 + 1]);
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+                const float2 back = __bfloat1622float2(b2);
+                if (rescale) {
+                  lt[n0] *= a_s[n0];
+                  lt[n0 + 1] *= a_s[n0 + 1];
+                }
+                lt[n0] += back.x;
+                lt[n0 + 1] += back.y;
+                packed[q4] = *reinterpret_cast<uint32_t*>(&b2);
+              }
+              *reinterpret_cast<uint4*>(pdst + blk * 2048 + kl * 16) =
+                  make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            }
+          }
+          // rows of the last page past the sequence end may hold anything (even NaN):
+          // zero those V rows so that 0 * V stays 0 in the PV MMA
+          if (kFP8 && kb + kTileKeys > it.Lk) {
+            const int zr = max(0, it.Lk - kb);
+            for (int c = 0; c < DC && ok; ++c) {
+              const uint32_t vi = sbase + v_stage_offset(u, n_t, DC) + c;
+              ok = pwait(&ring_full[vi % S], (vi / S) & 1, lim, abort_flag);
+              ok = __all_sync(0xFFFFFFFFu, ok);
+              if (ok) {
+                uint8_t* st = ring + (vi % S) * kStageBytes;
+                for (int x16 = zr * 8 + wt; x16 < kTileKeys * 8; x16 += 128)
+                  *reinterpret_cast<uint4*>(st + x16 * 16) = make_uint4(0, 0, 0, 0);
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          // rescale the running O when a row max grew (not needed on an item's first tile)
+          if (ok && rescale && u > 0) {
+            ok = pwait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, lim, abort_flag);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (ok) {
+              tc_fence_after();
+#pragma unroll
+              for (int c = 0; c < DC; ++c) {
+#pragma unroll
+                for (int cc = 0; cc < N; cc += 16) {
+                  uint32_t r[16];
+                  const uint32_t ta = tmem + lane_base + 2 * N + c * N + cc;
+                  tmem_load16(ta, r);
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a_s[cc + i]);
+                  tmem_store16(ta, r);
+                }
+              }
+            }
+          }
+        }
+        if (!ok) flag_timeout(p, abort_flag);
+        if (bar_red_or(1, 128, !ok)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[pb]);
+      }
+      if (aborted) break;
+      sbase += 2 * n_t * DC;
+      // ---------------- epilogue: O / l, lse
+      bool ok = pwait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, lim, abort_flag);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+#pragma unroll
+      for (int n = 0; n < N; ++n) {
+        float v = lt[n];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        if (lane == (n & 31)) lred[quarter * N + n] = v;
+      }
+      if (!ok) flag_timeout(p, abort_flag);
+      if (bar_red_or(1, 128, !ok)) {
+        aborted = true;
+        break;
+      }
+      if (wt < N) l_s[wt] = (lred[wt] + lred[N + wt]) + (lred[2 * N + wt] + lred[3 * N + wt]);
+      named_bar_sync(2, 128);
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < DC; ++c) {
+        const int d = c * 128 + kl;
+#pragma unroll
+        for (int cc = 0; cc < N; cc += 16) {
+          uint32_t r[16];
+          tmem_load16(tmem + lane_base + 2 * N + c * N + cc, r);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = cc + i;
+            if (n < it.nrows) {
+              const float l = l_s[n];
+              const float o = l > 0.f ? __uint_as_float(r[i]) / l * vd : 0.f;
+              const size_t row = (size_t)row_tok(n) * p.hq + row_head(n);
+              if (split_out)
+                p.o_part[((size_t)it.split * p.total_q * p.hq + row) * D + d] = o;
+              else
+                reinterpret_cast<__nv_bfloat16*>(p.out)[row * D + d] = __float2bfloat16_rn(o);
+            }
+          }
+        }
+      }
+      if (wt < it.nrows) {
+        const float l = l_s[wt];
+        const float lse = l > 0.f ? (m_s[wt] - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+        const size_t li = (size_t)row_head(wt) * p.total_q + row_tok(wt);
+        if (split_out)
+          p.lse_part[(size_t)it.split * p.hq * p.total_q + li] = lse;
+        else if (p.lse)
+          p.lse[li] = lse;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty);
+    }
+  } else {
+    // ------------------------------------------------------------------ E4M3 -> BF16 operand tiles (BF16-Q path)
+    if (!kFP8) {
+      const int dt = threadIdx.x - 192;  // 0..127
+      uint32_t idx = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const Item it = decode_item(p, p.work[w]);
+        if (it.t1 <= it.t0) continue;
+        const int n = it.t1 - it.t0;
+        auto convert_tile = [&](int u, bool is_v) -> bool {
+          const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
+          const int zero_from = (is_v && kb + kTileKeys > it.Lk) ? max(0, it.Lk - kb) : kTileKeys;
+          for (int c = 0; c < DC; ++c) {
+            const uint32_t slot = idx % S, bslot = idx % SBm;
+            bool w_ok = pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag) &&
+                        pwait(&bf_empty[bslot], ((idx / SBm) & 1) ^ 1, lim, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, w_ok)) return false;
+            const uint8_t* src = ring + slot * kStageBytes;
+            uint8_t* dst = bfbuf + bslot * C::kBfSlotBytes;
+            for (int x16 = dt; x16 < kTileKeys * 8; x16 += 128) {
+              const int row = x16 >> 3, c16 = x16 & 7, sw = row & 7;
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if (row < zero_from) v = *reinterpret_cast<const uint4*>(src + row * 128 + ((c16 ^ sw) << 4));
+              const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+              uint32_t o[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                o[2 * i] = cvt_e4m3x2_bf16x2((uint16_t)(in[i] & 0xFFFF));
+                o[2 * i + 1] = cvt_e4m3x2_bf16x2((uint16_t)(in[i] >> 16));
+              }
+              const int h = c16 >> 2, k0 = (c16 & 3) * 2;
+              uint8_t* drow = dst + h * 16384 + row * 128;
+              *reinterpret_cast<uint4*>(drow + ((k0 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(drow + (((k0 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(&ring_empty[slot]);
+              mbar_arrive(&bf_full[bslot]);
+            }
+            ++idx;
+          }
+          return true;
+        };
+        ok = convert_tile(0, false);
+        for (int u = 1; u <= n && ok; ++u) {
+          if (u < n) ok = convert_tile(u, false);
+          if (ok) ok = convert_tile(u - 1, true);
+        }
+      }
+      if (!ok) flag_timeout(p, abort_flag);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace fp8pa

@@ -1,0 +1,20 @@
+// Launch helper for one attention kernel variant.
+#pragma once
+#include "attn_kernel.cuh"
+#include "kernels.h"
+
+namespace fp8pa {
+
+template <int D, bool kFP8, int N>
+cudaError_t launch_attn_variant(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, int grid, cudaStream_t stream) {
+  using C = AttnCfg<D, kFP8, N>;
+  // the attribute is per device; setting it again is cheap and capture-safe
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kFP8, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  attn_fwd_kernel<D, kFP8, N><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p, tm_q, tm_k, tm_v);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8pa

@@ -1,0 +1,129 @@
+// Definitions shared by the plan, attention and combine kernels: launch
+// parameters, the work-item format and the per-item key ranges.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp8pa {
+
+constexpr int kPage = 64;          // tokens per KV-cache page
+constexpr int kTileKeys = 128;     // keys per MMA tile: two pages, the MMA's M dimension
+constexpr int kStageBytes = 16384; // one TMA stage: 128 keys x 128 bytes of head dim
+constexpr uint32_t kDefaultWaitLimit = 1u << 22;
+constexpr uint32_t kDrainWaitLimit = 1u << 22;
+
+enum : unsigned { kDevBadPage = 1, kDevTimeout = 2, kDevBadLength = 4 };
+
+// One sequence class of a launch: sequences whose Lq lies in [lq_min, lq_max]
+// are cut into row tiles of `rows` (query token, head-in-group) rows.
+struct ClassInfo {
+  int lq_min, lq_max;
+  int rows;        // N: rows per tile (multiple of 16)
+  int max_splits;  // split-KV count cap for single-row-tile sequences
+};
+
+struct AttnParams {
+  // problem
+  const int32_t* block_table;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seqused_k;
+  const float* q_descale;
+  const float* k_descale;
+  const float* v_descale;
+  int descale_b, descale_h;
+  int batch, total_q, hq, hkv, group, head_dim;
+  int max_pages, num_pages;
+  float softmax_scale_log2;  // softmax_scale * log2(e)
+  int window_left, causal;
+  // outputs
+  void* out;        // bf16 [total_q][hq][D]
+  float* lse;       // [hq][total_q] or null
+  float* o_part;    // f32 [splits][total_q][hq][D]
+  float* lse_part;  // f32 [splits][hq][total_q]
+  // plan
+  ClassInfo cls;
+  const int4* work;        // items of this class
+  const int* work_count;   // number of items
+  unsigned* status;
+  uint32_t wait_limit;
+};
+
+// Visible key range of query i of a sequence (Lq queries, Lk keys); hi < lo when empty.
+__host__ __device__ __forceinline__ void visible_range(int Lq, int Lk, int i, int window_left, int causal, int& lo,
+                                                       int& hi) {
+  int p = Lk - Lq + i;
+  lo = window_left >= 0 ? max(0, p - window_left) : 0;
+  hi = causal ? min(p, Lk - 1) : Lk - 1;
+}
+
+// Number of key splits of a sequence in a class: only single-row-tile
+// sequences split, and never into more splits than 128-key tiles.
+__host__ __device__ __forceinline__ int seq_splits(int Lq, int Lk, int group, int window_left, int causal,
+                                                   const ClassInfo& c) {
+  if (Lq * group > c.rows || c.max_splits <= 1 || Lk <= 0) return 1;
+  int lo0, hi0, lo1, hi1;
+  visible_range(Lq, Lk, 0, window_left, causal, lo0, hi0);
+  visible_range(Lq, Lk, Lq - 1, window_left, causal, lo1, hi1);
+  if (hi1 < lo0) return 1;
+  int pages = hi1 / kPage - lo0 / kPage + 1;
+  int tiles = (pages + 1) / 2;
+  return max(1, min(c.max_splits, tiles));
+}
+
+__host__ __device__ __forceinline__ int seq_row_tiles(int Lq, int group, int rows) {
+  return (Lq * group + rows - 1) / rows;
+}
+
+// Everything a CTA needs to know about one work item.
+struct Item {
+  int b, rt, hk, split, nsplit;
+  int q0, Lq, Lk;
+  int row0, nrows;       // first packed row of the tile, valid rows (<= N)
+  int pg_lo;             // first logical page of the tile's key union
+  int t0, t1;            // 128-key tiles [t0, t1) of this split; tile t starts at key (pg_lo + 2t) * 64
+  int lo_max, hi_min;    // keys in [lo_max, hi_min] are visible to every valid row
+  int hi_max;            // last key visible to any row (for tail sanitation)
+};
+
+// Work item encoding: {b, row_tile, hk | split << 16, nsplit}.
+__device__ __forceinline__ Item decode_item(const AttnParams& p, int4 w) {
+  Item it;
+  it.b = w.x;
+  it.rt = w.y;
+  it.hk = w.z & 0xFFFF;
+  it.split = w.z >> 16;
+  it.nsplit = w.w;
+  it.q0 = p.cu_seqlens_q[it.b];
+  it.Lq = p.cu_seqlens_q[it.b + 1] - it.q0;
+  int lk = p.seqused_k[it.b];
+  int lk_cap = p.max_pages * kPage;
+  if (lk < 0 || lk > lk_cap) {
+    atomicOr(p.status, kDevBadLength);
+    lk = lk < 0 ? 0 : lk_cap;
+  }
+  it.Lk = lk;
+  const int N = p.cls.rows;
+  it.row0 = it.rt * N;
+  it.nrows = min(N, it.Lq * p.group - it.row0);
+  int i_first = it.row0 / p.group;
+  int i_last = (it.row0 + it.nrows - 1) / p.group;
+  int lo_f, hi_f, lo_l, hi_l;
+  visible_range(it.Lq, it.Lk, i_first, p.window_left, p.causal, lo_f, hi_f);
+  visible_range(it.Lq, it.Lk, i_last, p.window_left, p.causal, lo_l, hi_l);
+  it.lo_max = lo_l;
+  it.hi_min = hi_f;
+  it.hi_max = hi_l;
+  if (it.Lk <= 0 || hi_l < lo_f || hi_l < 0) {
+    it.pg_lo = 0;
+    it.t0 = it.t1 = 0;
+    return it;
+  }
+  it.pg_lo = lo_f / kPage;
+  int pages = hi_l / kPage - it.pg_lo + 1;
+  int tiles = (pages + 1) / 2;
+  it.t0 = (int)((long long)it.split * tiles / it.nsplit);
+  it.t1 = (int)((long long)(it.split + 1) * tiles / it.nsplit);
+  return it;
+}
+
+}  // namespace fp8pa

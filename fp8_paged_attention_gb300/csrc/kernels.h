@@ -1,0 +1,45 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace fp8pa {
+
+struct PlanParams {
+  const int32_t* cu_seqlens_q;
+  const int32_t* seqused_k;
+  int batch, total_q, group, hkv, max_pages, window_left, causal;
+  int num_classes;
+  ClassInfo cls[2];
+  int4* work[2];
+  int* counts;  // [2]
+  unsigned* status;
+};
+
+struct CombineParams {
+  const int32_t* cu_seqlens_q;
+  const int32_t* seqused_k;
+  int batch, total_q, hq, group, head_dim, max_pages, window_left, causal;
+  ClassInfo cls;
+  const float* o_part;
+  const float* lse_part;
+  void* out;
+  float* lse;
+};
+
+cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& cp, cudaStream_t stream);
+cudaError_t launch_quantize_q(const void* q_bf16, void* q_e4m3, const float* q_descale, long long n,
+                              cudaStream_t stream);
+
+// Attention kernel launchers, one per (head dim, Q type, rows per tile).
+// `grid` CTAs, each persistent over the class's work list.
+cudaError_t launch_attn(int head_dim, bool fp8_q, int rows, const AttnParams& p, const CUtensorMap& tm_q,
+                        const CUtensorMap& tm_k, const CUtensorMap& tm_v, int grid, cudaStream_t stream);
+
+// Shared-memory bytes of a kernel variant (0 if the variant does not exist).
+int attn_smem_bytes(int head_dim, bool fp8_q, int rows);
+
+}  // namespace fp8pa

@@ -1,0 +1,168 @@
+/*
+ * fp8pa — attention forward over a paged FP8 E4M3 KV cache, for GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer argument is a DEVICE pointer owned by the caller unless
+ * stated otherwise; no call allocates device memory, synchronizes the stream or
+ * reads device memory from the host, so every call can be captured in a CUDA
+ * graph.  All work is enqueued on the caller's stream.  Functions return an
+ * fp8pa_status; on a non-zero status nothing was launched and
+ * fp8pa_last_error() gives a message naming the offending argument (dtype,
+ * head size, ...).
+ *
+ * Sources.  The operation is the one the Gemma-4 FP8-KV attention paths in
+ * vLLM compute:
+ *  - "[Kernel] Integrate FA4 SM90 FP8 MMA for Gemma-4 full attention" (vLLM PR
+ *    60372), Overview: head-dim-512 full attention with FP8 KV storage and
+ *    native BF16 Q, FP8 MMA in-kernel; review thread: 64-token pages
+ *    (page_size == tile_n == 64), splits chosen automatically with no
+ *    CUDA-graph cap, unsupported combinations rejected before launch.
+ *  - vLLM PR 63139, Overview: sliding-window layers at head dim 256 quantize Q
+ *    to FP8 and run a native FP8 (E4M3 Q/K/V) forward.
+ *  - vLLM PR 48666 summary (prhub), flash_attn_varlen_func snippet: paged FP8
+ *    E4M3 K/V dequantized in-kernel with the K/V descales folded in, BF16 Q,
+ *    output written in the native dtype, (batch, num_kv_heads) f32 descales,
+ *    softmax_lse returned.
+ */
+#ifndef FP8PA_H_
+#define FP8PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (0 = legacy default stream). */
+typedef struct CUstream_st* fp8pa_stream_t;
+
+typedef enum {
+  FP8PA_OK = 0,
+  FP8PA_EINVAL = 1,        /* bad argument: null pointer, size, alignment, workspace too small */
+  FP8PA_EUNSUPPORTED = 2,  /* valid but unsupported combination (head dim, Q dtype, ...) */
+  FP8PA_ECUDA = 3,         /* a CUDA runtime call failed (message has the CUDA error) */
+  FP8PA_EDEVICE = 4        /* returned by fp8pa_get_device_status when device flags are set */
+} fp8pa_status;
+
+typedef enum { FP8PA_BF16 = 0, FP8PA_E4M3 = 1 } fp8pa_dtype;
+
+/* Bits of the device status word (see fp8pa_get_device_status). */
+enum {
+  FP8PA_DEV_BAD_PAGE = 1,   /* a block-table entry outside [0, num_pages): that page read as zeros */
+  FP8PA_DEV_TIMEOUT = 2,    /* a bounded pipeline wait ran out; the kernel stopped early */
+  FP8PA_DEV_BAD_LENGTH = 4  /* seqused_k[b] > 64 * max_pages_per_seq or < 0: clamped */
+};
+
+/* Tokens per KV-cache page.  Fixed: the cache is laid out in 64-token pages
+ * (PR 60372 review thread: page_size == tile_n == 64). */
+#define FP8PA_PAGE_SIZE 64
+
+/*
+ * quantize_q_fp8 — Q to E4M3 (PR 63139, Overview: sliding-window layers
+ * quantize Q to FP8).
+ *   q_e4m3[i] = RNE_saturate_e4m3( fl32( float(q_bf16[i]) / *q_descale ) )
+ * i.e. an IEEE fp32 division, then round-to-nearest-even onto E4M3 with
+ * saturation to +-448 (also for +-inf); NaN gives 0x7F with the input's sign
+ * bit.  q_bf16: n_elems bf16 values; q_e4m3: n_elems bytes; q_descale: one
+ * f32 on the device (per tensor).  Any layout (the op is elementwise).
+ * Errors: EINVAL for null pointers or n_elems < 0.  n_elems == 0 is a no-op.
+ */
+int quantize_q_fp8(const void* q_bf16, void* q_e4m3, const float* q_descale, long long n_elems,
+                   fp8pa_stream_t stream);
+
+/*
+ * fp8pa_workspace_size — bytes of device workspace fp8_paged_attn_fwd needs for
+ * these host-known sizes (same values as passed to fp8_paged_attn_fwd).  The
+ * workspace holds the device-built work list and, when the split count is
+ * above 1, the per-split partial outputs and log-sum-exps.  Returns 0 for
+ * arguments fp8_paged_attn_fwd would reject.
+ */
+size_t fp8pa_workspace_size(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv,
+                            int head_dim, int max_pages_per_seq, int window_left, int num_splits);
+
+/*
+ * fp8pa_num_splits — the split-KV count fp8_paged_attn_fwd uses for these
+ * host-known sizes (num_splits = 0 asks for the automatic choice, which is a
+ * pure function of its arguments and the SM count, so it is CUDA-graph safe).
+ * Returns 0 for arguments fp8_paged_attn_fwd would reject.
+ */
+int fp8pa_num_splits(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
+                     int max_pages_per_seq, int window_left, int num_splits);
+
+/*
+ * fp8_paged_attn_fwd — varlen attention forward over a paged E4M3 KV cache.
+ *
+ * Layouts (row-major, innermost last):
+ *   q            [total_q][num_heads_q][head_dim]   bf16 (q_dtype = FP8PA_BF16) or
+ *                                                    E4M3 bytes (FP8PA_E4M3, e.g. from quantize_q_fp8)
+ *   k_cache,
+ *   v_cache      [num_pages][64][num_heads_kv][head_dim] E4M3 bytes
+ *   block_table  [batch][max_pages_per_seq] int32: physical page of logical page j of sequence b
+ *   cu_seqlens_q [batch + 1] int32, nondecreasing, cu_seqlens_q[0] = 0, cu_seqlens_q[batch] = total_q
+ *   seqused_k    [batch] int32: keys of sequence b, including its new tokens (already written)
+ *   out          [total_q][num_heads_q][head_dim] bf16
+ *   lse          [num_heads_q][total_q] f32, natural log; may be NULL
+ *
+ * Semantics, per sequence b with Lq = cu_seqlens_q[b+1] - cu_seqlens_q[b] and
+ * Lk = seqused_k[b], query i (0 <= i < Lq) at position p = Lk - Lq + i and
+ * query head h on KV head hk = h / (num_heads_q / num_heads_kv):
+ *   visible keys J = [lo, hi], lo = max(0, p - window_left) if window_left >= 0 else 0,
+ *                               hi = min(p, Lk - 1) if causal else Lk - 1
+ *   s_j = softmax_scale * (q . k_j),  with q = code * q_descale (E4M3 Q) or the bf16 value,
+ *         k_j = code * k_descale[b, hk]
+ *   out = sum_j softmax(s)_j * v_j,   v_j = code * v_descale[b, hk];  lse = ln sum_j exp(s_j)
+ *   An empty J gives out = 0 and lse = -inf.
+ * q_descale: one f32 (per tensor; read only on the E4M3-Q path).  k_descale,
+ * v_descale: f32 read at b * descale_batch_stride + hk * descale_head_stride
+ * (0, 0 = per tensor).
+ *
+ * Support: head_dim 256 with E4M3 Q; head_dim 512 with BF16 Q (K/V dequantized
+ * in-kernel, BF16 MMA) or E4M3 Q (FP8 MMA).  V head dim = head_dim.  num_heads_q
+ * a multiple of num_heads_kv with a group size in {1, 2, 4, 8, 16}.
+ * window_left >= -1.  num_splits: 0 = automatic, else the maximum number of
+ * key splits per (sequence, KV head); splits are combined by log-sum-exp.
+ * Pointers q, k_cache, v_cache, out must be 16-byte aligned.
+ *
+ * workspace: device buffer of at least fp8pa_workspace_size(...) bytes, 256-byte
+ * aligned; contents need not be initialized and are scratch after the call.
+ *
+ * Device-side faults are reported, not trapped: a block-table entry outside
+ * [0, num_pages) reads that page as zeros and sets FP8PA_DEV_BAD_PAGE; see
+ * fp8pa_get_device_status.
+ */
+int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* v_cache, int num_pages,
+                       const int32_t* block_table, int max_pages_per_seq, const int32_t* cu_seqlens_q,
+                       const int32_t* seqused_k, int batch, int total_q, int max_seqlen_q, int num_heads_q,
+                       int num_heads_kv, int head_dim, const float* q_descale, const float* k_descale,
+                       const float* v_descale, int descale_batch_stride, int descale_head_stride,
+                       float softmax_scale, int window_left, int causal, int num_splits, void* workspace,
+                       size_t workspace_bytes, void* out, float* lse, fp8pa_stream_t stream);
+
+/*
+ * fp8pa_get_device_status — enqueue on `stream` a copy of the current device's
+ * status word (FP8PA_DEV_* bits accumulated by earlier launches) into
+ * *host_status, which must be pinned host memory; the value is valid once the
+ * stream has reached this point.  Returns OK or ECUDA.
+ */
+int fp8pa_get_device_status(unsigned int* host_status, fp8pa_stream_t stream);
+
+/* fp8pa_reset_device_status — enqueue a clear of the current device's status word. */
+int fp8pa_reset_device_status(fp8pa_stream_t stream);
+
+/* fp8pa_last_error — message for the last non-OK status returned on this host thread. */
+const char* fp8pa_last_error(void);
+
+/*
+ * fp8pa_set_wait_limit — test hook.  Sets the iteration cap of every bounded
+ * pipeline wait in later launches (0 restores the default).  A tiny cap makes
+ * waits run out, which exercises the timeout path: the kernel sets
+ * FP8PA_DEV_TIMEOUT, drains its own copies and MMAs, frees its tensor memory
+ * and returns; results of that launch are undefined.
+ */
+void fp8pa_set_wait_limit(unsigned int max_iterations);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8PA_H_ */

@@ -1,0 +1,92 @@
+"""Host-side tests of the C ABI: the library loads, exports every declared
+entry point, and rejects bad arguments before touching the GPU; workspace and
+split sizing are pure functions of host-known sizes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_paged_attention_gb300 as fp8pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    txt = open(os.path.join(ROOT, "include", "fp8pa.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|void|const char\*)\s+(\w+)\s*\(", txt, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = fp8pa.load_library()
+    names = _declared_functions()
+    assert {"fp8_paged_attn_fwd", "quantize_q_fp8", "fp8pa_workspace_size"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def _fwd(**kw):
+    lib = fp8pa.load_library()
+    a = dict(q=16, q_dtype=1, k=16, v=16, num_pages=4, bt=16, max_pages=4, cu=16, su=16, batch=2, total_q=2,
+             max_seqlen_q=1, hq=32, hkv=16, d=256, qd=16, kd=16, vd=16, sb=0, sh=0, scale=0.0625, wl=-1,
+             causal=1, splits=0, ws=256, ws_bytes=1 << 30, out=16, lse=0, stream=0)
+    a.update(kw)
+    return lib.fp8_paged_attn_fwd(*a.values())
+
+
+@pytest.mark.parametrize("kw,code,needle", [
+    (dict(d=128), 2, "head_dim 128"),
+    (dict(d=256, q_dtype=0), 2, "bfloat16"),
+    (dict(q_dtype=7), 1, "q_dtype"),
+    (dict(hq=30, hkv=16), 2, "multiple"),
+    (dict(hq=96, hkv=3), 2, "per KV head"),
+    (dict(batch=-1), 1, ">= 0"),
+    (dict(wl=-2), 1, "window_left"),
+    (dict(splits=-1), 1, "num_splits"),
+    (dict(max_pages=0), 1, "max_pages"),
+    (dict(causal=2), 1, "causal"),
+    (dict(q=0), 1, "null"),
+    (dict(k=8), 1, "aligned"),
+    (dict(ws_bytes=16), 1, "workspace too small"),
+    (dict(ws=128), 1, "256-byte"),
+    (dict(scale=float("inf")), 1, "finite"),
+    (dict(sb=-1), 1, "strides"),
+    (dict(num_pages=0), 1, "num_pages"),
+])
+def test_fwd_rejects_bad_arguments_before_launch(kw, code, needle):
+    rc = _fwd(**kw)
+    assert rc == code
+    assert needle in fp8pa.load_library().fp8pa_last_error().decode()
+
+
+def test_empty_batch_is_a_noop():
+    assert _fwd(batch=0, total_q=0, max_seqlen_q=0) == 0
+
+
+def test_quantize_rejects_bad_arguments():
+    lib = fp8pa.load_library()
+    assert lib.quantize_q_fp8(16, 16, 16, -1, 0) == 1
+    assert lib.quantize_q_fp8(0, 16, 16, 8, 0) == 1
+    assert lib.quantize_q_fp8(0, 0, 0, 0, 0) == 0
+
+
+def test_workspace_and_splits_are_host_functions():
+    # SWA decode: 64 x 1 query, Hq 32 / Hkv 16, D 256, window 1023, 144 pages
+    ws = fp8pa.workspace_size(64, 64, 1, 32, 16, 256, 144, 1023, 0)
+    s = fp8pa.num_splits(64, 64, 1, 32, 16, 256, 144, 1023, 0)
+    assert ws > 0 and 1 <= s <= 64
+    assert ws == fp8pa.workspace_size(64, 64, 1, 32, 16, 256, 144, 1023, 0)
+    # explicit split count is honoured and grows the workspace by the partial buffers
+    w1 = fp8pa.workspace_size(64, 64, 1, 32, 4, 512, 144, -1, 1)
+    w4 = fp8pa.workspace_size(64, 64, 1, 32, 4, 512, 144, -1, 4)
+    assert fp8pa.num_splits(64, 64, 1, 32, 4, 512, 144, -1, 4) == 4
+    assert w4 - w1 >= 4 * 64 * 32 * 512 * 4
+    # a long full-attention decode batch with few (sequence, head) units gets split
+    assert fp8pa.num_splits(64, 64, 1, 32, 4, 512, 144, -1, 0) > 1
+    # the mixed chunked-prefill batch has plenty of units: no split
+    assert fp8pa.num_splits(4033, 8128, 4096, 32, 16, 256, 128, 1023, 0) == 1
+    # rejected shapes size to 0
+    assert fp8pa.workspace_size(1, 1, 1, 32, 16, 128, 4, -1, 0) == 0
+    assert fp8pa.num_splits(1, 1, 1, 30, 16, 256, 4, -1, 0) == 0

@@ -1,0 +1,157 @@
+"""GPU attention vs the fp64 oracle on small and edge-case inputs that span
+several 128-key tiles, ragged tails, every row class (decode, verify,
+prefill, chunked prefill), windows, empty rows, splits and permuted pages."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.helpers import LSE_GATE, TOL, bf16_bits, lse_error, oracle_problem, unit_scale_errors
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(w, num_splits=0, q8=None, **kw):
+    import fp8_paged_attention_gb300 as fp8pa
+    dev = w.k_cache.device
+    qd = torch.tensor([w.q_descale], dtype=torch.float32, device=dev)
+    kd = kw.pop("k_descale", torch.tensor([w.k_descale], dtype=torch.float32, device=dev))
+    vd = kw.pop("v_descale", torch.tensor([w.v_descale], dtype=torch.float32, device=dev))
+    q = w.q
+    if w.fp8_q:
+        q = q8 if q8 is not None else fp8pa.quantize_q_fp8(w.q, qd)
+    out, lse = fp8pa.fp8_paged_attn_fwd(q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q, w.seqused_k,
+                                        w.max_seqlen_q, qd, kd, vd, w.softmax_scale, w.window_left, w.causal,
+                                        num_splits=num_splits, **kw)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def check(w, out, lse, ref=None, prob=None):
+    if ref is None:
+        ref = oracle.paged_attention(prob if prob is not None else oracle_problem(w))
+    ro, rl = ref
+    g = out.float().cpu().numpy()
+    e = unit_scale_errors(g, ro, w)
+    le = lse_error(lse.cpu().numpy(), rl)
+    tmax, tmean = TOL[w.fp8_q]
+    assert np.isfinite(g).all()
+    assert e["max"] <= tmax and e["mean"] <= tmean, (w.name, e, le)
+    assert le <= LSE_GATE, (w.name, le)
+    return e, le
+
+
+def make(name, lq, lk, hq, hkv, d, wl, causal, fp8, seed=0, **kw):
+    return synth.make_workload(name, lq, lk, hq, hkv, d, wl, causal, fp8, seed=seed, device="cuda", **kw)
+
+
+def test_tiny_prefill_config():
+    w = synth.make_config("tiny_prefill_hd256", device="cuda")
+    out, lse = run_gpu(w)
+    check(w, out, lse)
+
+
+CASES = [
+    # name, lq, lk, hq, hkv, d, window_left, causal, fp8
+    ("prefill_ragged_hd256", [1, 63, 64, 65, 130, 200], [1, 63, 64, 65, 130, 200], 4, 2, 256, -1, True, True),
+    ("prefill_window_hd256", [150, 300], [150, 300], 4, 2, 256, 63, True, True),
+    ("chunked_hd256", [37, 100, 1], [300, 300, 5], 8, 4, 256, 100, True, True),
+    ("decode_swa_hd256", [1] * 9, [1, 2, 63, 64, 65, 1024, 1100, 1500, 2000], 32, 16, 256, 1023, True, True),
+    ("decode_hd512_bf16", [1] * 7, [1, 64, 129, 700, 1000, 2000, 3000], 32, 4, 512, -1, True, False),
+    ("decode_hd512_fp8", [1] * 7, [1, 64, 129, 700, 1000, 2000, 3000], 32, 4, 512, -1, True, True),
+    ("verify_hd512_bf16", [4] * 5, [4, 65, 300, 1000, 2000], 32, 4, 512, -1, True, False),
+    ("verify_hd512_fp8", [4] * 5, [4, 65, 300, 1000, 2000], 32, 4, 512, -1, True, True),
+    ("prefill_hd512_bf16", [3, 70, 129], [3, 70, 300], 16, 2, 512, -1, True, False),
+    ("prefill_hd512_fp8", [3, 70, 129], [3, 70, 300], 16, 2, 512, -1, True, True),
+    ("noncausal_window_hd256", [3, 70], [200, 70], 4, 2, 256, 50, False, True),
+    ("noncausal_hd512_bf16", [2, 40], [300, 40], 8, 1, 512, -1, False, False),
+    ("mha_group1_hd256", [5, 1], [77, 300], 2, 2, 256, -1, True, True),
+    ("group16_hd512", [1, 2], [500, 130], 16, 1, 512, -1, True, False),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_attention_cases(case):
+    name, lq, lk, hq, hkv, d, wl, causal, fp8 = case
+    w = make(name, lq, lk, hq, hkv, d, wl, causal, fp8, seed=len(name))
+    out, lse = run_gpu(w)
+    check(w, out, lse)
+
+
+def test_empty_rows_and_sequences():
+    # seq 0: 5 queries on 3 keys (the first two see nothing); seq 1: no keys; seq 2: no queries
+    w = make("empty", [5, 2, 0, 1], [3, 0, 10, 9], 4, 2, 256, -1, True, True)
+    out, lse = run_gpu(w)
+    ro, rl = oracle.paged_attention(oracle_problem(w))
+    g = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    for t in (0, 1, 5, 6):
+        assert np.all(g[t] == 0) and np.all(l[:, t] == -np.inf)
+    check(w, out, lse, ref=(ro, rl))
+
+
+@pytest.mark.parametrize("fp8", [True, False])
+def test_explicit_splits_agree_and_repeat_bit_identically(fp8):
+    w = make("splits", [1] * 5 + [4], [3000, 2500, 700, 64, 1, 2000], 32, 4, 512, -1, True, fp8, seed=3)
+    ref = oracle.paged_attention(oracle_problem(w))
+    for s in (1, 2, 3, 7):
+        out, lse = run_gpu(w, num_splits=s)
+        check(w, out, lse, ref=ref)
+        out2, lse2 = run_gpu(w, num_splits=s)
+        assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_page_permutation_is_bit_identical():
+    w = make("perm", [1, 1, 3, 40], [900, 1500, 700, 300], 32, 16, 256, 1023, True, True, seed=11)
+    out1, lse1 = run_gpu(w)
+    n = w.num_pages
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(5)).to("cuda")
+    kc = torch.empty_like(w.k_cache)
+    vc = torch.empty_like(w.v_cache)
+    kc[perm] = w.k_cache
+    vc[perm] = w.v_cache
+    bt = perm.to(torch.int32)[w.block_table.long()]
+    w2 = synth.Workload(**{**w.__dict__, "k_cache": kc, "v_cache": vc, "block_table": bt.contiguous()})
+    out2, lse2 = run_gpu(w2)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+def test_per_batch_head_descales():
+    w = make("descale", [1, 2, 1], [500, 300, 900], 8, 2, 256, 200, True, True, seed=9)
+    kd = torch.tensor([[w.k_descale, w.k_descale * 0.5], [w.k_descale * 2, w.k_descale],
+                       [w.k_descale, w.k_descale * 1.5]], dtype=torch.float32, device="cuda")
+    vd = torch.tensor([[w.v_descale, w.v_descale * 2], [w.v_descale * 0.25, w.v_descale],
+                       [w.v_descale * 3, w.v_descale]], dtype=torch.float32, device="cuda")
+    out, lse = run_gpu(w, k_descale=kd.reshape(-1), v_descale=vd.reshape(-1), descale_batch_stride=2,
+                       descale_head_stride=1)
+    prob = oracle_problem(w, k_descale=kd.cpu().numpy().ravel(), v_descale=vd.cpu().numpy().ravel(),
+                          descale_batch_stride=2, descale_head_stride=1)
+    ro, rl = oracle.paged_attention(prob)
+    # outputs scale with v_descale: compare on the scale of each sequence's V
+    g = out.float().cpu().numpy()
+    tok_seq = np.repeat(np.arange(3), w.lq)
+    G = 4
+    for t in range(w.total_q):
+        for h in range(8):
+            s = w.v_channel_scale[h // G] * float(vd[tok_seq[t], h // G] / w.v_descale)
+            assert np.max(np.abs(g[t, h] - ro[t, h]) / s) <= TOL[True][0]
+    assert lse_error(lse.cpu().numpy(), rl) <= LSE_GATE
+
+
+def test_bad_page_id_sets_status_and_reads_zeros():
+    import fp8_paged_attention_gb300 as fp8pa
+    w = make("badpage", [1, 1], [200, 300], 8, 4, 256, -1, True, True, seed=4)
+    bt = w.block_table.clone()
+    bt[1, 2] = 1 << 20
+    fp8pa.reset_device_status()
+    out, lse = run_gpu(synth.Workload(**{**w.__dict__, "block_table": bt}))
+    st = fp8pa.get_device_status()
+    assert st & fp8pa.DEV_BAD_PAGE
+    assert torch.isfinite(out.float()).all()
+    # sequence 0 is untouched by the bad entry
+    ro, rl = oracle.paged_attention(oracle_problem(w))
+    e = unit_scale_errors(out.float().cpu().numpy()[:1], ro[:1], w)
+    assert e["max"] <= TOL[True][0]
+    fp8pa.reset_device_status()
+    assert fp8pa.get_device_status() == 0

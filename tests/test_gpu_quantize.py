@@ -1,0 +1,38 @@
+"""quantize_q_fp8 on the GPU is bit-exact against the oracle quantizer over
+every bf16 bit pattern (normals, subnormals, +-0, +-inf, NaNs) and descales
+that exercise ties, saturation and underflow."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("descale", [1.0, 3.7 / 448, 2.0 ** -10, 1000.0, 0.0123456, 1.0 / 3.0])
+def test_quantize_all_bf16_patterns_bit_exact(descale):
+    import fp8_paged_attention_gb300 as fp8pa
+    bits = np.arange(65536, dtype=np.uint16)
+    q = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    d = torch.tensor([descale], dtype=torch.float32, device="cuda")
+    got = fp8pa.quantize_q_fp8(q, d).cpu().numpy()
+    want = oracle.quantize_q(bits, float(np.float32(descale)))
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(hex(int(bits[i])), hex(int(got[i])), hex(int(want[i]))) for i in bad[:10]]
+
+
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 1000, 4097])
+def test_quantize_ragged_lengths_and_unaligned(n):
+    import fp8_paged_attention_gb300 as fp8pa
+    rng = np.random.default_rng(n)
+    x = torch.from_numpy(rng.standard_normal(n + 3).astype(np.float32)).to(torch.bfloat16).cuda()
+    d = torch.tensor([0.01], dtype=torch.float32, device="cuda")
+    for off in (0, 1):  # offset 1 forces the unaligned scalar path
+        src = x[off:off + n]
+        out = torch.full((n + 1,), 0xAA, dtype=torch.uint8, device="cuda")
+        fp8pa.quantize_q_fp8(src.contiguous() if off == 0 else src, d, out=out[off:off + n])
+        want = oracle.quantize_q(src.cpu().view(torch.int16).numpy().view(np.uint16), 0.01)
+        assert np.array_equal(out[off:off + n].cpu().numpy(), want)
+        if off == 0:
+            assert out[n].item() == 0xAA   # no write past the end
