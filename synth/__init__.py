@@ -61,6 +61,7 @@ class Workload:
     bt: np.ndarray
     poison_page: int
     seed: int
+    v_channel_scale: np.ndarray  # [Hkv, D]: 1 or 8, the scale each V channel was drawn with
 
     @property
     def batch(self) -> int:
@@ -245,7 +246,7 @@ def make_workload(name: str, lq: Sequence[int], lk: Sequence[int], num_heads_q: 
         cu_seqlens_q=torch.from_numpy(cu).to(device), seqused_k=torch.from_numpy(lk.copy()).to(device),
         num_heads_q=num_heads_q, num_heads_kv=num_heads_kv, head_dim=head_dim,
         softmax_scale=float(np.float32(1.0 / math.sqrt(head_dim))), window_left=window_left, causal=causal,
-        fp8_q=fp8_q, lq=lq, lk=lk, bt=bt, poison_page=poison_page, seed=seed)
+        fp8_q=fp8_q, lq=lq, lk=lk, bt=bt, poison_page=poison_page, seed=seed, v_channel_scale=v_scale)
 
 
 # ------------------------------------------------------------------ named workloads
