@@ -1,0 +1,398 @@
+#!/usr/bin/env python3
+"""Benchmark of paged FP8 attention on GB300.
+
+One step = one pass of the whole hot path over one batch: Q -> E4M3 (FP8-MMA
+workloads), the device-side plan, the attention kernel(s) and the split-KV
+combine, through the library's C ABI.  Inputs are resident in HBM when the
+timed region starts.  The metric is KV-cache bytes read per second
+(algorithmic bytes: the K and V rows of every (sequence, KV head) visible
+key range, counted once), the decode roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica of the workload on its own GPU (the attention op has no exchange
+step), the timed region is bracketed by barriers and the slowest rank's time
+is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+DEFAULT_CONFIG = "swa_decode_hd256"
+METRIC = "paged FP8 attn: prefill TFLOP/s & decode KV GB/s, % of GB300 roofline"
+KERNEL_SOURCES = ["attn_kernel.cuh", "common.cuh", "ptx.cuh", "attn_launch.cuh"]
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]), source="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "fp8_paged_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(config)
+        if e and e.get("kernel_source_sha") == kernel_source_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    try:
+                        sm.append(float(parts[1]))
+                        smax = max(smax, float(parts[2]))
+                    except ValueError:
+                        continue
+                    for n, v in zip(names, parts[5:9]):
+                        if v.lower() == "active":
+                            reasons.add(n)
+            os.unlink(self.path)
+        except Exception:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def unit_bytes_of(w: synth.Workload, units):
+    """Algorithmic K+V bytes of a set of (sequence, kv-head) units."""
+    total = 0
+    for b, _hk in units:
+        span = synth._seq_visible_span(int(w.lq[b]), int(w.lk[b]), w.window_left, w.causal)
+        if span is not None:
+            total += (span[1] - span[0] + 1) * w.head_dim * 2
+    return total
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+
+def oracle_timing(w: synth.Workload, budget_s: float, seed: int = 0):
+    """Time the oracle on a bounded sample of (sequence, kv-head) units of the
+    workload (every query row and head of each unit).  Returns (GB/s, cores,
+    description, seconds)."""
+    import oracle  # test/benchmark infrastructure only
+    rng = np.random.default_rng(seed)
+    G = w.num_heads_q // w.num_heads_kv
+    units_all = [(b, hk) for b in range(w.batch) if w.lq[b] > 0 for hk in range(w.num_heads_kv)]
+    order = rng.permutation(len(units_all))
+    cu = np.zeros(w.batch + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(w.lq)
+
+    def run(units):
+        seqs = sorted({b for b, _ in units})
+        sub = synth.subproblem_pages(w, seqs)
+        q = sub["q"]
+        if w.fp8_q:
+            q = oracle.quantize_q(q, w.q_descale)
+        prob = oracle.AttnProblem(q, w.fp8_q, sub["k"], sub["v"], sub["block_table"], sub["cu_seqlens_q"],
+                                  sub["seqused_k"], w.num_heads_kv, w.q_descale, w.k_descale, w.v_descale,
+                                  w.softmax_scale, w.window_left, w.causal)
+        local = {b: i for i, b in enumerate(seqs)}
+        rows = []
+        for b, hk in units:
+            i = local[b]
+            for t in range(sub["cu_seqlens_q"][i], sub["cu_seqlens_q"][i + 1]):
+                for g in range(G):
+                    rows.append((t, hk * G + g))
+        rows = np.array(rows, dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.paged_attention(prob, rows=rows)
+        return time.perf_counter() - t0
+
+    # pilot on a few units, then size the sample to the budget
+    n = min(len(units_all), 8)
+    pilot = [units_all[i] for i in order[:n]]
+    t = run(pilot)
+    rate = unit_bytes_of(w, pilot) / max(t, 1e-9)
+    want = budget_s * rate
+    units, acc = [], 0
+    for i in order:
+        units.append(units_all[i])
+        acc += unit_bytes_of(w, [units_all[i]])
+        if acc >= want:
+            break
+    t = run(units)
+    gbs = unit_bytes_of(w, units) / t / 1e9
+    cores = os.cpu_count() or 1
+    desc = (f"{len(units)} of {len(units_all)} (sequence, KV head) units of {w.name}, every query row and head; "
+            f"{unit_bytes_of(w, units) / 1e6:.1f} MB of algorithmic KV bytes in {t:.2f} s")
+    return gbs, cores, desc, t
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = synth.make_config(args.config, device=dev)
+    total_steps = args.steps + args.warmup
+    per_step = max(0.05, min(30.0, 150.0 / max(1, total_steps)))
+    vals, cores, desc = [], 1, ""
+    t_all = 0.0
+    for i in range(total_steps):
+        gbs, cores, desc, t = oracle_timing(w, per_step, seed=i)
+        if i >= args.warmup:
+            vals.append(gbs)
+            t_all += t
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_all / max(1, len(vals)), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": "per step: " + desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ GPU leg
+
+def run_ours(args):
+    rank, local_rank, world = dist_env()
+    import fp8_paged_attention_gb300 as fp8pa  # the CUDA library; raises if it cannot load
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+    w = synth.make_config(args.config, device=dev)
+    stream = torch.cuda.current_stream()
+    qd = torch.tensor([w.q_descale], dtype=torch.float32, device=dev)
+    kd = torch.tensor([w.k_descale], dtype=torch.float32, device=dev)
+    vd = torch.tensor([w.v_descale], dtype=torch.float32, device=dev)
+    hq, hkv, D = w.num_heads_q, w.num_heads_kv, w.head_dim
+    max_pages = w.block_table.shape[1]
+    ws_bytes = fp8pa.workspace_size(w.batch, w.total_q, w.max_seqlen_q, hq, hkv, D, max_pages, w.window_left, 0)
+    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty((w.total_q, hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((hq, w.total_q), dtype=torch.float32, device=dev)
+    q8 = torch.empty((w.total_q, hq, D), dtype=torch.uint8, device=dev)
+    splits = fp8pa.num_splits(w.batch, w.total_q, w.max_seqlen_q, hq, hkv, D, max_pages, w.window_left, 0)
+    launches = fp8pa.kernel_launches(w.batch, w.total_q, w.max_seqlen_q, hq, hkv, D, max_pages, w.window_left, 0)
+    launches += 1 if w.fp8_q else 0
+
+    def step(q_src, bt, cu, su, o, l):
+        q = fp8pa.quantize_q_fp8(q_src, qd, out=q8) if w.fp8_q else q_src
+        fp8pa.fp8_paged_attn_fwd(q, w.k_cache, w.v_cache, bt, cu, su, w.max_seqlen_q, qd, kd, vd,
+                                 w.softmax_scale, w.window_left, w.causal, num_splits=0, out=o, lse=l,
+                                 workspace=workspace)
+
+    args_dev = (w.q, w.block_table, w.cu_seqlens_q, w.seqused_k, out, lse)
+    for _ in range(args.warmup):
+        step(*args_dev)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---------------- device-resident timed region
+    k_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    k_stop = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in k_start + k_stop:
+        e.record(stream)  # torch creates the CUDA event on first record; the library re-records it
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for i in range(args.steps):
+        fp8pa.set_timing_events(k_start[i], k_stop[i])
+        step(*args_dev)
+    fp8pa.set_timing_events(None, None)
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clock_info = clocks.stop()
+    ms_total = t_start.elapsed_time(t_stop)
+    k_ms = [a.elapsed_time(b) for a, b in zip(k_start, k_stop)]
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    kv_bytes = w.kv_bytes_algorithmic()
+    value = world * kv_bytes * args.steps / (ms_total * 1e-3) / 1e9
+    peaks = measured_peaks()
+    k_avg_ms = sum(k_ms) / len(k_ms)
+    achieved = kv_bytes / (k_avg_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(w.name),
+                "kernel": "attn_fwd_kernel", "kernel_ms": round(k_avg_ms, 5),
+                "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}
+
+    # ---------------- end to end through the public API, host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        h_q, h_bt, h_cu, h_su = pin(w.q), pin(w.block_table), pin(w.cu_seqlens_q), pin(w.seqused_k)
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        d_q, d_bt, d_cu, d_su = (torch.empty_like(w.q), torch.empty_like(w.block_table),
+                                 torch.empty_like(w.cu_seqlens_q), torch.empty_like(w.seqused_k))
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_bt, h_cu, h_su))
+        d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+        def e2e_step():
+            d_q.copy_(h_q, non_blocking=True)
+            d_bt.copy_(h_bt, non_blocking=True)
+            d_cu.copy_(h_cu, non_blocking=True)
+            d_su.copy_(h_su, non_blocking=True)
+            step(d_q, d_bt, d_cu, d_su, out, lse)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+
+        for _ in range(max(3, args.warmup // 4)):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(10, args.steps // 4)
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(world * kv_bytes * n_e2e / (e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
+               "ms_per_step": round(e_ms / n_e2e, 5),
+               "note": "K/V cache is resident state; per step Q, block table and lengths go up, out and lse come back"}
+
+    # ---------------- CPU oracle baseline (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, cores, desc, _t = oracle_timing(w, budget_s=args.cpu_budget)
+        cpu = {"value": round(gbs, 5), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3" if w.fp8_q else "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "total_q": w.total_q, "num_heads_q": hq,
+                       "num_heads_kv": hkv, "head_dim": D, "window_left": w.window_left, "causal": w.causal,
+                       "q": "e4m3" if w.fp8_q else "bf16", "kv": "e4m3, 64-token pages", "num_splits": splits,
+                       "kv_bytes_per_step": kv_bytes, "parallelism": f"replicas x{world}",
+                       "l2": f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB of visible KV per step"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches * args.steps,
+            "clocks": clock_info,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=synth.CONFIG_NAMES)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

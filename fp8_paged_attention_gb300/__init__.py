@@ -18,7 +18,8 @@ from . import _build
 
 __all__ = [
     "build", "load_library", "library_path", "quantize_q_fp8", "fp8_paged_attn_fwd", "workspace_size",
-    "num_splits", "get_device_status", "reset_device_status", "set_wait_limit", "FP8PA_BF16", "FP8PA_E4M3",
+    "num_splits", "kernel_launches", "set_timing_events", "get_device_status", "reset_device_status",
+    "set_wait_limit", "FP8PA_BF16", "FP8PA_E4M3",
     "DEV_BAD_PAGE", "DEV_TIMEOUT", "DEV_BAD_LENGTH", "PAGE_SIZE", "Fp8paError",
 ]
 
@@ -79,6 +80,10 @@ def load_library():
         lib.fp8pa_last_error.argtypes = []
         lib.fp8pa_set_wait_limit.restype = None
         lib.fp8pa_set_wait_limit.argtypes = [c.c_uint]
+        lib.fp8pa_kernel_launches.restype = c.c_int
+        lib.fp8pa_kernel_launches.argtypes = [c.c_int] * 9
+        lib.fp8pa_set_timing_events.restype = None
+        lib.fp8pa_set_timing_events.argtypes = [c.c_void_p, c.c_void_p]
         _lib = lib
         return lib
 
@@ -109,6 +114,25 @@ def num_splits(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim
                window_left=-1, num_splits=0) -> int:
     return int(load_library().fp8pa_num_splits(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim,
                                                max_pages_per_seq, window_left, num_splits))
+
+
+def kernel_launches(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq,
+                    window_left=-1, num_splits=0) -> int:
+    """Kernels one fp8_paged_attn_fwd call launches for these sizes."""
+    return int(load_library().fp8pa_kernel_launches(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv,
+                                                    head_dim, max_pages_per_seq, window_left, num_splits))
+
+
+def set_timing_events(start=None, stop=None):
+    """Profiling hook: record torch.cuda.Event `start`/`stop` around the
+    attention kernels of later calls on this thread (None, None: off)."""
+    lib = load_library()
+    if start is None or stop is None:
+        lib.fp8pa_set_timing_events(None, None)
+    else:
+        if not start.cuda_event or not stop.cuda_event:
+            raise ValueError("record the events once before passing them (torch creates them lazily)")
+        lib.fp8pa_set_timing_events(start.cuda_event, stop.cuda_event)
 
 
 def quantize_q_fp8(q: torch.Tensor, q_descale: torch.Tensor, out: torch.Tensor | None = None, stream=None):

@@ -47,6 +47,7 @@ namespace {
 __device__ unsigned int g_status;
 
 thread_local char g_err[512] = "";
+thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
 std::atomic<unsigned> g_wait_limit{0};
 
 int fail(int code, const char* fmt, ...) {
@@ -142,7 +143,7 @@ int check_shape(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int h
   if (max_pages < 1) return fail(FP8PA_EINVAL, "max_pages_per_seq must be >= 1");
   if ((long long)max_pages * kPage > 0x7FFFFFFFLL) return fail(FP8PA_EINVAL, "max_pages_per_seq too large");
   if (window_left < -1) return fail(FP8PA_EINVAL, "window_left must be >= -1 (got %d)", window_left);
-  if (num_splits < 0 || num_splits > 256) return fail(FP8PA_EINVAL, "num_splits must be in [0, 256] (got %d)", num_splits);
+  if (num_splits < 0 || num_splits > 64) return fail(FP8PA_EINVAL, "num_splits must be in [0, 64] (got %d)", num_splits);
   if ((long long)total_q * hq > 0x7FFFFFFFLL) return fail(FP8PA_EINVAL, "total_q * num_heads_q too large");
   return FP8PA_OK;
 }
@@ -225,6 +226,25 @@ extern "C" {
 const char* fp8pa_last_error(void) { return g_err; }
 
 void fp8pa_set_wait_limit(unsigned int max_iterations) { g_wait_limit.store(max_iterations); }
+
+void fp8pa_set_timing_events(void* start_event, void* stop_event) {
+  g_ev_start = static_cast<cudaEvent_t>(start_event);
+  g_ev_stop = static_cast<cudaEvent_t>(stop_event);
+}
+
+int fp8pa_kernel_launches(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
+                          int max_pages_per_seq, int window_left, int num_splits) {
+  CallPlan pl;
+  if (make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq, window_left,
+                num_splits, pl))
+    return 0;
+  if (batch == 0 || total_q == 0) return 0;
+  int n = 1;  // plan
+  for (int k = 0; k < pl.num_classes; ++k)
+    if (pl.cls[k].lq_max >= pl.cls[k].lq_min) ++n;
+  if (pl.splits > 1) ++n;
+  return n;
+}
 
 int quantize_q_fp8(const void* q_bf16, void* q_e4m3, const float* q_descale, long long n_elems,
                    fp8pa_stream_t stream) {
@@ -362,6 +382,8 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
   p.status = status;
   const unsigned wl = g_wait_limit.load();
   p.wait_limit = wl ? wl : kDefaultWaitLimit;
+  const bool timed = g_ev_start && g_ev_stop;
+  if (timed && (e = cudaEventRecord(g_ev_start, st)) != cudaSuccess) return cuda_fail(e, "timing event");
   for (int k = 0; k < pl.num_classes; ++k) {
     if (pl.cls[k].lq_max < pl.cls[k].lq_min) continue;
     p.cls = pl.cls[k];
@@ -371,6 +393,7 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
     e = launch_attn(head_dim, fp8_q, pl.cls[k].rows, p, tm_q[k], tm_k, tm_v, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   }
+  if (timed && (e = cudaEventRecord(g_ev_stop, st)) != cudaSuccess) return cuda_fail(e, "timing event");
   if (pl.splits > 1) {
     CombineParams cp{};
     cp.cu_seqlens_q = cu_seqlens_q;

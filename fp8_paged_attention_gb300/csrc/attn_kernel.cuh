@@ -20,8 +20,9 @@
 // operand tiles (exact: every E4M3 value is a BF16 value).
 //
 // FP8 path (E4M3 Q): QK^T and PV are kind::f8f6f4 MMAs.  P is requantized to
-// E4M3 after a 2^8 pre-scale (P' = 2^(x - m + 8) in [0, 256], keeping small
-// weights out of E4M3's subnormal range) as a pair on one scale:
+// E4M3 after a 2^4 pre-scale (P' = 2^(x - m + 4), at most 256 under the lazy
+// rescale below, keeping small weights out of E4M3's subnormal range) as a
+// pair on one scale:
 // hi = e4m3(P'), lo = e4m3(P' - hi); both PV MMAs accumulate into the same
 // TMEM O, so P carries about 8 significant bits instead of E4M3's 4.  The row
 // sum accumulates hi + lo, so O / l is an exact convex combination of the V
@@ -61,7 +62,12 @@ struct AttnCfg {
   static constexpr int kTmemUsed = 2 * N + kDC * N;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
                                         : kTmemUsed <= 256 ? 256 : 512;
-  static constexpr float kPShift = kFP8 ? 8.0f : 0.0f;
+  // Lazy rescaling: the running max used for the exponent only moves when a
+  // row's max grows by more than kTau (log2 units), so most tiles need no O
+  // rescale.  P' = 2^(x - m_used + kPShift) <= 2^(kTau + kPShift) stays within
+  // E4M3's range (<= 256 < 448) and keeps small weights out of its subnormals.
+  static constexpr float kTau = kFP8 ? 4.0f : 8.0f;
+  static constexpr float kPShift = kFP8 ? 4.0f : 0.0f;
 };
 
 namespace detail {
@@ -391,6 +397,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
       auto row_head = [&](int n) { return it.hk * G + (it.row0 + n) % G; };
       if (it.t1 <= it.t0) {
         // nothing visible: out = 0, lse = -inf
+#pragma unroll 1
         for (int n = 0; n < it.nrows; ++n) {
           const size_t r = (size_t)row_tok(n) * p.hq + row_head(n);
           for (int d = wt; d < D; d += 128) {
@@ -439,10 +446,14 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
           if (lane == 0) mbar_arrive(&s_empty[sb]);
           const bool interior = kb >= it.lo_max && kb + kTileKeys - 1 <= it.hi_min;
           if (!interior) {
+            // query i sits at p = Lk - Lq + i; rows n and n' share a token when n / G == n' / G
+            const int lg = __ffs(G) - 1;
+            const int p0 = it.Lk - it.Lq + (it.row0 >> lg);
 #pragma unroll
             for (int n = 0; n < N; ++n) {
-              int lo, hi;
-              visible_range(it.Lq, it.Lk, (it.row0 + n) / G, p.window_left, p.causal, lo, hi);
+              const int pn = p0 + (n >> lg);
+              const int lo = p.window_left >= 0 ? max(0, pn - p.window_left) : 0;
+              const int hi = p.causal ? min(pn, it.Lk - 1) : it.Lk - 1;
               if (j < lo || j > hi) x[n] = NEG_INF;
             }
           }
@@ -468,8 +479,12 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
           const float* rr = red + (g & 1) * 4 * N;
           const float tmax = fmaxf(fmaxf(rr[wt], rr[N + wt]), fmaxf(rr[2 * N + wt], rr[3 * N + wt]));
           const float mo = m_s[wt];
-          const float mn = fmaxf(mo, tmax);
-          const float alpha = (mo == mn) ? 1.0f : ex2(mo - mn);
+          float mn = mo, alpha = 1.0f;
+          if (tmax > mo + C::kTau) {
+            mn = tmax;
+            // a row that has seen no key yet has O = 0 and l = 0: nothing to rescale
+            if (mo != NEG_INF) alpha = ex2(mo - mn);
+          }
           m_s[wt] = mn;
           a_s[wt] = alpha;
           msub_s[wt] = (mn == NEG_INF ? 0.0f : mn) - C::kPShift;
@@ -547,6 +562,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
           // zero those V rows so that 0 * V stays 0 in the PV MMA
           if (kFP8 && kb + kTileKeys > it.Lk) {
             const int zr = max(0, it.Lk - kb);
+#pragma unroll 1
             for (int c = 0; c < DC && ok; ++c) {
               const uint32_t vi = sbase + v_stage_offset(u, n_t, DC) + c;
               ok = pwait(&ring_full[vi % S], (vi / S) & 1, lim, abort_flag);
@@ -565,7 +581,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (ok) {
               tc_fence_after();
-#pragma unroll
+#pragma unroll 1
               for (int c = 0; c < DC; ++c) {
 #pragma unroll
                 for (int cc = 0; cc < N; cc += 16) {
@@ -609,7 +625,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
       if (wt < N) l_s[wt] = (lred[wt] + lred[N + wt]) + (lred[2 * N + wt] + lred[3 * N + wt]);
       named_bar_sync(2, 128);
       tc_fence_after();
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < DC; ++c) {
         const int d = c * 128 + kl;
 #pragma unroll
@@ -664,10 +680,18 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
             if (!__all_sync(0xFFFFFFFFu, w_ok)) return false;
             const uint8_t* src = ring + slot * kStageBytes;
             uint8_t* dst = bfbuf + bslot * C::kBfSlotBytes;
-            for (int x16 = dt; x16 < kTileKeys * 8; x16 += 128) {
+            uint4 vin[8];
+#pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8) {
+              const int x16 = dt + k8 * 128, row = x16 >> 3, c16 = x16 & 7;
+              vin[k8] = row < zero_from ? *reinterpret_cast<const uint4*>(src + row * 128 + ((c16 ^ (row & 7)) << 4))
+                                        : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8) {
+              const int x16 = dt + k8 * 128;
               const int row = x16 >> 3, c16 = x16 & 7, sw = row & 7;
-              uint4 v = make_uint4(0, 0, 0, 0);
-              if (row < zero_from) v = *reinterpret_cast<const uint4*>(src + row * 128 + ((c16 ^ sw) << 4));
+              const uint4 v = vin[k8];
               const uint32_t in[4] = {v.x, v.y, v.z, v.w};
               uint32_t o[8];
 #pragma unroll

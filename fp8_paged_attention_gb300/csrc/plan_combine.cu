@@ -87,8 +87,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
   }
 }
 
-__global__ void __launch_bounds__(128) combine_kernel(CombineParams cp) {
-  const int t = blockIdx.x;
+constexpr int kCombineWarps = 8;
+
+// One warp per (token, head) row: lane s holds split s's log-sum-exp, the
+// weights exp(lse_s - L) are formed once, then the warp sums the partial rows
+// with 16-byte loads.
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(CombineParams cp) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  if (row >= (long long)cp.total_q * cp.hq) return;
+  const int t = (int)(row / cp.hq), h = (int)(row % cp.hq);
   // sequence of token t: largest b with cu_seqlens_q[b] <= t
   int lo = 0, hi = cp.batch - 1, b = 0;
   while (lo <= hi) {
@@ -109,25 +117,43 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineParams cp) {
   if (ns <= 1) return;
   const float NEG_INF = __int_as_float(0xFF800000);
   const size_t plane = (size_t)cp.total_q * cp.hq;
-  for (int h = 0; h < cp.hq; ++h) {
-    float mx = NEG_INF;
-    for (int s = 0; s < ns; ++s) mx = fmaxf(mx, cp.lse_part[(size_t)s * plane + (size_t)h * cp.total_q + t]);
-    float sum = 0.f;
-    if (mx != NEG_INF)
-      for (int s = 0; s < ns; ++s) sum += expf(cp.lse_part[(size_t)s * plane + (size_t)h * cp.total_q + t] - mx);
-    const float L = (mx == NEG_INF) ? NEG_INF : mx + logf(sum);
-    const size_t row = (size_t)t * cp.hq + h;
-    for (int d = threadIdx.x; d < cp.head_dim; d += blockDim.x) {
-      float o = 0.f;
-      if (L != NEG_INF)
-        for (int s = 0; s < ns; ++s) {
-          const float w = expf(cp.lse_part[(size_t)s * plane + (size_t)h * cp.total_q + t] - L);
-          o += w * cp.o_part[((size_t)s * plane + row) * cp.head_dim + d];
-        }
-      reinterpret_cast<__nv_bfloat16*>(cp.out)[row * cp.head_dim + d] = __float2bfloat16_rn(o);
-    }
-    if (threadIdx.x == 0 && cp.lse) cp.lse[(size_t)h * cp.total_q + t] = L;
+  float lse_s[2], w_s[2];  // ns <= 64: lane holds splits lane and lane + 32
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int s = lane + 32 * k;
+    lse_s[k] = s < ns ? cp.lse_part[(size_t)s * plane + (size_t)h * cp.total_q + t] : NEG_INF;
   }
+  float mx = fmaxf(lse_s[0], lse_s[1]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    w_s[k] = (mx == NEG_INF || lse_s[k] == NEG_INF) ? 0.f : expf(lse_s[k] - mx);
+    sum += w_s[k];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  const float L = (mx == NEG_INF) ? NEG_INF : mx + logf(sum);
+  const size_t rbase = (size_t)t * cp.hq + h;
+  for (int d0 = lane * 4; d0 < cp.head_dim; d0 += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < ns; ++s) {
+      const float ws = __shfl_sync(0xFFFFFFFFu, w_s[s >> 5], s & 31) * inv;
+      if (ws != 0.f) {
+        const float4 v = *reinterpret_cast<const float4*>(cp.o_part + ((size_t)s * plane + rbase) * cp.head_dim + d0);
+        acc.x += ws * v.x;
+        acc.y += ws * v.y;
+        acc.z += ws * v.z;
+        acc.w += ws * v.w;
+      }
+    }
+    __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(cp.out) + rbase * cp.head_dim + d0);
+    o2[0] = __floats2bfloat162_rn(acc.x, acc.y);
+    o2[1] = __floats2bfloat162_rn(acc.z, acc.w);
+  }
+  if (lane == 0 && cp.lse) cp.lse[(size_t)h * cp.total_q + t] = L;
 }
 
 }  // namespace
@@ -139,7 +165,8 @@ cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream) {
 
 cudaError_t launch_combine(const CombineParams& cp, cudaStream_t stream) {
   if (cp.total_q <= 0) return cudaSuccess;
-  combine_kernel<<<cp.total_q, 128, 0, stream>>>(cp);
+  const long long rows = (long long)cp.total_q * cp.hq;
+  combine_kernel<<<(unsigned)((rows + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32, 0, stream>>>(cp);
   return cudaGetLastError();
 }
 

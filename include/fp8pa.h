@@ -119,8 +119,8 @@ int fp8pa_num_splits(int batch, int total_q, int max_seqlen_q, int num_heads_q, 
  * Support: head_dim 256 with E4M3 Q; head_dim 512 with BF16 Q (K/V dequantized
  * in-kernel, BF16 MMA) or E4M3 Q (FP8 MMA).  V head dim = head_dim.  num_heads_q
  * a multiple of num_heads_kv with a group size in {1, 2, 4, 8, 16}.
- * window_left >= -1.  num_splits: 0 = automatic, else the maximum number of
- * key splits per (sequence, KV head); splits are combined by log-sum-exp.
+ * window_left >= -1.  num_splits: 0 = automatic, else (1..64) the maximum number
+ * of key splits per (sequence, KV head); splits are combined by log-sum-exp.
  * Pointers q, k_cache, v_cache, out must be 16-byte aligned.
  *
  * workspace: device buffer of at least fp8pa_workspace_size(...) bytes, 256-byte
@@ -137,6 +137,23 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
                        const float* v_descale, int descale_batch_stride, int descale_head_stride,
                        float softmax_scale, int window_left, int causal, int num_splits, void* workspace,
                        size_t workspace_bytes, void* out, float* lse, fp8pa_stream_t stream);
+
+/*
+ * fp8pa_kernel_launches — number of kernels fp8_paged_attn_fwd launches for
+ * these host-known sizes (plan, one attention kernel per row class, and the
+ * LSE combine when the split count is above 1).  0 for rejected arguments.
+ */
+int fp8pa_kernel_launches(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv,
+                          int head_dim, int max_pages_per_seq, int window_left, int num_splits);
+
+/*
+ * fp8pa_set_timing_events — profiling hook for the calling host thread.  When
+ * both are non-NULL (cudaEvent_t handles), later fp8_paged_attn_fwd calls on
+ * this thread record `start` on their stream just before the first attention
+ * kernel and `stop` just after the last one, so the caller can time the
+ * attention kernels alone.  NULL, NULL turns it off.
+ */
+void fp8pa_set_timing_events(void* start_event, void* stop_event);
 
 /*
  * fp8pa_get_device_status — enqueue on `stream` a copy of the current device's
