@@ -238,6 +238,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
     dev = torch.device("cuda", local_rank)
+    fp8pa.set_ctas_per_sm(args.ctas_per_sm)
     w = synth.make_config(args.config, device=dev)
     stream = torch.cuda.current_stream()
     qd = torch.tensor([w.q_descale], dtype=torch.float32, device=dev)
@@ -386,6 +387,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ctas-per-sm", type=int, default=0, help="force 1 or 2 attention CTAs per SM (0 = auto)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

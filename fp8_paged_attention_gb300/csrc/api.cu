@@ -14,28 +14,28 @@
 #include "kernels.h"
 
 namespace fp8pa {
-cudaError_t launch_attn_fp8_d256(int, const AttnParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                 int, cudaStream_t);
-cudaError_t launch_attn_fp8_d512(int, const AttnParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                 int, cudaStream_t);
-cudaError_t launch_attn_bf16_d512(int, const AttnParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                  int, cudaStream_t);
-int smem_attn_fp8_d256(int);
-int smem_attn_fp8_d512(int);
-int smem_attn_bf16_d512(int);
+cudaError_t launch_attn_fp8_d256(int, int, const AttnParams&, const CUtensorMap&, const CUtensorMap&,
+                                 const CUtensorMap&, int, cudaStream_t);
+cudaError_t launch_attn_fp8_d512(int, int, const AttnParams&, const CUtensorMap&, const CUtensorMap&,
+                                 const CUtensorMap&, int, cudaStream_t);
+cudaError_t launch_attn_bf16_d512(int, int, const AttnParams&, const CUtensorMap&, const CUtensorMap&,
+                                  const CUtensorMap&, int, cudaStream_t);
+int smem_attn_fp8_d256(int, int);
+int smem_attn_fp8_d512(int, int);
+int smem_attn_bf16_d512(int, int);
 
-cudaError_t launch_attn(int head_dim, bool fp8_q, int rows, const AttnParams& p, const CUtensorMap& tm_q,
-                        const CUtensorMap& tm_k, const CUtensorMap& tm_v, int grid, cudaStream_t stream) {
-  if (head_dim == 256 && fp8_q) return launch_attn_fp8_d256(rows, p, tm_q, tm_k, tm_v, grid, stream);
-  if (head_dim == 512 && fp8_q) return launch_attn_fp8_d512(rows, p, tm_q, tm_k, tm_v, grid, stream);
-  if (head_dim == 512 && !fp8_q) return launch_attn_bf16_d512(rows, p, tm_q, tm_k, tm_v, grid, stream);
+cudaError_t launch_attn(int head_dim, bool fp8_q, int rows, int ctas, const AttnParams& p, const CUtensorMap& tm_q,
+                        const CUtensorMap& tm_k, const CUtensorMap& tm_v, int sms, cudaStream_t stream) {
+  if (head_dim == 256 && fp8_q) return launch_attn_fp8_d256(rows, ctas, p, tm_q, tm_k, tm_v, sms, stream);
+  if (head_dim == 512 && fp8_q) return launch_attn_fp8_d512(rows, ctas, p, tm_q, tm_k, tm_v, sms, stream);
+  if (head_dim == 512 && !fp8_q) return launch_attn_bf16_d512(rows, ctas, p, tm_q, tm_k, tm_v, sms, stream);
   return cudaErrorInvalidValue;
 }
 
-int attn_smem_bytes(int head_dim, bool fp8_q, int rows) {
-  if (head_dim == 256 && fp8_q) return smem_attn_fp8_d256(rows);
-  if (head_dim == 512 && fp8_q) return smem_attn_fp8_d512(rows);
-  if (head_dim == 512 && !fp8_q) return smem_attn_bf16_d512(rows);
+int attn_smem_bytes(int head_dim, bool fp8_q, int rows, int ctas) {
+  if (head_dim == 256 && fp8_q) return smem_attn_fp8_d256(rows, ctas);
+  if (head_dim == 512 && fp8_q) return smem_attn_fp8_d512(rows, ctas);
+  if (head_dim == 512 && !fp8_q) return smem_attn_bf16_d512(rows, ctas);
   return 0;
 }
 }  // namespace fp8pa
@@ -48,6 +48,18 @@ __device__ unsigned int g_status;
 
 thread_local char g_err[512] = "";
 thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+std::atomic<int> g_ctas_override{0};
+
+// CTAs per SM for a kernel variant: two co-resident CTAs where both fit
+// (E4M3 Q with up to 32 rows per tile), else one.
+int ctas_per_sm(int head_dim, bool fp8_q, int rows) {
+  const int forced = g_ctas_override.load();
+  if (forced == 1 || forced == 2) {
+    if (attn_smem_bytes(head_dim, fp8_q, rows, forced) > 0) return forced;
+  }
+  if (fp8_q && rows == 16 && attn_smem_bytes(head_dim, fp8_q, rows, 2) > 0) return 2;
+  return 1;
+}
 std::atomic<unsigned> g_wait_limit{0};
 
 int fail(int code, const char* fmt, ...) {
@@ -154,7 +166,8 @@ int auto_splits(const CallPlan& pl, int batch, int hkv, int max_pages, int windo
   long long pages = max_pages;
   if (window_left >= 0) pages = std::min<long long>(pages, (window_left + max_lq0 - 1) / kPage + 2);
   const long long tiles = (pages + 1) / 2;
-  long long s = (8LL * sms + units - 1) / units;
+  // enough items for about four per SM; each split keeps at least 4 tiles (512 keys)
+  long long s = (4LL * sms + units - 1) / units;
   s = std::min<long long>(s, std::max<long long>(1, tiles / 4));
   s = std::max<long long>(1, std::min<long long>(s, 64));
   (void)pl;
@@ -226,6 +239,8 @@ extern "C" {
 const char* fp8pa_last_error(void) { return g_err; }
 
 void fp8pa_set_wait_limit(unsigned int max_iterations) { g_wait_limit.store(max_iterations); }
+
+void fp8pa_set_ctas_per_sm(int ctas) { g_ctas_override.store(ctas); }
 
 void fp8pa_set_timing_events(void* start_event, void* stop_event) {
   g_ev_start = static_cast<cudaEvent_t>(start_event);
@@ -389,8 +404,8 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
     p.cls = pl.cls[k];
     p.work = reinterpret_cast<const int4*>(ws + pl.off_work[k]);
     p.work_count = counts + k;
-    const int grid = (int)std::min<size_t>((size_t)sms, std::max<size_t>(1, pl.items_max[k]));
-    e = launch_attn(head_dim, fp8_q, pl.cls[k].rows, p, tm_q[k], tm_k, tm_v, grid, st);
+    e = launch_attn(head_dim, fp8_q, pl.cls[k].rows, ctas_per_sm(head_dim, fp8_q, pl.cls[k].rows), p, tm_q[k], tm_k,
+                    tm_v, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   }
   if (timed && (e = cudaEventRecord(g_ev_stop, st)) != cudaSuccess) return cuda_fail(e, "timing event");

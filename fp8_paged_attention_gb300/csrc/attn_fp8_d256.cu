@@ -3,21 +3,26 @@
 
 namespace fp8pa {
 
-cudaError_t launch_attn_fp8_d256(int rows, const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                                const CUtensorMap& tm_v, int grid, cudaStream_t stream) {
-  switch (rows) {
-    case 16: return launch_attn_variant<256, true, 16>(p, tm_q, tm_k, tm_v, grid, stream);
-    case 32: return launch_attn_variant<256, true, 32>(p, tm_q, tm_k, tm_v, grid, stream);
-    case 64: return launch_attn_variant<256, true, 64>(p, tm_q, tm_k, tm_v, grid, stream);
+// rows: 16, 32 or 64 query rows per tile; ctas: CTAs per SM (1 or 2).
+cudaError_t launch_attn_fp8_d256(int rows, int ctas, const AttnParams& p, const CUtensorMap& tm_q,
+                                const CUtensorMap& tm_k, const CUtensorMap& tm_v, int sms, cudaStream_t stream) {
+  switch (rows * 2 + ctas) {
+    case 16 * 2 + 1: return launch_attn_variant<256, true, 16, 1>(p, tm_q, tm_k, tm_v, sms, stream);
+    case 32 * 2 + 1: return launch_attn_variant<256, true, 32, 1>(p, tm_q, tm_k, tm_v, sms, stream);
+    case 64 * 2 + 1: return launch_attn_variant<256, true, 64, 1>(p, tm_q, tm_k, tm_v, sms, stream);
+    case 16 * 2 + 2: return launch_attn_variant<256, true, 16, 2>(p, tm_q, tm_k, tm_v, sms, stream);
+    case 32 * 2 + 2: return launch_attn_variant<256, true, 32, 2>(p, tm_q, tm_k, tm_v, sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-int smem_attn_fp8_d256(int rows) {
-  switch (rows) {
-    case 16: return AttnCfg<256, true, 16>::kSmemBytes;
-    case 32: return AttnCfg<256, true, 32>::kSmemBytes;
-    case 64: return AttnCfg<256, true, 64>::kSmemBytes;
+int smem_attn_fp8_d256(int rows, int ctas) {
+  switch (rows * 2 + ctas) {
+    case 16 * 2 + 1: return AttnCfg<256, true, 16, 1>::kSmemBytes;
+    case 32 * 2 + 1: return AttnCfg<256, true, 32, 1>::kSmemBytes;
+    case 64 * 2 + 1: return AttnCfg<256, true, 64, 1>::kSmemBytes;
+    case 16 * 2 + 2: return AttnCfg<256, true, 16, 2>::kSmemBytes;
+    case 32 * 2 + 2: return AttnCfg<256, true, 32, 2>::kSmemBytes;
     default: return 0;
   }
 }

@@ -38,10 +38,14 @@
 
 namespace fp8pa {
 
-template <int D, bool kFP8, int N>
+// kCtas: CTAs resident per SM.  Two co-resident CTAs run two independent
+// item pipelines per SM, hiding each other's per-item bubbles (epilogue,
+// first-tile latency); each then gets half the shared memory and TMEM.
+template <int D, bool kFP8, int N, int kCtas = 1>
 struct AttnCfg {
   static_assert(D == 256 || D == 512, "head dim");
   static_assert(N == 16 || N == 32 || N == 64, "rows per tile");
+  static_assert(kCtas == 1 || kCtas == 2, "CTAs per SM");
   static constexpr int kDC = D / 128;                    // 128-byte chunks of an E4M3 row
   static constexpr int kQChunkElems = kFP8 ? 128 : 64;   // Q elements per 128-byte chunk
   static constexpr int kQChunks = D / kQChunkElems;
@@ -50,7 +54,8 @@ struct AttnCfg {
   static constexpr int kPBytes = kFP8 ? 2 * N * 128 : N * 256;
   static constexpr int kBfSlotBytes = 32768;             // BF16 tile of 128 keys x 128 dims
   static constexpr int kThreads = kFP8 ? 192 : 320;
-  static constexpr int kSmemLimit = 232448;              // opt-in maximum per block
+  // opt-in maximum per block; two blocks share the SM's 228 KB minus 1 KB reserved each
+  static constexpr int kSmemLimit = kCtas == 1 ? 232448 : 115712;
   // barriers (< 1 KB) + per-row softmax state: red[2][4][N], lred[4][N], 4 x [N] floats
   static constexpr int kCtrlBytes = 1024 + 64 * N + 64;
   static constexpr int kQBufs = kFP8 ? ((2 * kQBytes <= 65536) ? 2 : 1) : ((2 * kQBytes <= 32768) ? 2 : 1);
@@ -58,6 +63,9 @@ struct AttnCfg {
   static constexpr int kFixed = kQBufs * kQBytes + 2 * kPBytes + kBfSlots * kBfSlotBytes + kCtrlBytes + 1024;
   static constexpr int kStages = (kSmemLimit - kFixed) / kStageBytes > 16 ? 16 : (kSmemLimit - kFixed) / kStageBytes;
   static_assert(kStages >= 2, "smem");
+  // FP8 path: the tail tile's V chunks must fit in the ring together (the softmax zeroes them in place)
+  static_assert(!kFP8 || kStages >= kDC, "ring shorter than one tile's V");
+  static_assert(kCtas == 1 || 2 * (2 * N + (D / 128) * N) <= 512, "TMEM for two CTAs");
   static constexpr int kSmemBytes = kFixed + kStages * kStageBytes;
   static constexpr int kTmemUsed = 2 * N + kDC * N;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
@@ -154,11 +162,11 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2_bf16x2(uint16_t v) {
 
 }  // namespace detail
 
-template <int D, bool kFP8, int N>
-__global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
+template <int D, bool kFP8, int N, int kCtas>
+__global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
     attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
-  using C = AttnCfg<D, kFP8, N>;
+  using C = AttnCfg<D, kFP8, N, kCtas>;
   using namespace ptx;
   using namespace detail;
   constexpr int S = C::kStages;
@@ -185,7 +193,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
   uint64_t* p_full = s_empty + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* o_empty = pv_done + 2;
-  uint64_t* drain = o_empty + 1;
+  uint64_t* v_ready = o_empty + 1;  // tail tile: its V stages have landed (MMA thread -> softmax)
+  uint64_t* drain = v_ready + 1;
   float* red = reinterpret_cast<float*>(drain + 1);  // [2][4][N] per-warp tile maxima
   float* lred = red + 2 * 4 * N;                      // [4][N] per-warp row sums
   float* m_s = lred + 4 * N;                          // [N] running max (log2 units)
@@ -217,6 +226,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(o_empty, 4);
+    mbar_init(v_ready, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -328,9 +338,15 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
           mma_commit(&s_full[sb]);
           return true;
         };
-        // O^T += V^T . P^T(gg)
-        auto pv = [&](uint32_t gg, bool first) -> bool {
+        // O^T += V^T . P^T(gg).  On a tail tile (keys past Lk) the softmax zeroes
+        // the V rows past Lk first; the in-order wait here tells it the stages landed.
+        auto pv = [&](uint32_t gg, bool first, bool tail) -> bool {
           const uint32_t pb = gg & 1;
+          if (kFP8 && tail) {
+            for (int c = 0; c < DC; ++c)
+              if (!pwait(&ring_full[(idx + c) % S], ((idx + c) / S) & 1, lim, abort_flag)) return false;
+            mbar_arrive(v_ready);
+          }
           if (!pwait(&p_full[pb], (gg >> 1) & 1, lim, abort_flag)) return false;
           if (first && !pwait(o_empty, ((qit - 1) & 1) ^ 1, lim, abort_flag)) return false;
           tc_fence_after();
@@ -372,7 +388,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
           if (u + 1 < n) ok = qk(g + u + 1);
           if (!ok) break;
           if (u + 1 == n) mma_commit(&q_empty[qb]);
-          ok = pv(g + u, u == 0);
+          const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
+          ok = pv(g + u, u == 0, kb + kTileKeys > it.Lk);
         }
         g += n;
       }
@@ -387,7 +404,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
     const int kl = quarter * 32 + lane;     // key (S) or head-dim (O) lane within the tile
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float NEG_INF = __int_as_float(0xFF800000);
-    uint32_t g = 0, sbase = 0;
+    uint32_t g = 0, sbase = 0, tails = 0;
     bool aborted = false;
     for (int w = blockIdx.x; w < n_items && !aborted; w += gridDim.x) {
       const Item it = decode_item(p, p.work[w]);
@@ -420,7 +437,11 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
       const float kd = load_descale(p.k_descale, p, it);
       const float vd = load_descale(p.v_descale, p, it);
       const float scale = p.softmax_scale_log2 * kd * (kFP8 ? *p.q_descale : 1.0f);
-      if (wt < N) m_s[wt] = NEG_INF;
+      if (wt < N) {
+        m_s[wt] = NEG_INF;
+        a_s[wt] = 1.0f;
+        msub_s[wt] = -C::kPShift;
+      }
       float lt[N];
 #pragma unroll
       for (int n = 0; n < N; ++n) lt[n] = 0.f;
@@ -434,12 +455,18 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
         float x[N];
         if (ok) {
           tc_fence_after();
+          // rows past nrows are padding (decode tiles hold G * Lq real rows): skip their work
 #pragma unroll
           for (int c = 0; c < N; c += 16) {
-            uint32_t r[16];
-            tmem_load16(tmem + lane_base + sb * N + c, r);
+            if (c < it.nrows) {
+              uint32_t r[16];
+              tmem_load16(tmem + lane_base + sb * N + c, r);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(r[i]) * scale;
+              for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(r[i]) * scale;
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) x[c + i] = NEG_INF;
+            }
           }
           tc_fence_before();
           __syncwarp();
@@ -463,8 +490,10 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
           float* rb = red + (g & 1) * 4 * N + quarter * N;
 #pragma unroll
           for (int n = 0; n < N; ++n) {
-            const float mx = warp_max(x[n]);
-            if (lane == (n & 31)) rb[n] = mx;
+            if (n < it.nrows) {
+              const float mx = warp_max(x[n]);
+              if (lane == (n & 31)) rb[n] = mx;
+            }
           }
         } else {
           flag_timeout(p, abort_flag);
@@ -475,7 +504,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
         }
         // row owners fold the four warp maxima into the running max
         bool resc = false;
-        if (wt < N) {
+        if (wt < it.nrows) {
           const float* rr = red + (g & 1) * 4 * N;
           const float tmax = fmaxf(fmaxf(rr[wt], rr[N + wt]), fmaxf(rr[2 * N + wt], rr[3 * N + wt]));
           const float mo = m_s[wt];
@@ -501,6 +530,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
           if (kFP8) {
 #pragma unroll
             for (int blk = 0; blk < N / 16; ++blk) {
+              if (blk * 16 >= it.nrows) break;
               uint32_t hi_w[4], lo_w[4];
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) {
@@ -538,6 +568,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
           } else {
 #pragma unroll
             for (int blk = 0; blk < N / 8; ++blk) {
+              if (blk * 8 >= it.nrows) break;
               uint32_t packed[4];
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) {
@@ -562,16 +593,15 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
           // zero those V rows so that 0 * V stays 0 in the PV MMA
           if (kFP8 && kb + kTileKeys > it.Lk) {
             const int zr = max(0, it.Lk - kb);
+            ok = pwait(v_ready, tails & 1, lim, abort_flag);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            ++tails;
 #pragma unroll 1
             for (int c = 0; c < DC && ok; ++c) {
               const uint32_t vi = sbase + v_stage_offset(u, n_t, DC) + c;
-              ok = pwait(&ring_full[vi % S], (vi / S) & 1, lim, abort_flag);
-              ok = __all_sync(0xFFFFFFFFu, ok);
-              if (ok) {
-                uint8_t* st = ring + (vi % S) * kStageBytes;
-                for (int x16 = zr * 8 + wt; x16 < kTileKeys * 8; x16 += 128)
-                  *reinterpret_cast<uint4*>(st + x16 * 16) = make_uint4(0, 0, 0, 0);
-              }
+              uint8_t* st = ring + (vi % S) * kStageBytes;
+              for (int x16 = zr * 8 + wt; x16 < kTileKeys * 8; x16 += 128)
+                *reinterpret_cast<uint4*>(st + x16 * 16) = make_uint4(0, 0, 0, 0);
             }
           }
           fence_proxy_async_smem();
@@ -585,6 +615,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
               for (int c = 0; c < DC; ++c) {
 #pragma unroll
                 for (int cc = 0; cc < N; cc += 16) {
+                  if (cc >= it.nrows) break;
                   uint32_t r[16];
                   const uint32_t ta = tmem + lane_base + 2 * N + c * N + cc;
                   tmem_load16(ta, r);
@@ -612,17 +643,19 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
       ok = __all_sync(0xFFFFFFFFu, ok);
 #pragma unroll
       for (int n = 0; n < N; ++n) {
-        float v = lt[n];
+        if (n < it.nrows) {
+          float v = lt[n];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-        if (lane == (n & 31)) lred[quarter * N + n] = v;
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+          if (lane == (n & 31)) lred[quarter * N + n] = v;
+        }
       }
       if (!ok) flag_timeout(p, abort_flag);
       if (bar_red_or(1, 128, !ok)) {
         aborted = true;
         break;
       }
-      if (wt < N) l_s[wt] = (lred[wt] + lred[N + wt]) + (lred[2 * N + wt] + lred[3 * N + wt]);
+      if (wt < it.nrows) l_s[wt] = (lred[wt] + lred[N + wt]) + (lred[2 * N + wt] + lred[3 * N + wt]);
       named_bar_sync(2, 128);
       tc_fence_after();
 #pragma unroll 1
@@ -630,6 +663,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N>::kThreads, 1)
         const int d = c * 128 + kl;
 #pragma unroll
         for (int cc = 0; cc < N; cc += 16) {
+          if (cc >= it.nrows) break;
           uint32_t r[16];
           tmem_load16(tmem + lane_base + 2 * N + c * N + cc, r);
 #pragma unroll

@@ -34,12 +34,13 @@ cudaError_t launch_combine(const CombineParams& cp, cudaStream_t stream);
 cudaError_t launch_quantize_q(const void* q_bf16, void* q_e4m3, const float* q_descale, long long n,
                               cudaStream_t stream);
 
-// Attention kernel launchers, one per (head dim, Q type, rows per tile).
-// `grid` CTAs, each persistent over the class's work list.
-cudaError_t launch_attn(int head_dim, bool fp8_q, int rows, const AttnParams& p, const CUtensorMap& tm_q,
-                        const CUtensorMap& tm_k, const CUtensorMap& tm_v, int grid, cudaStream_t stream);
+// Attention kernel launchers, one per (head dim, Q type, rows per tile, CTAs per SM);
+// every CTA is persistent over the class's work list.
+// `ctas` CTAs per SM, `sms` SMs: grid = sms * ctas persistent CTAs.
+cudaError_t launch_attn(int head_dim, bool fp8_q, int rows, int ctas, const AttnParams& p, const CUtensorMap& tm_q,
+                        const CUtensorMap& tm_k, const CUtensorMap& tm_v, int sms, cudaStream_t stream);
 
 // Shared-memory bytes of a kernel variant (0 if the variant does not exist).
-int attn_smem_bytes(int head_dim, bool fp8_q, int rows);
+int attn_smem_bytes(int head_dim, bool fp8_q, int rows, int ctas);
 
 }  // namespace fp8pa

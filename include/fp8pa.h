@@ -156,6 +156,13 @@ int fp8pa_kernel_launches(int batch, int total_q, int max_seqlen_q, int num_head
 void fp8pa_set_timing_events(void* start_event, void* stop_event);
 
 /*
+ * fp8pa_set_ctas_per_sm — tuning hook: 1 or 2 forces that many attention CTAs
+ * per SM where the kernel variant supports it; 0 restores the automatic choice
+ * (two co-resident CTAs for E4M3 Q with 16-row tiles, else one).
+ */
+void fp8pa_set_ctas_per_sm(int ctas);
+
+/*
  * fp8pa_get_device_status — enqueue on `stream` a copy of the current device's
  * status word (FP8PA_DEV_* bits accumulated by earlier launches) into
  * *host_status, which must be pinned host memory; the value is valid once the
