@@ -146,10 +146,17 @@ def unit_bytes_of(w: synth.Workload, units):
 
 # ------------------------------------------------------------------ CPU oracle leg
 
-def oracle_timing(w: synth.Workload, budget_s: float, seed: int = 0):
+def unit_flops_of(w: synth.Workload, units):
+    """QK^T + PV flops (4 D per visible pair) of a set of (sequence, kv-head) units."""
+    G = w.num_heads_q // w.num_heads_kv
+    return sum(synth._visible_count(int(w.lq[b]), int(w.lk[b]), w.window_left, w.causal) * G * 4 * w.head_dim
+               for b, _hk in units)
+
+
+def oracle_timing(w: synth.Workload, budget_s: float, seed: int = 0, tflops: bool = False):
     """Time the oracle on a bounded sample of (sequence, kv-head) units of the
-    workload (every query row and head of each unit).  Returns (GB/s, cores,
-    description, seconds)."""
+    workload (every query row and head of each unit).  Returns (rate in GB/s,
+    or TFLOP/s when tflops, cores, description, seconds)."""
     import oracle  # test/benchmark infrastructure only
     rng = np.random.default_rng(seed)
     G = w.num_heads_q // w.num_heads_kv
@@ -183,20 +190,21 @@ def oracle_timing(w: synth.Workload, budget_s: float, seed: int = 0):
     n = min(len(units_all), 8)
     pilot = [units_all[i] for i in order[:n]]
     t = run(pilot)
-    rate = unit_bytes_of(w, pilot) / max(t, 1e-9)
-    want = budget_s * rate
+    pilot_rate = unit_flops_of(w, pilot) / max(t, 1e-9)
+    want = budget_s * pilot_rate
     units, acc = [], 0
     for i in order:
         units.append(units_all[i])
-        acc += unit_bytes_of(w, [units_all[i]])
+        acc += unit_flops_of(w, [units_all[i]])
         if acc >= want:
             break
     t = run(units)
-    gbs = unit_bytes_of(w, units) / t / 1e9
+    rate = unit_flops_of(w, units) / t / 1e12 if tflops else unit_bytes_of(w, units) / t / 1e9
     cores = os.cpu_count() or 1
     desc = (f"{len(units)} of {len(units_all)} (sequence, KV head) units of {w.name}, every query row and head; "
-            f"{unit_bytes_of(w, units) / 1e6:.1f} MB of algorithmic KV bytes in {t:.2f} s")
-    return gbs, cores, desc, t
+            f"{unit_bytes_of(w, units) / 1e6:.1f} MB of algorithmic KV bytes, "
+            f"{unit_flops_of(w, units) / 1e9:.2f} GFLOP, in {t:.2f} s")
+    return rate, cores, desc, t
 
 
 def run_reference(args):
@@ -209,20 +217,22 @@ def run_reference(args):
     per_step = max(0.05, min(30.0, 150.0 / max(1, total_steps)))
     vals, cores, desc = [], 1, ""
     t_all = 0.0
+    tensor_bound = w.name.startswith("chunk_")
+    unit = "TFLOP/s" if tensor_bound else "GB/s"
     for i in range(total_steps):
-        gbs, cores, desc, t = oracle_timing(w, per_step, seed=i)
+        r, cores, desc, t = oracle_timing(w, per_step, seed=i, tflops=tensor_bound)
         if i >= args.warmup:
-            vals.append(gbs)
+            vals.append(r)
             t_all += t
     value = statistics.median(vals)
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_all / max(1, len(vals)), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "sample": "per step: " + desc},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": desc},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
     return 0
@@ -246,19 +256,23 @@ def run_ours(args):
     vd = torch.tensor([w.v_descale], dtype=torch.float32, device=dev)
     hq, hkv, D = w.num_heads_q, w.num_heads_kv, w.head_dim
     max_pages = w.block_table.shape[1]
-    ws_bytes = fp8pa.workspace_size(w.batch, w.total_q, w.max_seqlen_q, hq, hkv, D, max_pages, w.window_left, 0)
+    qdt = fp8pa.FP8PA_E4M3 if w.fp8_q else fp8pa.FP8PA_BF16
+    ns_arg = args.num_splits
+    ws_bytes = fp8pa.workspace_size(w.batch, w.total_q, w.max_seqlen_q, hq, hkv, D, qdt, max_pages, w.window_left,
+                                    ns_arg)
     workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     out = torch.empty((w.total_q, hq, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((hq, w.total_q), dtype=torch.float32, device=dev)
     q8 = torch.empty((w.total_q, hq, D), dtype=torch.uint8, device=dev)
-    splits = fp8pa.num_splits(w.batch, w.total_q, w.max_seqlen_q, hq, hkv, D, max_pages, w.window_left, 0)
-    launches = fp8pa.kernel_launches(w.batch, w.total_q, w.max_seqlen_q, hq, hkv, D, max_pages, w.window_left, 0)
+    splits = fp8pa.num_splits(w.batch, w.total_q, w.max_seqlen_q, hq, hkv, D, qdt, max_pages, w.window_left, ns_arg)
+    launches = fp8pa.kernel_launches(w.batch, w.total_q, w.max_seqlen_q, hq, hkv, D, qdt, max_pages, w.window_left,
+                                     ns_arg)
     launches += 1 if w.fp8_q else 0
 
     def step(q_src, bt, cu, su, o, l):
         q = fp8pa.quantize_q_fp8(q_src, qd, out=q8) if w.fp8_q else q_src
         fp8pa.fp8_paged_attn_fwd(q, w.k_cache, w.v_cache, bt, cu, su, w.max_seqlen_q, qd, kd, vd,
-                                 w.softmax_scale, w.window_left, w.causal, num_splits=0, out=o, lse=l,
+                                 w.softmax_scale, w.window_left, w.causal, num_splits=ns_arg, out=o, lse=l,
                                  workspace=workspace)
 
     args_dev = (w.q, w.block_table, w.cu_seqlens_q, w.seqused_k, out, lse)
@@ -298,14 +312,33 @@ def run_ours(args):
         ms_total = float(t.item())
     ms_step = ms_total / args.steps
     kv_bytes = w.kv_bytes_algorithmic()
-    value = world * kv_bytes * args.steps / (ms_total * 1e-3) / 1e9
     peaks = measured_peaks()
     k_avg_ms = sum(k_ms) / len(k_ms)
-    achieved = kv_bytes / (k_avg_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(w.name),
-                "kernel": "attn_fwd_kernel", "kernel_ms": round(k_avg_ms, 5),
-                "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}
+    tensor_bound = w.name.startswith("chunk_")
+    if tensor_bound:
+        # a prefill chunk alone: causal/window-visible QK^T + PV flops against the dense tensor peak
+        flops = w.flops_algorithmic()
+        unit = "TFLOP/s"
+        value = world * flops * args.steps / (ms_total * 1e-3) / 1e12
+        achieved = flops / (k_avg_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"] * (2.0 if w.fp8_q else 1.0)
+        peak_src = (peaks["source"] + " MEASURED_PEAKS.json bf16_tflops (burst)" +
+                    (" x 2, the nominal FP8/BF16 dense ratio" if w.fp8_q else ""))
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
+                    "frac": round(achieved / peak, 4), "traffic": ncu_traffic(w.name), "kernel": "attn_fwd_kernel",
+                    "kernel_ms": round(k_avg_ms, 5), "peak_source": peak_src}
+    else:
+        unit = "GB/s"
+        value = world * kv_bytes * args.steps / (ms_total * 1e-3) / 1e9
+        achieved = kv_bytes / (k_avg_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": unit,
+                    "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(w.name),
+                    "kernel": "attn_fwd_kernel", "kernel_ms": round(k_avg_ms, 5),
+                    "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}
+
+    def rate(n_steps, ms):
+        work = w.flops_algorithmic() if tensor_bound else kv_bytes
+        return world * work * n_steps / (ms * 1e-3) / (1e12 if tensor_bound else 1e9)
 
     # ---------------- end to end through the public API, host buffers
     e2e = None
@@ -344,7 +377,7 @@ def run_ours(args):
             t = torch.tensor([e_ms], device=dev)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             e_ms = float(t.item())
-        e2e = {"value": round(world * kv_bytes * n_e2e / (e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+        e2e = {"value": round(rate(n_e2e, e_ms), 3), "unit": unit,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
                "ms_per_step": round(e_ms / n_e2e, 5),
                "note": "K/V cache is resident state; per step Q, block table and lengths go up, out and lse come back"}
@@ -352,12 +385,12 @@ def run_ours(args):
     # ---------------- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, cores, desc, _t = oracle_timing(w, budget_s=args.cpu_budget)
-        cpu = {"value": round(gbs, 5), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+        r, cores, desc, _t = oracle_timing(w, budget_s=args.cpu_budget, tflops=tensor_bound)
+        cpu = {"value": round(r, 6), "unit": unit, "cores": cores, "kind": "oracle", "sample": desc}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3" if w.fp8_q else "bf16", "data": "synthetic",
             "config": {"workload": w.name, "batch": w.batch, "total_q": w.total_q, "num_heads_q": hq,
@@ -388,6 +421,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ctas-per-sm", type=int, default=0, help="force 1 or 2 attention CTAs per SM (0 = auto)")
+    ap.add_argument("--num-splits", type=int, default=0, help="split-KV count (0 = automatic)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -62,9 +62,9 @@ def load_library():
         lib.quantize_q_fp8.restype = c.c_int
         lib.quantize_q_fp8.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_longlong, c.c_void_p]
         lib.fp8pa_workspace_size.restype = c.c_size_t
-        lib.fp8pa_workspace_size.argtypes = [c.c_int] * 9
+        lib.fp8pa_workspace_size.argtypes = [c.c_int] * 10
         lib.fp8pa_num_splits.restype = c.c_int
-        lib.fp8pa_num_splits.argtypes = [c.c_int] * 9
+        lib.fp8pa_num_splits.argtypes = [c.c_int] * 10
         lib.fp8_paged_attn_fwd.restype = c.c_int
         lib.fp8_paged_attn_fwd.argtypes = [
             c.c_void_p, c.c_int, c.c_void_p, c.c_void_p, c.c_int, c.c_void_p, c.c_int, c.c_void_p, c.c_void_p,
@@ -81,7 +81,7 @@ def load_library():
         lib.fp8pa_set_wait_limit.restype = None
         lib.fp8pa_set_wait_limit.argtypes = [c.c_uint]
         lib.fp8pa_kernel_launches.restype = c.c_int
-        lib.fp8pa_kernel_launches.argtypes = [c.c_int] * 9
+        lib.fp8pa_kernel_launches.argtypes = [c.c_int] * 10
         lib.fp8pa_set_ctas_per_sm.restype = None
         lib.fp8pa_set_ctas_per_sm.argtypes = [c.c_int]
         lib.fp8pa_set_timing_events.restype = None
@@ -106,23 +106,23 @@ def _ptr(t) -> int:
     return 0 if t is None else int(t.data_ptr())
 
 
-def workspace_size(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq,
+def workspace_size(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_dtype, max_pages_per_seq,
                    window_left=-1, num_splits=0) -> int:
     return int(load_library().fp8pa_workspace_size(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv,
-                                                   head_dim, max_pages_per_seq, window_left, num_splits))
+                                                   head_dim, q_dtype, max_pages_per_seq, window_left, num_splits))
 
 
-def num_splits(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq,
+def num_splits(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_dtype, max_pages_per_seq,
                window_left=-1, num_splits=0) -> int:
     return int(load_library().fp8pa_num_splits(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim,
-                                               max_pages_per_seq, window_left, num_splits))
+                                               q_dtype, max_pages_per_seq, window_left, num_splits))
 
 
-def kernel_launches(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq,
+def kernel_launches(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_dtype, max_pages_per_seq,
                     window_left=-1, num_splits=0) -> int:
     """Kernels one fp8_paged_attn_fwd call launches for these sizes."""
     return int(load_library().fp8pa_kernel_launches(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv,
-                                                    head_dim, max_pages_per_seq, window_left, num_splits))
+                                                    head_dim, q_dtype, max_pages_per_seq, window_left, num_splits))
 
 
 def set_timing_events(start=None, stop=None):
@@ -180,7 +180,7 @@ def fp8_paged_attn_fwd(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k
         out = torch.empty((total_q, hq, d), dtype=torch.bfloat16, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty((hq, total_q), dtype=torch.float32, device=q.device)
-    need = workspace_size(batch, total_q, max_seqlen_q, hq, hkv, d, max_pages, window_left, num_splits)
+    need = workspace_size(batch, total_q, max_seqlen_q, hq, hkv, d, q_dtype, max_pages, window_left, num_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("block_table", block_table),

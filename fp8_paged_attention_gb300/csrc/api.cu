@@ -128,6 +128,7 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Everything about a call that follows from host-known sizes.
 struct CallPlan {
   int group;
+  bool fp8_q;
   int num_classes;
   ClassInfo cls[2];
   int splits;
@@ -160,24 +161,35 @@ int check_shape(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int h
   return FP8PA_OK;
 }
 
-int auto_splits(const CallPlan& pl, int batch, int hkv, int max_pages, int window_left, int max_lq0, int sms) {
+// Split count for single-row-tile sequences.  Measured on GB300: once every
+// SM has a (sequence, KV head) unit the kernel streams at the HBM roofline and
+// splitting only adds partial writes and the combine, so split only when there
+// are fewer units than SMs, to about two items per SM, each split keeping at
+// least four 128-key tiles.
+int auto_splits(int batch, int hkv, int max_pages, int window_left, int max_lq0, int sms) {
   const long long units = (long long)hkv * batch;
-  if (units <= 0) return 1;
+  if (units <= 0 || units >= sms) return 1;
   long long pages = max_pages;
   if (window_left >= 0) pages = std::min<long long>(pages, (window_left + max_lq0 - 1) / kPage + 2);
   const long long tiles = (pages + 1) / 2;
-  // enough items for about four per SM; each split keeps at least 4 tiles (512 keys)
-  long long s = (4LL * sms + units - 1) / units;
+  long long s = (2LL * sms + units - 1) / units;
   s = std::min<long long>(s, std::max<long long>(1, tiles / 4));
   s = std::max<long long>(1, std::min<long long>(s, 64));
-  (void)pl;
-  return (int)s;
+  // two splits measured far slower than one or three on the sliding-window decode
+  return (int)(s == 2 ? 3 : s);
 }
 
-int make_plan(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int head_dim, int max_pages,
+int make_plan(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int head_dim, int q_dtype, int max_pages,
               int window_left, int num_splits, CallPlan& pl) {
   int rc = check_shape(batch, total_q, max_seqlen_q, hq, hkv, head_dim, max_pages, window_left, num_splits);
   if (rc) return rc;
+  if (q_dtype != FP8PA_BF16 && q_dtype != FP8PA_E4M3)
+    return fail(FP8PA_EINVAL, "q_dtype must be FP8PA_BF16 (0) or FP8PA_E4M3 (1), got %d", q_dtype);
+  if (head_dim == 256 && q_dtype != FP8PA_E4M3)
+    return fail(FP8PA_EUNSUPPORTED,
+                "q dtype bfloat16 with k/v dtype float8_e4m3fn at head_size 256 is not supported "
+                "(head_size 256 takes E4M3 Q; quantize it with quantize_q_fp8)");
+  pl.fp8_q = q_dtype == FP8PA_E4M3;
   const int g = hq / hkv;
   pl.group = g;
   const long long rmax = (long long)max_seqlen_q * g;
@@ -199,8 +211,10 @@ int make_plan(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int hea
       lq0_max = 1;
     }
   }
-  pl.splits = num_splits > 0 ? num_splits
-                             : auto_splits(pl, batch, hkv, max_pages, window_left, lq0_max, device_sms());
+  // With a prefill row class in the batch its tiles keep every SM busy: no split.
+  pl.splits = num_splits > 0       ? num_splits
+              : pl.num_classes > 1 ? 1
+                                   : auto_splits(batch, hkv, max_pages, window_left, lq0_max, device_sms());
   pl.cls[0].max_splits = pl.splits;
   // workspace layout: [counts][class-0 items][class-1 items][o_part][lse_part]
   pl.items_max[0] = (size_t)hkv * batch * pl.splits;
@@ -247,11 +261,11 @@ void fp8pa_set_timing_events(void* start_event, void* stop_event) {
   g_ev_stop = static_cast<cudaEvent_t>(stop_event);
 }
 
-int fp8pa_kernel_launches(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
+int fp8pa_kernel_launches(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim, int q_dtype,
                           int max_pages_per_seq, int window_left, int num_splits) {
   CallPlan pl;
-  if (make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq, window_left,
-                num_splits, pl))
+  if (make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_dtype, max_pages_per_seq,
+                window_left, num_splits, pl))
     return 0;
   if (batch == 0 || total_q == 0) return 0;
   int n = 1;  // plan
@@ -272,19 +286,19 @@ int quantize_q_fp8(const void* q_bf16, void* q_e4m3, const float* q_descale, lon
 }
 
 size_t fp8pa_workspace_size(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv,
-                            int head_dim, int max_pages_per_seq, int window_left, int num_splits) {
+                            int head_dim, int q_dtype, int max_pages_per_seq, int window_left, int num_splits) {
   CallPlan pl;
-  if (make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq, window_left,
-                num_splits, pl))
+  if (make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_dtype, max_pages_per_seq,
+                window_left, num_splits, pl))
     return 0;
   return pl.total;
 }
 
-int fp8pa_num_splits(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
+int fp8pa_num_splits(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim, int q_dtype,
                      int max_pages_per_seq, int window_left, int num_splits) {
   CallPlan pl;
-  if (make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq, window_left,
-                num_splits, pl))
+  if (make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_dtype, max_pages_per_seq,
+                window_left, num_splits, pl))
     return 0;
   return pl.splits;
 }
@@ -296,17 +310,11 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
                        const float* v_descale, int descale_batch_stride, int descale_head_stride,
                        float softmax_scale, int window_left, int causal, int num_splits, void* workspace,
                        size_t workspace_bytes, void* out, float* lse, fp8pa_stream_t stream) {
-  if (q_dtype != FP8PA_BF16 && q_dtype != FP8PA_E4M3)
-    return fail(FP8PA_EINVAL, "q_dtype must be FP8PA_BF16 (0) or FP8PA_E4M3 (1), got %d", q_dtype);
   const bool fp8_q = q_dtype == FP8PA_E4M3;
   CallPlan pl;
-  int rc = make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, max_pages_per_seq,
+  int rc = make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_dtype, max_pages_per_seq,
                      window_left, num_splits, pl);
   if (rc) return rc;
-  if (head_dim == 256 && !fp8_q)
-    return fail(FP8PA_EUNSUPPORTED,
-                "q dtype bfloat16 with k/v dtype float8_e4m3fn at head_size 256 is not supported "
-                "(head_size 256 takes E4M3 Q; quantize it with quantize_q_fp8)");
   if (causal != 0 && causal != 1) return fail(FP8PA_EINVAL, "causal must be 0 or 1 (got %d)", causal);
   if (!std::isfinite(softmax_scale)) return fail(FP8PA_EINVAL, "softmax_scale must be finite");
   if (descale_batch_stride < 0 || descale_head_stride < 0) return fail(FP8PA_EINVAL, "descale strides must be >= 0");

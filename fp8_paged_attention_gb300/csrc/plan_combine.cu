@@ -3,9 +3,10 @@
 // plan_kernel turns (cu_seqlens_q, seqused_k) into the work lists of up to two
 // sequence classes (decode-like sequences with few query rows, prefill-like
 // sequences with many) without any host read of device memory, so a forward
-// call stays capturable in a CUDA graph.  Items are ordered KV-head-major, then
-// by sequence, row tile and split: CTAs that run side by side then touch the
-// same KV head, which keeps shared-prefix pages hot in L2.
+// call stays capturable in a CUDA graph.  Items are ordered by sequence, then
+// KV head, row tile and split: CTAs that run side by side read every KV head
+// of the same pages (the heads of one slot are adjacent in memory), and with a
+// shared prefix the same pages again a few sequences later, while still in L2.
 //
 // combine_kernel merges the per-split partial outputs with their log-sum-exps:
 //   L = log sum_s exp(lse_s),  out = sum_s exp(lse_s - L) * O_s
@@ -77,11 +78,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
       if (!(Lq > 0 && in_class(Lq, c))) continue;
       const int rts = seq_row_tiles(Lq, pp.group, c.rows);
       const int ns = seq_splits(Lq, Lk, pp.group, pp.window_left, pp.causal, c);
-      for (int hk = 0; hk < pp.hkv; ++hk) {
-        int4* dst = pp.work[k] + (size_t)hk * total[k] + excl[k];
+      int4* dst = pp.work[k] + (size_t)excl[k] * pp.hkv;
+      for (int hk = 0; hk < pp.hkv; ++hk)
         for (int rt = 0; rt < rts; ++rt)
-          for (int s = 0; s < ns; ++s) dst[rt * ns + s] = make_int4(b, rt, hk | (s << 16), ns);
-      }
+          for (int s = 0; s < ns; ++s) *dst++ = make_int4(b, rt, hk | (s << 16), ns);
       excl[k] += rts * ns;
     }
   }

@@ -72,21 +72,22 @@ int quantize_q_fp8(const void* q_bf16, void* q_e4m3, const float* q_descale, lon
 
 /*
  * fp8pa_workspace_size — bytes of device workspace fp8_paged_attn_fwd needs for
- * these host-known sizes (same values as passed to fp8_paged_attn_fwd).  The
+ * these host-known sizes and Q dtype (same values as passed to fp8_paged_attn_fwd).  The
  * workspace holds the device-built work list and, when the split count is
  * above 1, the per-split partial outputs and log-sum-exps.  Returns 0 for
  * arguments fp8_paged_attn_fwd would reject.
  */
 size_t fp8pa_workspace_size(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv,
-                            int head_dim, int max_pages_per_seq, int window_left, int num_splits);
+                            int head_dim, int q_dtype, int max_pages_per_seq, int window_left, int num_splits);
 
 /*
  * fp8pa_num_splits — the split-KV count fp8_paged_attn_fwd uses for these
  * host-known sizes (num_splits = 0 asks for the automatic choice, which is a
- * pure function of its arguments and the SM count, so it is CUDA-graph safe).
+ * pure function of its arguments, the SM count and the kernel variant's CTAs
+ * per SM, so it is CUDA-graph safe).
  * Returns 0 for arguments fp8_paged_attn_fwd would reject.
  */
-int fp8pa_num_splits(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
+int fp8pa_num_splits(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim, int q_dtype,
                      int max_pages_per_seq, int window_left, int num_splits);
 
 /*
@@ -144,7 +145,7 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
  * LSE combine when the split count is above 1).  0 for rejected arguments.
  */
 int fp8pa_kernel_launches(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv,
-                          int head_dim, int max_pages_per_seq, int window_left, int num_splits);
+                          int head_dim, int q_dtype, int max_pages_per_seq, int window_left, int num_splits);
 
 /*
  * fp8pa_set_timing_events — profiling hook for the calling host thread.  When

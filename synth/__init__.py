@@ -260,6 +260,9 @@ CONFIG_NAMES = [
     "mixed_hd512_causal",          # same batch, D 512 causal, Hq 32 / Hkv 4, BF16 Q
     "mixed_hd512_causal_fp8q",     # same batch, FP8 Q
     "spec_verify_hd512",           # 64 x 4 causal queries, 25600 shared + 3072 unique keys, BF16 Q
+    "chunk_hd256_swa",             # the mixed batch's 4096-token chunk alone (prefill, tensor-bound)
+    "chunk_hd512_causal",
+    "chunk_hd512_causal_fp8q",
 ]
 
 
@@ -290,6 +293,11 @@ def make_config(name: str, device="cpu", scale_batch: float = 1.0) -> Workload:
         if name == "mixed_hd256_swa":
             return make_workload(name, lq, lk, 32, 16, 256, 1023, True, True, seed=3, device=device)
         return make_workload(name, lq, lk, 32, 4, 512, -1, True, name.endswith("fp8q"), seed=3, device=device)
+    if name == "chunk_hd256_swa":
+        return make_workload(name, [4096], [8192], 32, 16, 256, 1023, True, True, seed=3, device=device)
+    if name in ("chunk_hd512_causal", "chunk_hd512_causal_fp8q"):
+        return make_workload(name, [4096], [8192], 32, 4, 512, -1, True, name.endswith("fp8q"), seed=3,
+                             device=device)
     if name == "spec_verify_hd512":
         B = nb(64)
         lk = [25600 + 3072] * B

@@ -73,20 +73,27 @@ def test_quantize_rejects_bad_arguments():
 
 
 def test_workspace_and_splits_are_host_functions():
+    E4M3, BF16 = fp8pa.FP8PA_E4M3, fp8pa.FP8PA_BF16
     # SWA decode: 64 x 1 query, Hq 32 / Hkv 16, D 256, window 1023, 144 pages
-    ws = fp8pa.workspace_size(64, 64, 1, 32, 16, 256, 144, 1023, 0)
-    s = fp8pa.num_splits(64, 64, 1, 32, 16, 256, 144, 1023, 0)
+    ws = fp8pa.workspace_size(64, 64, 1, 32, 16, 256, E4M3, 144, 1023, 0)
+    s = fp8pa.num_splits(64, 64, 1, 32, 16, 256, E4M3, 144, 1023, 0)
     assert ws > 0 and 1 <= s <= 64
-    assert ws == fp8pa.workspace_size(64, 64, 1, 32, 16, 256, 144, 1023, 0)
+    assert ws == fp8pa.workspace_size(64, 64, 1, 32, 16, 256, E4M3, 144, 1023, 0)
     # explicit split count is honoured and grows the workspace by the partial buffers
-    w1 = fp8pa.workspace_size(64, 64, 1, 32, 4, 512, 144, -1, 1)
-    w4 = fp8pa.workspace_size(64, 64, 1, 32, 4, 512, 144, -1, 4)
-    assert fp8pa.num_splits(64, 64, 1, 32, 4, 512, 144, -1, 4) == 4
+    w1 = fp8pa.workspace_size(64, 64, 1, 32, 4, 512, BF16, 144, -1, 1)
+    w4 = fp8pa.workspace_size(64, 64, 1, 32, 4, 512, BF16, 144, -1, 4)
+    assert fp8pa.num_splits(64, 64, 1, 32, 4, 512, BF16, 144, -1, 4) == 4
     assert w4 - w1 >= 4 * 64 * 32 * 512 * 4
-    # a long full-attention decode batch with few (sequence, head) units gets split
-    assert fp8pa.num_splits(64, 64, 1, 32, 4, 512, 144, -1, 0) > 1
+    # fewer (sequence, KV head) units than SMs: long contexts get split; plenty of units: no split
+    assert fp8pa.num_splits(8, 8, 1, 32, 4, 512, BF16, 144, -1, 0) > 1
+    assert fp8pa.num_splits(8, 8, 1, 32, 4, 512, E4M3, 144, -1, 0) > 1
+    assert fp8pa.num_splits(64, 64, 1, 32, 4, 512, E4M3, 144, -1, 0) == 1
     # the mixed chunked-prefill batch has plenty of units: no split
-    assert fp8pa.num_splits(4033, 8128, 4096, 32, 16, 256, 128, 1023, 0) == 1
+    assert fp8pa.num_splits(4033, 8128, 4096, 32, 16, 256, E4M3, 128, 1023, 0) == 1
+    # launches: plan + attention (+ combine when split)
+    assert fp8pa.kernel_launches(4033, 8128, 4096, 32, 16, 256, E4M3, 128, 1023, 0) == 3  # two row classes
+    assert fp8pa.kernel_launches(64, 64, 1, 32, 4, 512, BF16, 144, -1, 1) == 2
     # rejected shapes size to 0
-    assert fp8pa.workspace_size(1, 1, 1, 32, 16, 128, 4, -1, 0) == 0
-    assert fp8pa.num_splits(1, 1, 1, 30, 16, 256, 4, -1, 0) == 0
+    assert fp8pa.workspace_size(1, 1, 1, 32, 16, 128, E4M3, 4, -1, 0) == 0
+    assert fp8pa.workspace_size(1, 1, 1, 32, 16, 256, BF16, 4, -1, 0) == 0
+    assert fp8pa.num_splits(1, 1, 1, 30, 16, 256, E4M3, 4, -1, 0) == 0
