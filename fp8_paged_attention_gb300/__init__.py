@@ -72,6 +72,12 @@ def load_library():
             c.c_int, c.c_float, c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_size_t, c.c_void_p, c.c_void_p,
             c.c_void_p,
         ]
+        lib.fp8_paged_attn_fwd_noalloc.restype = c.c_int
+        lib.fp8_paged_attn_fwd_noalloc.argtypes = [
+            c.c_void_p, c.c_int, c.c_void_p, c.c_void_p, c.c_int, c.c_void_p, c.c_int, c.c_void_p, c.c_void_p,
+            c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p, c.c_int,
+            c.c_int, c.c_float, c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p,
+        ]
         lib.fp8pa_get_device_status.restype = c.c_int
         lib.fp8pa_get_device_status.argtypes = [c.c_void_p, c.c_void_p]
         lib.fp8pa_reset_device_status.restype = c.c_int

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(LIB_DIR, "libfp8pa.so")
 
 SOURCES = [
     "api.cu",
+    "noalloc.cu",
     "plan_combine.cu",
     "quantize_q.cu",
     "attn_fp8_d256.cu",

@@ -70,6 +70,13 @@ int fail(int code, const char* fmt, ...) {
   return code;
 }
 
+}  // namespace
+
+// Records `msg` as the message fp8pa_last_error() returns on this thread.
+int fp8pa::set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
+namespace {
+
 int cuda_fail(cudaError_t e, const char* what) {
   return fail(FP8PA_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }

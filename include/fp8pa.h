@@ -71,6 +71,40 @@ int quantize_q_fp8(const void* q_bf16, void* q_e4m3, const float* q_descale, lon
                    fp8pa_stream_t stream);
 
 /*
+ * fp8_paged_attn_fwd_noalloc — the same forward as fp8_paged_attn_fwd (same
+ * arguments, layouts and results) for callers that cannot allocate device
+ * memory at call time: for instance an inference engine that reserves nearly
+ * all HBM for its KV-cache pool at start-up, or a plugin host that gives the
+ * library no allocator.  It allocates nothing: its scratch is a device array
+ * of FP8PA_NOALLOC_SCRATCH_BYTES inside the library, which every device that
+ * loads the library holds until the process exits.  The caller passes only
+ * inputs and outputs.
+ *
+ * Limits and rules:
+ *  - A call whose scratch need (fp8pa_workspace_size for the same arguments)
+ *    exceeds FP8PA_NOALLOC_SCRATCH_BYTES is rejected with FP8PA_EINVAL and a
+ *    message; nothing is launched.  Splits above 1 need the most scratch.
+ *  - All calls share the one array on a device: calls whose kernels may
+ *    overlap on the GPU (e.g. on different streams without ordering) race and
+ *    give undefined results.  Calls ordered on one stream are fine; each call
+ *    rewrites all the scratch it reads, so nothing must be cleared between calls.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture on that device.
+ * This entry point has no counterpart on the source pages: it is a deployment
+ * convenience of this library.
+ */
+#define FP8PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int fp8_paged_attn_fwd_noalloc(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* v_cache,
+                               int num_pages, const int32_t* block_table, int max_pages_per_seq,
+                               const int32_t* cu_seqlens_q, const int32_t* seqused_k, int batch, int total_q,
+                               int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
+                               const float* q_descale, const float* k_descale, const float* v_descale,
+                               int descale_batch_stride, int descale_head_stride, float softmax_scale,
+                               int window_left, int causal, int num_splits, void* out, float* lse,
+                               fp8pa_stream_t stream);
+
+/*
  * fp8pa_workspace_size — bytes of device workspace fp8_paged_attn_fwd needs for
  * these host-known sizes and Q dtype (same values as passed to fp8_paged_attn_fwd).  The
  * workspace holds the device-built work list and, when the split count is
