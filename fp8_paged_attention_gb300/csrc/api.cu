@@ -419,6 +419,7 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
     p.cls = pl.cls[k];
     p.work = reinterpret_cast<const int4*>(ws + pl.off_work[k]);
     p.work_count = counts + k;
+    p.work_next = counts + 2 + k;
     e = launch_attn(head_dim, fp8_q, pl.cls[k].rows, ctas_per_sm(head_dim, fp8_q, pl.cls[k].rows), p, tm_q[k], tm_k,
                     tm_v, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");

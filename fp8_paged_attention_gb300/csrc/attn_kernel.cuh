@@ -13,10 +13,11 @@
 // shares every K/V page among all heads of its group and all query tokens of
 // the tile.  Keys sit on the 128 TMEM lanes; each softmax thread owns one key.
 //
-// Warp roles: warp 0 issues TMA loads (Q tile, then K/V page tiles in the
-// order the MMAs consume them), warp 1 allocates tensor memory and issues the
-// MMAs from one thread, warps 2-5 run the softmax, the O rescale and the
-// epilogue.  On the BF16-Q path warps 6-9 turn each E4M3 K/V stage into BF16
+// Warp roles: warp 0 takes work items from a global counter, publishes each
+// decoded item to the other roles through a small ring in shared memory, and
+// issues the TMA loads (Q tile, then K/V page tiles in the order the MMAs
+// consume them); warp 1 allocates tensor memory and issues the MMAs from one
+// thread; warps 2-5 run the softmax, the O rescale and the epilogue.  On the BF16-Q path warps 6-9 turn each E4M3 K/V stage into BF16
 // operand tiles (exact: every E4M3 value is a BF16 value).
 //
 // FP8 path (E4M3 Q): QK^T and PV are kind::f8f6f4 MMAs.  P is requantized to
@@ -57,7 +58,7 @@ struct AttnCfg {
   // opt-in maximum per block; two blocks share the SM's 228 KB minus 1 KB reserved each
   static constexpr int kSmemLimit = kCtas == 1 ? 232448 : 115712;
   // barriers (< 1 KB) + per-row softmax state: red[2][4][N], lred[4][N], 4 x [N] floats
-  static constexpr int kCtrlBytes = 1024 + 64 * N + 64;
+  static constexpr int kCtrlBytes = 1536 + 64 * N + 64;  // + the item ring
   static constexpr int kQBufs = kFP8 ? ((2 * kQBytes <= 65536) ? 2 : 1) : ((2 * kQBytes <= 32768) ? 2 : 1);
   static constexpr int kBfSlots = kFP8 ? 0 : 2;
   static constexpr int kFixed = kQBufs * kQBytes + 2 * kPBytes + kBfSlots * kBfSlotBytes + kCtrlBytes + 1024;
@@ -162,6 +163,13 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2_bf16x2(uint16_t v) {
 
 }  // namespace detail
 
+// One published work item; valid = 0 marks the end of the CTA's work.
+struct ItemSlot {
+  Item it;
+  int valid;
+};
+constexpr int kItemSlots = 4;
+
 template <int D, bool kFP8, int N, int kCtas>
 __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
     attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
@@ -195,7 +203,10 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
   uint64_t* o_empty = pv_done + 2;
   uint64_t* v_ready = o_empty + 1;  // tail tile: its V stages have landed (MMA thread -> softmax)
   uint64_t* drain = v_ready + 1;
-  float* red = reinterpret_cast<float*>(drain + 1);  // [2][4][N] per-warp tile maxima
+  uint64_t* item_full = drain + 1;
+  uint64_t* item_empty = item_full + kItemSlots;
+  ItemSlot* islot = reinterpret_cast<ItemSlot*>(item_empty + kItemSlots);
+  float* red = reinterpret_cast<float*>(islot + kItemSlots);  // [2][4][N] per-warp tile maxima
   float* lred = red + 2 * 4 * N;                      // [4][N] per-warp row sums
   float* m_s = lred + 4 * N;                          // [N] running max (log2 units)
   float* a_s = m_s + N;                               // [N] rescale factor of this tile
@@ -228,6 +239,10 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
     mbar_init(o_empty, 4);
     mbar_init(v_ready, 1);
     mbar_init(drain, 1);
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_empty[i], kFP8 ? 5 : 9);  // MMA thread + 4 softmax warps (+ 4 dequant warps)
+    }
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_q);
@@ -250,8 +265,17 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
     if (lane == 0) {
       uint32_t idx = 0, qit = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const Item it = decode_item(p, p.work[w]);
+      for (uint32_t ik = 0; ok; ++ik) {
+        const int w = atomicAdd(p.work_next, 1);
+        const bool valid = w < n_items;
+        const uint32_t is = ik % kItemSlots;
+        if (!(ok = pwait(&item_empty[is], ((ik / kItemSlots) & 1) ^ 1, lim, abort_flag))) break;
+        Item it{};
+        if (valid) it = decode_item(p, p.work[w]);
+        islot[is].it = it;
+        islot[is].valid = valid;
+        mbar_arrive(&item_full[is]);  // release: the slot's contents are visible to waiters
+        if (!valid) break;
         if (it.t1 <= it.t0) continue;
         const int qb = qit % QB;
         if (!(ok = pwait(&q_empty[qb], ((qit / QB) & 1) ^ 1, lim, abort_flag))) break;
@@ -296,8 +320,13 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
       constexpr uint32_t idesc_pv = make_idesc(kFmt, kMNMajor, kMNMajor, 128, N);
       uint32_t idx = 0, g = 0, qit = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const Item it = decode_item(p, p.work[w]);
+      for (uint32_t ik = 0; ok; ++ik) {
+        const uint32_t is = ik % kItemSlots;
+        if (!(ok = pwait(&item_full[is], (ik / kItemSlots) & 1, lim, abort_flag))) break;
+        const Item it = islot[is].it;
+        const bool valid = islot[is].valid != 0;
+        mbar_arrive(&item_empty[is]);
+        if (!valid) break;
         if (it.t1 <= it.t0) continue;
         const int qb = qit % QB;
         if (!(ok = pwait(&q_full[qb], (qit / QB) & 1, lim, abort_flag))) break;
@@ -406,8 +435,25 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
     const float NEG_INF = __int_as_float(0xFF800000);
     uint32_t g = 0, sbase = 0, tails = 0;
     bool aborted = false;
-    for (int w = blockIdx.x; w < n_items && !aborted; w += gridDim.x) {
-      const Item it = decode_item(p, p.work[w]);
+    for (uint32_t ik = 0; !aborted; ++ik) {
+      const uint32_t is = ik % kItemSlots;
+      bool iok = pwait(&item_full[is], (ik / kItemSlots) & 1, lim, abort_flag);
+      iok = __all_sync(0xFFFFFFFFu, iok);
+      Item it{};
+      bool valid = false;
+      if (iok) {
+        it = islot[is].it;
+        valid = islot[is].valid != 0;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&item_empty[is]);
+      } else {
+        flag_timeout(p, abort_flag);
+      }
+      if (bar_red_or(1, 128, !iok)) {  // all four warps leave together
+        aborted = true;
+        break;
+      }
+      if (!valid) break;
       const int G = p.group;
       const bool split_out = it.nsplit > 1;
       auto row_tok = [&](int n) { return it.q0 + (it.row0 + n) / G; };
@@ -700,8 +746,15 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
       const int dt = threadIdx.x - 192;  // 0..127
       uint32_t idx = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const Item it = decode_item(p, p.work[w]);
+      for (uint32_t ik = 0; ok; ++ik) {
+        const uint32_t is = ik % kItemSlots;
+        ok = __all_sync(0xFFFFFFFFu, pwait(&item_full[is], (ik / kItemSlots) & 1, lim, abort_flag));
+        if (!ok) break;
+        const Item it = islot[is].it;
+        const bool valid = islot[is].valid != 0;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&item_empty[is]);
+        if (!valid) break;
         if (it.t1 <= it.t0) continue;
         const int n = it.t1 - it.t0;
         auto convert_tile = [&](int u, bool is_v) -> bool {

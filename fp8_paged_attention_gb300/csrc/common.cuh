@@ -44,6 +44,7 @@ struct AttnParams {
   ClassInfo cls;
   const int4* work;        // items of this class
   const int* work_count;   // number of items
+  int* work_next;          // dynamic item counter (zeroed by the plan kernel)
   unsigned* status;
   uint32_t wait_limit;
 };

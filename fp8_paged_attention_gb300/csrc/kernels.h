@@ -14,7 +14,7 @@ struct PlanParams {
   int num_classes;
   ClassInfo cls[2];
   int4* work[2];
-  int* counts;  // [2]
+  int* counts;  // [4]: item counts of the two classes, then their dynamic counters
   unsigned* status;
 };
 

@@ -69,7 +69,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
   int excl[2] = {sums[0][tid] - cnt[0], sums[1][tid] - cnt[1]};
   const int total[2] = {sums[0][kPlanThreads - 1], sums[1][kPlanThreads - 1]};
   if (tid == 0)
-    for (int k = 0; k < 2; ++k) pp.counts[k] = k < pp.num_classes ? total[k] * pp.hkv : 0;
+    for (int k = 0; k < 2; ++k) {
+      pp.counts[k] = k < pp.num_classes ? total[k] * pp.hkv : 0;
+      pp.counts[2 + k] = 0;  // the attention kernel's dynamic item counter
+    }
   for (int b = b0; b < b1; ++b) {
     const int Lq = seq_lq(pp, b);
     const int Lk = clamp_lk(pp.seqused_k[b], pp.max_pages);
