@@ -61,8 +61,11 @@ def cu_from_lq(lq):
     return cu
 
 
-# Tolerances on unit-scale outputs: (max, mean) of |gpu - oracle| / s, where s
-# is the scale the V channel was drawn with (1, or 8 for the boosted channels).
+# Tolerances on unit-scale outputs: (max, mean) of |gpu - oracle| / max(s, |oracle|),
+# where s is the scale the V channel was drawn with (1, or 8 for the boosted
+# channels).  The output is bf16, which carries up to 2^-9 of |o| of rounding
+# error whatever the arithmetic, so an output above its channel's scale is
+# measured relative to its own magnitude.
 TOL = {True: (3e-2, 3e-3), False: (1e-2, 1e-3)}   # keyed by "FP8-MMA path"
 LSE_REPORT = {True: 2e-2, False: 5e-3}            # reported; gated only loosely
 LSE_GATE = 0.1
@@ -76,7 +79,7 @@ def unit_scale_errors(gpu_out: np.ndarray, ref_out: np.ndarray, w, heads=None):
     else:
         s = w.v_channel_scale[np.asarray(heads) // G]
     diff = np.abs(gpu_out.astype(np.float64) - ref_out)
-    e = diff / s
+    e = diff / np.maximum(s, np.abs(ref_out))
     return dict(max=float(e.max()) if e.size else 0.0, mean=float(e.mean()) if e.size else 0.0,
                 raw_max=float(diff.max()) if diff.size else 0.0)
 

@@ -79,6 +79,26 @@ def test_attention_cases(case):
     check(w, out, lse)
 
 
+BF16_CASES = [c for c in CASES if not c[8]]
+
+
+@pytest.mark.parametrize("case", BF16_CASES, ids=[c[0] for c in BF16_CASES])
+def test_bf16_q_literal_v_dequant_path(case):
+    """The BF16-Q path with V also dequantized to BF16 (BF16 P, BF16 PV MMA)."""
+    import fp8_paged_attention_gb300 as fp8pa
+    name, lq, lk, hq, hkv, d, wl, causal, fp8 = case
+    w = make(name, lq, lk, hq, hkv, d, wl, causal, fp8, seed=len(name) + 1)
+    fp8pa.set_bf16_dequant_v(True)
+    try:
+        out, lse = run_gpu(w)
+        out3, lse3 = run_gpu(w, num_splits=3)
+    finally:
+        fp8pa.set_bf16_dequant_v(False)
+    ref = oracle.paged_attention(oracle_problem(w))
+    check(w, out, lse, ref=ref)
+    check(w, out3, lse3, ref=ref)
+
+
 def test_empty_rows_and_sequences():
     # seq 0: 5 queries on 3 keys (the first two see nothing); seq 1: no keys; seq 2: no queries
     w = make("empty", [5, 2, 0, 1], [3, 0, 10, 9], 4, 2, 256, -1, True, True)
@@ -135,7 +155,7 @@ def test_per_batch_head_descales():
     for t in range(w.total_q):
         for h in range(8):
             s = w.v_channel_scale[h // G] * float(vd[tok_seq[t], h // G] / w.v_descale)
-            assert np.max(np.abs(g[t, h] - ro[t, h]) / s) <= TOL[True][0]
+            assert np.max(np.abs(g[t, h] - ro[t, h]) / np.maximum(s, np.abs(ro[t, h]))) <= TOL[True][0]
     assert lse_error(lse.cpu().numpy(), rl) <= LSE_GATE
 
 
