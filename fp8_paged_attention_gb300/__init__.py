@@ -18,7 +18,7 @@ from . import _build
 
 __all__ = [
     "build", "load_library", "library_path", "quantize_q_fp8", "fp8_paged_attn_fwd", "workspace_size",
-    "num_splits", "kernel_launches", "set_timing_events", "set_ctas_per_sm", "get_device_status", "reset_device_status",
+    "num_splits", "kernel_launches", "set_timing_events", "set_ctas_per_sm", "set_bf16_dequant_v", "get_device_status", "reset_device_status",
     "set_wait_limit", "FP8PA_BF16", "FP8PA_E4M3",
     "DEV_BAD_PAGE", "DEV_TIMEOUT", "DEV_BAD_LENGTH", "PAGE_SIZE", "Fp8paError",
 ]
@@ -88,6 +88,8 @@ def load_library():
         lib.fp8pa_set_wait_limit.argtypes = [c.c_uint]
         lib.fp8pa_kernel_launches.restype = c.c_int
         lib.fp8pa_kernel_launches.argtypes = [c.c_int] * 10
+        lib.fp8pa_set_bf16_dequant_v.restype = None
+        lib.fp8pa_set_bf16_dequant_v.argtypes = [c.c_int]
         lib.fp8pa_set_ctas_per_sm.restype = None
         lib.fp8pa_set_ctas_per_sm.argtypes = [c.c_int]
         lib.fp8pa_set_timing_events.restype = None
@@ -146,6 +148,12 @@ def set_timing_events(start=None, stop=None):
 def set_ctas_per_sm(ctas: int):
     """Tuning hook: force 1 or 2 attention CTAs per SM (0 = automatic)."""
     load_library().fp8pa_set_ctas_per_sm(int(ctas))
+
+
+def set_bf16_dequant_v(on: bool):
+    """BF16-Q path: keep V E4M3 with a hi/lo E4M3 P (False, default) or
+    dequantize V to BF16 with a BF16 P (True)."""
+    load_library().fp8pa_set_bf16_dequant_v(int(bool(on)))
 
 
 def quantize_q_fp8(q: torch.Tensor, q_descale: torch.Tensor, out: torch.Tensor | None = None, stream=None):

@@ -26,6 +26,7 @@ SOURCES = [
     "attn_fp8_d256.cu",
     "attn_fp8_d512.cu",
     "attn_bf16_d512.cu",
+    "attn_bf16dqv_d512.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -14,28 +14,31 @@
 #include "kernels.h"
 
 namespace fp8pa {
-cudaError_t launch_attn_fp8_d256(int, int, const AttnParams&, const CUtensorMap&, const CUtensorMap&,
-                                 const CUtensorMap&, int, cudaStream_t);
-cudaError_t launch_attn_fp8_d512(int, int, const AttnParams&, const CUtensorMap&, const CUtensorMap&,
-                                 const CUtensorMap&, int, cudaStream_t);
-cudaError_t launch_attn_bf16_d512(int, int, const AttnParams&, const CUtensorMap&, const CUtensorMap&,
-                                  const CUtensorMap&, int, cudaStream_t);
-int smem_attn_fp8_d256(int, int);
-int smem_attn_fp8_d512(int, int);
-int smem_attn_bf16_d512(int, int);
+#define FP8PA_DECLARE_VARIANT(name)                                                                          \
+  cudaError_t launch_##name(int, int, const AttnParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, \
+                            int, cudaStream_t);                                                             \
+  int smem_##name(int, int);
+FP8PA_DECLARE_VARIANT(attn_fp8_d256)
+FP8PA_DECLARE_VARIANT(attn_fp8_d512)
+FP8PA_DECLARE_VARIANT(attn_bf16_d512)
+FP8PA_DECLARE_VARIANT(attn_bf16dqv_d512)
+#undef FP8PA_DECLARE_VARIANT
 
-cudaError_t launch_attn(int head_dim, bool fp8_q, int rows, int ctas, const AttnParams& p, const CUtensorMap& tm_q,
+cudaError_t launch_attn(int head_dim, int path, int rows, int ctas, const AttnParams& p, const CUtensorMap& tm_q,
                         const CUtensorMap& tm_k, const CUtensorMap& tm_v, int sms, cudaStream_t stream) {
-  if (head_dim == 256 && fp8_q) return launch_attn_fp8_d256(rows, ctas, p, tm_q, tm_k, tm_v, sms, stream);
-  if (head_dim == 512 && fp8_q) return launch_attn_fp8_d512(rows, ctas, p, tm_q, tm_k, tm_v, sms, stream);
-  if (head_dim == 512 && !fp8_q) return launch_attn_bf16_d512(rows, ctas, p, tm_q, tm_k, tm_v, sms, stream);
+  if (head_dim == 256 && path == kPathE4M3) return launch_attn_fp8_d256(rows, ctas, p, tm_q, tm_k, tm_v, sms, stream);
+  if (head_dim == 512 && path == kPathE4M3) return launch_attn_fp8_d512(rows, ctas, p, tm_q, tm_k, tm_v, sms, stream);
+  if (head_dim == 512 && path == kPathBf16) return launch_attn_bf16_d512(rows, ctas, p, tm_q, tm_k, tm_v, sms, stream);
+  if (head_dim == 512 && path == kPathBf16DqV)
+    return launch_attn_bf16dqv_d512(rows, ctas, p, tm_q, tm_k, tm_v, sms, stream);
   return cudaErrorInvalidValue;
 }
 
-int attn_smem_bytes(int head_dim, bool fp8_q, int rows, int ctas) {
-  if (head_dim == 256 && fp8_q) return smem_attn_fp8_d256(rows, ctas);
-  if (head_dim == 512 && fp8_q) return smem_attn_fp8_d512(rows, ctas);
-  if (head_dim == 512 && !fp8_q) return smem_attn_bf16_d512(rows, ctas);
+int attn_smem_bytes(int head_dim, int path, int rows, int ctas) {
+  if (head_dim == 256 && path == kPathE4M3) return smem_attn_fp8_d256(rows, ctas);
+  if (head_dim == 512 && path == kPathE4M3) return smem_attn_fp8_d512(rows, ctas);
+  if (head_dim == 512 && path == kPathBf16) return smem_attn_bf16_d512(rows, ctas);
+  if (head_dim == 512 && path == kPathBf16DqV) return smem_attn_bf16dqv_d512(rows, ctas);
   return 0;
 }
 }  // namespace fp8pa
@@ -49,15 +52,20 @@ __device__ unsigned int g_status;
 thread_local char g_err[512] = "";
 thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
 std::atomic<int> g_ctas_override{0};
+std::atomic<int> g_dequant_v{0};
+
+// Kernel path for a Q dtype: E4M3 Q, or BF16 Q with V kept E4M3 (default) or
+// dequantized to BF16 (fp8pa_set_bf16_dequant_v).
+int kernel_path(bool fp8_q) { return fp8_q ? kPathE4M3 : (g_dequant_v.load() ? kPathBf16DqV : kPathBf16); }
 
 // CTAs per SM for a kernel variant: two co-resident CTAs where both fit
-// (E4M3 Q with up to 32 rows per tile), else one.
-int ctas_per_sm(int head_dim, bool fp8_q, int rows) {
+// (16-row tiles of the E4M3-Q path), else one.
+int ctas_per_sm(int head_dim, int path, int rows) {
   const int forced = g_ctas_override.load();
   if (forced == 1 || forced == 2) {
-    if (attn_smem_bytes(head_dim, fp8_q, rows, forced) > 0) return forced;
+    if (attn_smem_bytes(head_dim, path, rows, forced) > 0) return forced;
   }
-  if (fp8_q && rows == 16 && attn_smem_bytes(head_dim, fp8_q, rows, 2) > 0) return 2;
+  if (rows == 16 && attn_smem_bytes(head_dim, path, rows, 2) > 0) return 2;
   return 1;
 }
 std::atomic<unsigned> g_wait_limit{0};
@@ -263,6 +271,8 @@ void fp8pa_set_wait_limit(unsigned int max_iterations) { g_wait_limit.store(max_
 
 void fp8pa_set_ctas_per_sm(int ctas) { g_ctas_override.store(ctas); }
 
+void fp8pa_set_bf16_dequant_v(int on) { g_dequant_v.store(on ? 1 : 0); }
+
 void fp8pa_set_timing_events(void* start_event, void* stop_event) {
   g_ev_start = static_cast<cudaEvent_t>(start_event);
   g_ev_stop = static_cast<cudaEvent_t>(stop_event);
@@ -420,7 +430,8 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
     p.work = reinterpret_cast<const int4*>(ws + pl.off_work[k]);
     p.work_count = counts + k;
     p.work_next = counts + 2 + k;
-    e = launch_attn(head_dim, fp8_q, pl.cls[k].rows, ctas_per_sm(head_dim, fp8_q, pl.cls[k].rows), p, tm_q[k], tm_k,
+    const int path = kernel_path(fp8_q);
+    e = launch_attn(head_dim, path, pl.cls[k].rows, ctas_per_sm(head_dim, path, pl.cls[k].rows), p, tm_q[k], tm_k,
                     tm_v, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   }

@@ -17,17 +17,24 @@
 // decoded item to the other roles through a small ring in shared memory, and
 // issues the TMA loads (Q tile, then K/V page tiles in the order the MMAs
 // consume them); warp 1 allocates tensor memory and issues the MMAs from one
-// thread; warps 2-5 run the softmax, the O rescale and the epilogue.  On the BF16-Q path warps 6-9 turn each E4M3 K/V stage into BF16
-// operand tiles (exact: every E4M3 value is a BF16 value).
+// thread; warps 2-5 run the softmax, the O rescale and the epilogue.  On the
+// BF16-Q paths warps 6-9 dequantize each E4M3 K stage into BF16 straight into
+// tensor memory, where it is the A operand of the QK^T MMA (exact: every E4M3
+// value is a BF16 value); on the literal path they also dequantize V into BF16
+// shared-memory tiles.
 //
-// FP8 path (E4M3 Q): QK^T and PV are kind::f8f6f4 MMAs.  P is requantized to
-// E4M3 after a 2^4 pre-scale (P' = 2^(x - m + 4), at most 256 under the lazy
-// rescale below, keeping small weights out of E4M3's subnormal range) as a
-// pair on one scale:
+// Paths (template parameter kPath):
+//  kPathE4M3    E4M3 Q: QK^T and PV are kind::f8f6f4 MMAs.
+//  kPathBf16    BF16 Q: K dequantized to BF16, QK^T a kind::f16 MMA with BF16 Q;
+//               V stays E4M3 (exact) in a kind::f8f6f4 PV MMA.
+//  kPathBf16DqV BF16 Q: K and V dequantized to BF16, both MMAs kind::f16, P in BF16.
+// Where the PV MMA is E4M3, P is requantized to E4M3 after a 2^4 pre-scale
+// (P' = 2^(x - m + 4), at most 256 under the lazy rescale below, keeping small
+// weights out of E4M3's subnormal range) as a pair on one scale:
 // hi = e4m3(P'), lo = e4m3(P' - hi); both PV MMAs accumulate into the same
-// TMEM O, so P carries about 8 significant bits instead of E4M3's 4.  The row
-// sum accumulates hi + lo, so O / l is an exact convex combination of the V
-// rows the MMAs saw.  BF16 path: kind::f16 MMAs, P in BF16.
+// TMEM O, so P carries about 8 significant bits (BF16 carries 8) instead of
+// E4M3's 4.  The row sum accumulates the values the MMAs saw, so O / l is an
+// exact convex combination of V rows.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -42,41 +49,48 @@ namespace fp8pa {
 // kCtas: CTAs resident per SM.  Two co-resident CTAs run two independent
 // item pipelines per SM, hiding each other's per-item bubbles (epilogue,
 // first-tile latency); each then gets half the shared memory and TMEM.
-template <int D, bool kFP8, int N, int kCtas = 1>
+template <int D, int kPath, int N, int kCtas = 1>
 struct AttnCfg {
   static_assert(D == 256 || D == 512, "head dim");
   static_assert(N == 16 || N == 32 || N == 64, "rows per tile");
   static_assert(kCtas == 1 || kCtas == 2, "CTAs per SM");
+  static_assert(kPath >= 0 && kPath <= 2, "path");
+  static constexpr bool kQ8 = kPath == kPathE4M3;     // Q and K enter QK^T as E4M3
+  static constexpr bool kP8 = kPath != kPathBf16DqV;  // P (hi/lo) and V enter PV as E4M3
+  static constexpr bool kDq = kPath != kPathE4M3;     // dequant warps: K -> BF16 in TMEM
+  static constexpr bool kDqV = kPath == kPathBf16DqV; // ... and V -> BF16 in shared memory
   static constexpr int kDC = D / 128;                    // 128-byte chunks of an E4M3 row
-  static constexpr int kQChunkElems = kFP8 ? 128 : 64;   // Q elements per 128-byte chunk
+  static constexpr int kQChunkElems = kQ8 ? 128 : 64;    // Q elements per 128-byte chunk
   static constexpr int kQChunks = D / kQChunkElems;
   static constexpr int kQBytes = kQChunks * N * 128;
-  // P^T for 128 keys: FP8 path = E4M3 hi term then E4M3 lo term (N x 128 bytes each)
-  static constexpr int kPBytes = kFP8 ? 2 * N * 128 : N * 256;
+  // P^T for 128 keys: E4M3 hi term then E4M3 lo term (N x 128 bytes each), or BF16
+  static constexpr int kPBytes = kP8 ? 2 * N * 128 : N * 256;
   static constexpr int kBfSlotBytes = 32768;             // BF16 tile of 128 keys x 128 dims
-  static constexpr int kThreads = kFP8 ? 192 : 320;
+  static constexpr int kThreads = kDq ? 320 : 192;
   // opt-in maximum per block; two blocks share the SM's 228 KB minus 1 KB reserved each
   static constexpr int kSmemLimit = kCtas == 1 ? 232448 : 115712;
   // barriers (< 1 KB) + per-row softmax state: red[2][4][N], lred[4][N], 4 x [N] floats
   static constexpr int kCtrlBytes = 1536 + 64 * N + 64;  // + the item ring
-  static constexpr int kQBufs = kFP8 ? ((2 * kQBytes <= 65536) ? 2 : 1) : ((2 * kQBytes <= 32768) ? 2 : 1);
-  static constexpr int kBfSlots = kFP8 ? 0 : 2;
+  static constexpr int kQBufs = kQ8 ? ((2 * kQBytes <= 65536) ? 2 : 1) : ((2 * kQBytes <= 32768) ? 2 : 1);
+  static constexpr int kBfSlots = kDqV ? 2 : 0;
   static constexpr int kFixed = kQBufs * kQBytes + 2 * kPBytes + kBfSlots * kBfSlotBytes + kCtrlBytes + 1024;
   static constexpr int kStages = (kSmemLimit - kFixed) / kStageBytes > 16 ? 16 : (kSmemLimit - kFixed) / kStageBytes;
   static_assert(kStages >= 2, "smem");
-  // FP8 path: the tail tile's V chunks must fit in the ring together (the softmax zeroes them in place)
-  static_assert(!kFP8 || kStages >= kDC, "ring shorter than one tile's V");
-  static_assert(kCtas == 1 || 2 * (2 * N + (D / 128) * N) <= 512, "TMEM for two CTAs");
+  // E4M3 V: the tail tile's V chunks must fit in the ring together (the softmax zeroes them in place)
+  static_assert(!kP8 || kStages >= kDC, "ring shorter than one tile's V");
   static constexpr int kSmemBytes = kFixed + kStages * kStageBytes;
-  static constexpr int kTmemUsed = 2 * N + kDC * N;
+  // TMEM columns: S (2 buffers of N), O (kDC chunks of N), BF16 K (2 slots of 64 columns = 128 dims)
+  static constexpr int kKCol = 2 * N + kDC * N;
+  static constexpr int kTmemUsed = kKCol + (kDq ? 128 : 0);
   static constexpr uint32_t kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
                                         : kTmemUsed <= 256 ? 256 : 512;
+  static_assert(kTmemUsed <= 512 && kCtas * kTmemCols <= 512, "TMEM");
   // Lazy rescaling: the running max used for the exponent only moves when a
   // row's max grows by more than kTau (log2 units), so most tiles need no O
   // rescale.  P' = 2^(x - m_used + kPShift) <= 2^(kTau + kPShift) stays within
   // E4M3's range (<= 256 < 448) and keeps small weights out of its subnormals.
-  static constexpr float kTau = kFP8 ? 4.0f : 8.0f;
-  static constexpr float kPShift = kFP8 ? 4.0f : 0.0f;
+  static constexpr float kTau = kP8 ? 4.0f : 8.0f;
+  static constexpr float kPShift = kP8 ? 4.0f : 0.0f;
 };
 
 namespace detail {
@@ -170,16 +184,17 @@ struct ItemSlot {
 };
 constexpr int kItemSlots = 4;
 
-template <int D, bool kFP8, int N, int kCtas>
-__global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
+template <int D, int kPath, int N, int kCtas>
+__global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
     attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
-  using C = AttnCfg<D, kFP8, N, kCtas>;
+  using C = AttnCfg<D, kPath, N, kCtas>;
+  constexpr bool kQ8 = C::kQ8, kP8 = C::kP8, kDq = C::kDq, kDqV = C::kDqV;
   using namespace ptx;
   using namespace detail;
   constexpr int S = C::kStages;
   constexpr int SB = C::kBfSlots;
-  constexpr int SBm = SB > 0 ? SB : 1;  // modulus for the BF16 operand ring (unused on the FP8 path)
+  constexpr int SBm = SB > 0 ? SB : 1;  // modulus for the BF16 V ring (literal path only)
   constexpr int QB = C::kQBufs;
   constexpr int DC = C::kDC;
 
@@ -205,7 +220,9 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
   uint64_t* drain = v_ready + 1;
   uint64_t* item_full = drain + 1;
   uint64_t* item_empty = item_full + kItemSlots;
-  ItemSlot* islot = reinterpret_cast<ItemSlot*>(item_empty + kItemSlots);
+  uint64_t* kt_full = item_empty + kItemSlots;  // BF16 K slot in TMEM written (dequant -> MMA)
+  uint64_t* kt_empty = kt_full + 2;             // BF16 K slot consumed (MMA commit -> dequant)
+  ItemSlot* islot = reinterpret_cast<ItemSlot*>(kt_empty + 2);
   float* red = reinterpret_cast<float*>(islot + kItemSlots);  // [2][4][N] per-warp tile maxima
   float* lred = red + 2 * 4 * N;                      // [4][N] per-warp row sums
   float* m_s = lred + 4 * N;                          // [N] running max (log2 units)
@@ -220,11 +237,15 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&ring_full[i], 1);
-      mbar_init(&ring_empty[i], kFP8 ? 1 : 4);
+      mbar_init(&ring_empty[i], 1);  // one MMA commit or one arrive for the four dequant warps
     }
     for (int i = 0; i < SB; ++i) {
-      mbar_init(&bf_full[i], 4);
+      mbar_init(&bf_full[i], 1);
       mbar_init(&bf_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kt_full[i], 1);
+      mbar_init(&kt_empty[i], 1);
     }
     for (int i = 0; i < QB; ++i) {
       mbar_init(&q_full[i], 1);
@@ -241,7 +262,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
     mbar_init(drain, 1);
     for (int i = 0; i < kItemSlots; ++i) {
       mbar_init(&item_full[i], 1);
-      mbar_init(&item_empty[i], kFP8 ? 5 : 9);  // MMA thread + 4 softmax warps (+ 4 dequant warps)
+      mbar_init(&item_empty[i], kDq ? 9 : 5);  // MMA thread + 4 softmax warps (+ 4 dequant warps)
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -315,10 +336,11 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kFmt = kFP8 ? kFmtE4M3 : kFmtBF16;
-      constexpr uint32_t idesc_qk = make_idesc(kFmt, kKMajor, kKMajor, 128, N);
-      constexpr uint32_t idesc_pv = make_idesc(kFmt, kMNMajor, kMNMajor, 128, N);
-      uint32_t idx = 0, g = 0, qit = 0;
+      constexpr uint32_t idesc_qk = make_idesc(kQ8 ? kFmtE4M3 : kFmtBF16, kKMajor, kKMajor, 128, N);
+      constexpr uint32_t idesc_pv = make_idesc(kP8 ? kFmtE4M3 : kFmtBF16, kMNMajor, kMNMajor, 128, N);
+      // idx: position in the K/V stage stream (the ring); kidx: BF16 K chunks in TMEM;
+      // bidx: BF16 V tiles in shared memory
+      uint32_t idx = 0, kidx = 0, bidx = 0, g = 0, qit = 0;
       bool ok = true;
       for (uint32_t ik = 0; ok; ++ik) {
         const uint32_t is = ik % kItemSlots;
@@ -339,8 +361,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
           tc_fence_after();
           const uint32_t d_tmem = tmem + sb * N;
           for (int c = 0; c < DC; ++c) {
-            const uint32_t slot = idx % (kFP8 ? S : SBm);
-            if (kFP8) {
+            if (kQ8) {
+              const uint32_t slot = idx % S;
               if (!pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag)) return false;
               tc_fence_after();
               const uint32_t a0 = smem_u32(ring + slot * kStageBytes), b0 = qaddr + c * N * 128;
@@ -350,28 +372,31 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
                            make_sdesc(b0 + kk * 32, 16, 1024, kLayoutSW128), idesc_qk, (c | kk) != 0);
               mma_commit(&ring_empty[slot]);
             } else {
-              if (!pwait(&bf_full[slot], (idx / SBm) & 1, lim, abort_flag)) return false;
+              // BF16 K chunk (128 dims = 64 columns) in TMEM slot kidx & 1, written by the dequant warps
+              const uint32_t ks = kidx & 1;
+              if (!pwait(&kt_full[ks], (kidx >> 1) & 1, lim, abort_flag)) return false;
               tc_fence_after();
-              const uint32_t a0 = smem_u32(bfbuf + slot * C::kBfSlotBytes);
+              const uint32_t a_t = tmem + C::kKCol + ks * 64;
 #pragma unroll
-              for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  mma_f16(d_tmem, make_sdesc(a0 + h * 16384 + kk * 32, 16, 1024, kLayoutSW128),
-                          make_sdesc(qaddr + (2 * c + h) * N * 128 + kk * 32, 16, 1024, kLayoutSW128), idesc_qk,
-                          (c | h | kk) != 0);
-              mma_commit(&bf_empty[slot]);
+              for (int kk = 0; kk < 8; ++kk)
+                mma_f16_tmem_a(d_tmem, a_t + kk * 8,
+                               make_sdesc(qaddr + (2 * c + (kk >> 2)) * N * 128 + (kk & 3) * 32, 16, 1024,
+                                          kLayoutSW128),
+                               idesc_qk, (c | kk) != 0);
+              mma_commit(&kt_empty[ks]);
+              ++kidx;
             }
             ++idx;
           }
           mma_commit(&s_full[sb]);
           return true;
         };
-        // O^T += V^T . P^T(gg).  On a tail tile (keys past Lk) the softmax zeroes
-        // the V rows past Lk first; the in-order wait here tells it the stages landed.
+        // O^T += V^T . P^T(gg).  On a tail tile (keys past Lk) with E4M3 V the
+        // softmax zeroes the V rows past Lk first; the in-order wait here tells it
+        // the stages landed.
         auto pv = [&](uint32_t gg, bool first, bool tail) -> bool {
           const uint32_t pb = gg & 1;
-          if (kFP8 && tail) {
+          if (kP8 && tail) {
             for (int c = 0; c < DC; ++c)
               if (!pwait(&ring_full[(idx + c) % S], ((idx + c) / S) & 1, lim, abort_flag)) return false;
             mbar_arrive(v_ready);
@@ -382,8 +407,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
           const uint32_t paddr = smem_u32(pbuf + pb * C::kPBytes);
           for (int c = 0; c < DC; ++c) {
             const uint32_t d_tmem = tmem + 2 * N + c * N;
-            const uint32_t slot = idx % (kFP8 ? S : SBm);
-            if (kFP8) {
+            if (kP8) {
+              const uint32_t slot = idx % S;
               if (!pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag)) return false;
               tc_fence_after();
               const uint32_t a0 = smem_u32(ring + slot * kStageBytes);
@@ -396,7 +421,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
               }
               mma_commit(&ring_empty[slot]);
             } else {
-              if (!pwait(&bf_full[slot], (idx / SBm) & 1, lim, abort_flag)) return false;
+              const uint32_t slot = bidx % SBm;
+              if (!pwait(&bf_full[slot], (bidx / SBm) & 1, lim, abort_flag)) return false;
               tc_fence_after();
               const uint32_t a0 = smem_u32(bfbuf + slot * C::kBfSlotBytes);
 #pragma unroll
@@ -404,6 +430,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
                 mma_f16(d_tmem, make_sdesc(a0 + kk * 2048, 16384, 1024, kLayoutSW128),
                         make_sdesc(paddr + kk * 256, 128, 2048, kLayoutNone), idesc_pv, !(first && kk == 0));
               mma_commit(&bf_empty[slot]);
+              ++bidx;
             }
             ++idx;
           }
@@ -482,7 +509,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
       const int n_t = it.t1 - it.t0;
       const float kd = load_descale(p.k_descale, p, it);
       const float vd = load_descale(p.v_descale, p, it);
-      const float scale = p.softmax_scale_log2 * kd * (kFP8 ? *p.q_descale : 1.0f);
+      const float scale = p.softmax_scale_log2 * kd * (kQ8 ? *p.q_descale : 1.0f);
       if (wt < N) {
         m_s[wt] = NEG_INF;
         a_s[wt] = 1.0f;
@@ -573,7 +600,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (ok) {
           uint8_t* pdst = pbuf + pb * C::kPBytes;
-          if (kFP8) {
+          if (kP8) {
 #pragma unroll
             for (int blk = 0; blk < N / 16; ++blk) {
               if (blk * 16 >= it.nrows) break;
@@ -637,7 +664,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
           }
           // rows of the last page past the sequence end may hold anything (even NaN):
           // zero those V rows so that 0 * V stays 0 in the PV MMA
-          if (kFP8 && kb + kTileKeys > it.Lk) {
+          if (kP8 && kb + kTileKeys > it.Lk) {
             const int zr = max(0, it.Lk - kb);
             ok = pwait(v_ready, tails & 1, lim, abort_flag);
             ok = __all_sync(0xFFFFFFFFu, ok);
@@ -741,14 +768,26 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
       if (lane == 0) mbar_arrive(o_empty);
     }
   } else {
-    // ------------------------------------------------------------------ E4M3 -> BF16 operand tiles (BF16-Q path)
-    if (!kFP8) {
+    // ------------------------------------------------------------------ E4M3 -> BF16 dequant (BF16-Q paths)
+    if (kDq) {
       const int dt = threadIdx.x - 192;  // 0..127
-      uint32_t idx = 0;
+      const int quarter = warp & 3;
+      const int row = quarter * 32 + lane;  // this thread's key row = its TMEM lane
+      const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+      uint32_t idx = 0, kidx = 0, bidx = 0;
       bool ok = true;
+      // the four dequant warps hand a stage back with a single arrive
+      auto release = [&](uint64_t* a, uint64_t* b) {
+        named_bar_sync(3, 128);
+        if (dt == 0) {
+          mbar_arrive(a);
+          mbar_arrive(b);
+        }
+      };
       for (uint32_t ik = 0; ok; ++ik) {
         const uint32_t is = ik % kItemSlots;
-        ok = __all_sync(0xFFFFFFFFu, pwait(&item_full[is], (ik / kItemSlots) & 1, lim, abort_flag));
+        // every wait decision is a vote of all four dequant warps: they share named barrier 3
+        ok = !bar_red_or(3, 128, !pwait(&item_full[is], (ik / kItemSlots) & 1, lim, abort_flag));
         if (!ok) break;
         const Item it = islot[is].it;
         const bool valid = islot[is].valid != 0;
@@ -757,27 +796,67 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
         if (!valid) break;
         if (it.t1 <= it.t0) continue;
         const int n = it.t1 - it.t0;
-        auto convert_tile = [&](int u, bool is_v) -> bool {
-          const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
-          const int zero_from = (is_v && kb + kTileKeys > it.Lk) ? max(0, it.Lk - kb) : kTileKeys;
+        // K tile u: each chunk (128 dims) -> BF16 in TMEM slot kidx & 1, one key row per thread
+        auto convert_k = [&](int u) -> bool {
           for (int c = 0; c < DC; ++c) {
-            const uint32_t slot = idx % S, bslot = idx % SBm;
-            bool w_ok = pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag) &&
-                        pwait(&bf_empty[bslot], ((idx / SBm) & 1) ^ 1, lim, abort_flag);
-            if (!__all_sync(0xFFFFFFFFu, w_ok)) return false;
+            const uint32_t slot = idx % S, ks = kidx & 1;
+            const bool w_ok = pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag) &&
+                              pwait(&kt_empty[ks], ((kidx >> 1) & 1) ^ 1, lim, abort_flag);
+            if (bar_red_or(3, 128, !w_ok)) return false;
+            tc_fence_after();
+            const uint8_t* src = ring + slot * kStageBytes + row * 128;
+            uint4 vin[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) vin[j] = *reinterpret_cast<const uint4*>(src + ((j ^ (row & 7)) << 4));
+            const uint32_t ta = tmem + lane_base + C::kKCol + ks * 64;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              uint32_t o[16];
+#pragma unroll
+              for (int jj = 0; jj < 2; ++jj) {
+                const uint4 v = vin[2 * h + jj];
+                const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  o[jj * 8 + 2 * i] = cvt_e4m3x2_bf16x2((uint16_t)(in[i] & 0xFFFF));
+                  o[jj * 8 + 2 * i + 1] = cvt_e4m3x2_bf16x2((uint16_t)(in[i] >> 16));
+                }
+              }
+              tmem_store16(ta + h * 16, o);  // dims 32h .. 32h+31 -> columns 16h .. 16h+15
+            }
+            tc_fence_before();
+            release(&ring_empty[slot], &kt_full[ks]);
+            ++idx;
+            ++kidx;
+          }
+          return true;
+        };
+        // V tile u, literal path: -> BF16 in shared memory; rows past Lk become zeros
+        auto convert_v = [&](int u) -> bool {
+          if (!kDqV) {
+            idx += DC;  // the PV MMA reads these stages as E4M3
+            return true;
+          }
+          const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
+          const int zero_from = (kb + kTileKeys > it.Lk) ? max(0, it.Lk - kb) : kTileKeys;
+          for (int c = 0; c < DC; ++c) {
+            const uint32_t slot = idx % S, bslot = bidx % SBm;
+            const bool w_ok = pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag) &&
+                              pwait(&bf_empty[bslot], ((bidx / SBm) & 1) ^ 1, lim, abort_flag);
+            if (bar_red_or(3, 128, !w_ok)) return false;
             const uint8_t* src = ring + slot * kStageBytes;
             uint8_t* dst = bfbuf + bslot * C::kBfSlotBytes;
             uint4 vin[8];
 #pragma unroll
             for (int k8 = 0; k8 < 8; ++k8) {
-              const int x16 = dt + k8 * 128, row = x16 >> 3, c16 = x16 & 7;
-              vin[k8] = row < zero_from ? *reinterpret_cast<const uint4*>(src + row * 128 + ((c16 ^ (row & 7)) << 4))
-                                        : make_uint4(0, 0, 0, 0);
+              const int x16 = dt + k8 * 128, r = x16 >> 3, c16 = x16 & 7;
+              vin[k8] = r < zero_from ? *reinterpret_cast<const uint4*>(src + r * 128 + ((c16 ^ (r & 7)) << 4))
+                                      : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int k8 = 0; k8 < 8; ++k8) {
               const int x16 = dt + k8 * 128;
-              const int row = x16 >> 3, c16 = x16 & 7, sw = row & 7;
+              const int r = x16 >> 3, c16 = x16 & 7, sw = r & 7;
               const uint4 v = vin[k8];
               const uint32_t in[4] = {v.x, v.y, v.z, v.w};
               uint32_t o[8];
@@ -787,24 +866,21 @@ __global__ void __launch_bounds__(AttnCfg<D, kFP8, N, kCtas>::kThreads, kCtas)
                 o[2 * i + 1] = cvt_e4m3x2_bf16x2((uint16_t)(in[i] >> 16));
               }
               const int h = c16 >> 2, k0 = (c16 & 3) * 2;
-              uint8_t* drow = dst + h * 16384 + row * 128;
+              uint8_t* drow = dst + h * 16384 + r * 128;
               *reinterpret_cast<uint4*>(drow + ((k0 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
               *reinterpret_cast<uint4*>(drow + (((k0 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
             }
             fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              mbar_arrive(&ring_empty[slot]);
-              mbar_arrive(&bf_full[bslot]);
-            }
+            release(&ring_empty[slot], &bf_full[bslot]);
             ++idx;
+            ++bidx;
           }
           return true;
         };
-        ok = convert_tile(0, false);
+        ok = convert_k(0);
         for (int u = 1; u <= n && ok; ++u) {
-          if (u < n) ok = convert_tile(u, false);
-          if (ok) ok = convert_tile(u - 1, true);
+          if (u < n) ok = convert_k(u);
+          if (ok) ok = convert_v(u - 1);
         }
       }
       if (!ok) flag_timeout(p, abort_flag);

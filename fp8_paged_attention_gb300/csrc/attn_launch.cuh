@@ -5,16 +5,16 @@
 
 namespace fp8pa {
 
-template <int D, bool kFP8, int N, int kCtas>
+template <int D, int kPath, int N, int kCtas>
 cudaError_t launch_attn_variant(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, int sms, cudaStream_t stream) {
-  using C = AttnCfg<D, kFP8, N, kCtas>;
+  using C = AttnCfg<D, kPath, N, kCtas>;
   const int grid = sms * kCtas;
   // the attribute is per device; setting it again is cheap and capture-safe
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kFP8, N, kCtas>,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kPath, N, kCtas>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_fwd_kernel<D, kFP8, N, kCtas><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p, tm_q, tm_k, tm_v);
+  attn_fwd_kernel<D, kPath, N, kCtas><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p, tm_q, tm_k, tm_v);
   return cudaGetLastError();
 }
 

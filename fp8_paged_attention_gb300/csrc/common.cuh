@@ -14,6 +14,10 @@ constexpr uint32_t kDrainWaitLimit = 1u << 22;
 
 enum : unsigned { kDevBadPage = 1, kDevTimeout = 2, kDevBadLength = 4 };
 
+// Attention kernel paths: E4M3 Q; BF16 Q with K dequantized to BF16 and V kept
+// E4M3; BF16 Q with K and V dequantized to BF16.
+enum : int { kPathE4M3 = 0, kPathBf16 = 1, kPathBf16DqV = 2 };
+
 // One sequence class of a launch: sequences whose Lq lies in [lq_min, lq_max]
 // are cut into row tiles of `rows` (query token, head-in-group) rows.
 struct ClassInfo {

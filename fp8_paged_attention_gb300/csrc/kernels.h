@@ -37,13 +37,14 @@ cudaError_t launch_quantize_q(const void* q_bf16, void* q_e4m3, const float* q_d
 // Attention kernel launchers, one per (head dim, Q type, rows per tile, CTAs per SM);
 // every CTA is persistent over the class's work list.
 // `ctas` CTAs per SM, `sms` SMs: grid = sms * ctas persistent CTAs.
-cudaError_t launch_attn(int head_dim, bool fp8_q, int rows, int ctas, const AttnParams& p, const CUtensorMap& tm_q,
+// path: kPathE4M3, kPathBf16 or kPathBf16DqV (common.cuh).
+cudaError_t launch_attn(int head_dim, int path, int rows, int ctas, const AttnParams& p, const CUtensorMap& tm_q,
                         const CUtensorMap& tm_k, const CUtensorMap& tm_v, int sms, cudaStream_t stream);
 
 // Records a message for fp8pa_last_error() on this thread; returns `code`.
 int set_last_error(int code, const char* msg);
 
 // Shared-memory bytes of a kernel variant (0 if the variant does not exist).
-int attn_smem_bytes(int head_dim, bool fp8_q, int rows, int ctas);
+int attn_smem_bytes(int head_dim, int path, int rows, int ctas);
 
 }  // namespace fp8pa

@@ -198,6 +198,15 @@ void fp8pa_set_timing_events(void* start_event, void* stop_event);
 void fp8pa_set_ctas_per_sm(int ctas);
 
 /*
+ * fp8pa_set_bf16_dequant_v — selects how the BF16-Q path treats V (K is always
+ * dequantized to BF16 in-kernel and multiplied with BF16 Q on BF16 tensor
+ * cores).  0 (default): V stays E4M3, exact, in an E4M3 PV MMA with P carried
+ * as an E4M3 hi/lo pair (about BF16's 8 significant bits).  1: V is also
+ * dequantized to BF16 in shared memory and PV is a BF16 MMA with BF16 P.
+ */
+void fp8pa_set_bf16_dequant_v(int on);
+
+/*
  * fp8pa_get_device_status — enqueue on `stream` a copy of the current device's
  * status word (FP8PA_DEV_* bits accumulated by earlier launches) into
  * *host_status, which must be pinned host memory; the value is valid once the
