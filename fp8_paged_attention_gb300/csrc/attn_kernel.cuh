@@ -76,8 +76,18 @@ struct AttnCfg {
   static constexpr int kFixed = kQBufs * kQBytes + 2 * kPBytes + kBfSlots * kBfSlotBytes + kCtrlBytes + 1024;
   static constexpr int kStages = (kSmemLimit - kFixed) / kStageBytes > 16 ? 16 : (kSmemLimit - kFixed) / kStageBytes;
   static_assert(kStages >= 2, "smem");
+  // Stage ring(s).  Every ring needs one in-order consumer that waits on all of
+  // its fills: an mbarrier phase wait only tells parities apart, so a consumer
+  // that skipped the slot's previous fill could take that pending fill's phase
+  // for its own.  When K and V have different consumers (dequant warps and MMA
+  // thread on the BF16-Q path with E4M3 V) they get a ring each: K stages in
+  // slots [0, kKStages), V stages in [kKStages, kStages).
+  static constexpr bool kSplitRing = kPath == kPathBf16;
+  static constexpr int kVStages = kSplitRing ? ((kStages + 1) / 2 > kDC ? (kStages + 1) / 2 : kDC) : kStages;
+  static constexpr int kKStages = kSplitRing ? kStages - kVStages : kStages;
+  static_assert(kKStages >= 1, "no room for a K ring");
   // E4M3 V: the tail tile's V chunks must fit in the ring together (the softmax zeroes them in place)
-  static_assert(!kP8 || kStages >= kDC, "ring shorter than one tile's V");
+  static_assert(!kP8 || kVStages >= kDC, "ring shorter than one tile's V");
   static constexpr int kSmemBytes = kFixed + kStages * kStageBytes;
   // TMEM columns: S (2 buffers of N), O (kDC chunks of N), BF16 K (2 slots of 64 columns = 128 dims)
   static constexpr int kKCol = 2 * N + kDC * N;
@@ -193,6 +203,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
   using namespace ptx;
   using namespace detail;
   constexpr int S = C::kStages;
+  constexpr bool kSplit = C::kSplitRing;
+  constexpr int SK = C::kKStages, SV = C::kVStages;
   constexpr int SB = C::kBfSlots;
   constexpr int SBm = SB > 0 ? SB : 1;  // modulus for the BF16 V ring (literal path only)
   constexpr int QB = C::kQBufs;
@@ -284,7 +296,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t idx = 0, qit = 0;
+      // idx: stage stream position (one ring); kq / vq: K and V ring positions (split rings)
+      uint32_t idx = 0, kq = 0, vq = 0, qit = 0;
       bool ok = true;
       for (uint32_t ik = 0; ok; ++ik) {
         const int w = atomicAdd(p.work_next, 1);
@@ -306,30 +319,41 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
                       it.hk * p.group, it.q0 + it.row0 / p.group);
         ++qit;
         const int n = it.t1 - it.t0;
-        auto load_tile = [&](int u, const CUtensorMap* tm) -> bool {
+        auto load_tile = [&](int u, bool is_v) -> bool {
+          const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
           const int pg = it.pg_lo + 2 * (it.t0 + u);
           const int pa = page_id(p, it, pg), pb = page_id(p, it, pg + 1);
           for (int c = 0; c < DC; ++c) {
-            const uint32_t slot = idx % S;
-            if (!pwait(&ring_empty[slot], ((idx / S) & 1) ^ 1, lim, abort_flag)) return false;
+            uint32_t& pos = !kSplit ? idx : is_v ? vq : kq;
+            const uint32_t len = !kSplit ? S : is_v ? SV : SK;
+            const uint32_t slot = (kSplit && is_v ? SK : 0) + pos % len;
+            if (!pwait(&ring_empty[slot], ((pos / len) & 1) ^ 1, lim, abort_flag)) return false;
             mbar_arrive_expect_tx(&ring_full[slot], kStageBytes);
             uint8_t* dst = ring + slot * kStageBytes;
             tma_load_4d(dst, tm, &ring_full[slot], c * 128, it.hk, 0, pa);
             tma_load_4d(dst + kStageBytes / 2, tm, &ring_full[slot], c * 128, it.hk, 0, pb);
-            ++idx;
+            ++pos;
           }
           return true;
         };
-        ok = load_tile(0, &tm_k);
+        ok = load_tile(0, false);
         for (int u = 1; u <= n && ok; ++u) {
-          if (u < n) ok = load_tile(u, &tm_k);
-          if (ok) ok = load_tile(u - 1, &tm_v);
+          if (u < n) ok = load_tile(u, false);
+          if (ok) ok = load_tile(u - 1, true);
         }
       }
       if (!ok) flag_timeout(p, abort_flag);
       // drain: every issued copy must land before the CTA may exit
-      for (uint32_t j = idx > (uint32_t)S ? idx - S : 0; j < idx; ++j)
-        mbar_wait(&ring_full[j % S], (j / S) & 1, kDrainWaitLimit);
+      auto drain_ring = [&](uint32_t pos, uint32_t len, uint32_t first) {
+        for (uint32_t j = pos > len ? pos - len : 0; j < pos; ++j)
+          mbar_wait(&ring_full[first + j % len], (j / len) & 1, kDrainWaitLimit);
+      };
+      if (kSplit) {
+        drain_ring(kq, SK, 0);
+        drain_ring(vq, SV, SK);
+      } else {
+        drain_ring(idx, S, 0);
+      }
       for (uint32_t j = qit > (uint32_t)QB ? qit - QB : 0; j < qit; ++j)
         mbar_wait(&q_full[j % QB], (j / QB) & 1, kDrainWaitLimit);
     }
@@ -338,9 +362,13 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc(kQ8 ? kFmtE4M3 : kFmtBF16, kKMajor, kKMajor, 128, N);
       constexpr uint32_t idesc_pv = make_idesc(kP8 ? kFmtE4M3 : kFmtBF16, kMNMajor, kMNMajor, 128, N);
-      // idx: position in the K/V stage stream (the ring); kidx: BF16 K chunks in TMEM;
-      // bidx: BF16 V tiles in shared memory
+      // idx: position in the K/V stage stream (one ring) or in the V ring (split rings);
+      // kidx: BF16 K chunks in TMEM; bidx: BF16 V tiles in shared memory
       uint32_t idx = 0, kidx = 0, bidx = 0, g = 0, qit = 0;
+      // ring slot and phase parity of E4M3 stage position `pos`; the MMA thread
+      // reads K stages only on the E4M3 path and V stages only from the V ring
+      auto vslot = [&](uint32_t pos) { return kSplit ? SK + pos % SV : pos % S; };
+      auto vpar = [&](uint32_t pos) { return kSplit ? (pos / SV) & 1 : (pos / S) & 1; };
       bool ok = true;
       for (uint32_t ik = 0; ok; ++ik) {
         const uint32_t is = ik % kItemSlots;
@@ -386,7 +414,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
               mma_commit(&kt_empty[ks]);
               ++kidx;
             }
-            ++idx;
+            if (!kSplit) ++idx;
           }
           mma_commit(&s_full[sb]);
           return true;
@@ -398,7 +426,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           const uint32_t pb = gg & 1;
           if (kP8 && tail) {
             for (int c = 0; c < DC; ++c)
-              if (!pwait(&ring_full[(idx + c) % S], ((idx + c) / S) & 1, lim, abort_flag)) return false;
+              if (!pwait(&ring_full[vslot(idx + c)], vpar(idx + c), lim, abort_flag)) return false;
             mbar_arrive(v_ready);
           }
           if (!pwait(&p_full[pb], (gg >> 1) & 1, lim, abort_flag)) return false;
@@ -408,8 +436,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           for (int c = 0; c < DC; ++c) {
             const uint32_t d_tmem = tmem + 2 * N + c * N;
             if (kP8) {
-              const uint32_t slot = idx % S;
-              if (!pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag)) return false;
+              const uint32_t slot = vslot(idx);
+              if (!pwait(&ring_full[slot], vpar(idx), lim, abort_flag)) return false;
               tc_fence_after();
               const uint32_t a0 = smem_u32(ring + slot * kStageBytes);
 #pragma unroll
@@ -460,7 +488,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
     const int kl = quarter * 32 + lane;     // key (S) or head-dim (O) lane within the tile
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float NEG_INF = __int_as_float(0xFF800000);
-    uint32_t g = 0, sbase = 0, tails = 0;
+    uint32_t g = 0, sbase = 0, tails = 0;  // sbase: first stage of the item (stream, or V ring)
     bool aborted = false;
     for (uint32_t ik = 0; !aborted; ++ik) {
       const uint32_t is = ik % kItemSlots;
@@ -671,8 +699,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
             ++tails;
 #pragma unroll 1
             for (int c = 0; c < DC && ok; ++c) {
-              const uint32_t vi = sbase + v_stage_offset(u, n_t, DC) + c;
-              uint8_t* st = ring + (vi % S) * kStageBytes;
+              const uint32_t vi = kSplit ? sbase + u * DC + c : sbase + v_stage_offset(u, n_t, DC) + c;
+              uint8_t* st = ring + (kSplit ? SK + vi % SV : vi % S) * kStageBytes;
               for (int x16 = zr * 8 + wt; x16 < kTileKeys * 8; x16 += 128)
                 *reinterpret_cast<uint4*>(st + x16 * 16) = make_uint4(0, 0, 0, 0);
             }
@@ -710,7 +738,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         if (lane == 0) mbar_arrive(&p_full[pb]);
       }
       if (aborted) break;
-      sbase += 2 * n_t * DC;
+      sbase += (kSplit ? 1 : 2) * n_t * DC;
       // ---------------- epilogue: O / l, lse
       bool ok = pwait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, lim, abort_flag);
       ok = __all_sync(0xFFFFFFFFu, ok);
@@ -774,7 +802,9 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       const int quarter = warp & 3;
       const int row = quarter * 32 + lane;  // this thread's key row = its TMEM lane
       const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+      // idx: stage stream position (literal path, one ring) or K ring position (split rings)
       uint32_t idx = 0, kidx = 0, bidx = 0;
+      constexpr uint32_t KR = kSplit ? SK : S;
       bool ok = true;
       // the four dequant warps hand a stage back with a single arrive
       auto release = [&](uint64_t* a, uint64_t* b) {
@@ -799,8 +829,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         // K tile u: each chunk (128 dims) -> BF16 in TMEM slot kidx & 1, one key row per thread
         auto convert_k = [&](int u) -> bool {
           for (int c = 0; c < DC; ++c) {
-            const uint32_t slot = idx % S, ks = kidx & 1;
-            const bool w_ok = pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag) &&
+            const uint32_t slot = idx % KR, ks = kidx & 1;
+            const bool w_ok = pwait(&ring_full[slot], (idx / KR) & 1, lim, abort_flag) &&
                               pwait(&kt_empty[ks], ((kidx >> 1) & 1) ^ 1, lim, abort_flag);
             if (bar_red_or(3, 128, !w_ok)) return false;
             tc_fence_after();
@@ -833,10 +863,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         };
         // V tile u, literal path: -> BF16 in shared memory; rows past Lk become zeros
         auto convert_v = [&](int u) -> bool {
-          if (!kDqV) {
-            idx += DC;  // the PV MMA reads these stages as E4M3
-            return true;
-          }
+          if (!kDqV) return true;  // the PV MMA reads these stages as E4M3, from the V ring
           const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
           const int zero_from = (kb + kTileKeys > it.Lk) ? max(0, it.Lk - kb) : kTileKeys;
           for (int c = 0; c < DC; ++c) {
