@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "build", "load_library", "library_path", "quantize_q_fp8", "fp8_paged_attn_fwd", "workspace_size",
     "num_splits", "kernel_launches", "set_timing_events", "set_ctas_per_sm", "set_bf16_dequant_v", "get_device_status", "reset_device_status",
-    "set_wait_limit", "FP8PA_BF16", "FP8PA_E4M3",
+    "set_wait_limit", "set_stall_injection", "FP8PA_BF16", "FP8PA_E4M3",
     "DEV_BAD_PAGE", "DEV_TIMEOUT", "DEV_BAD_LENGTH", "PAGE_SIZE", "Fp8paError",
 ]
 
@@ -86,6 +86,8 @@ def load_library():
         lib.fp8pa_last_error.argtypes = []
         lib.fp8pa_set_wait_limit.restype = None
         lib.fp8pa_set_wait_limit.argtypes = [c.c_uint]
+        lib.fp8pa_set_stall_injection.restype = None
+        lib.fp8pa_set_stall_injection.argtypes = [c.c_int]
         lib.fp8pa_kernel_launches.restype = c.c_int
         lib.fp8pa_kernel_launches.argtypes = [c.c_int] * 10
         lib.fp8pa_set_bf16_dequant_v.restype = None
@@ -227,3 +229,9 @@ def reset_device_status(stream=None):
 def set_wait_limit(max_iterations: int):
     """Test hook: cap every bounded pipeline wait (0 restores the default)."""
     load_library().fp8pa_set_wait_limit(int(max_iterations))
+
+
+def set_stall_injection(on: bool):
+    """Test hook: make every attention CTA's MMA thread wait on a barrier that
+    nothing arrives on, so that the launch takes its bounded-wait timeout path."""
+    load_library().fp8pa_set_stall_injection(int(bool(on)))

@@ -69,6 +69,7 @@ int ctas_per_sm(int head_dim, int path, int rows) {
   return 1;
 }
 std::atomic<unsigned> g_wait_limit{0};
+std::atomic<int> g_inject_stall{0};
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -269,6 +270,8 @@ const char* fp8pa_last_error(void) { return g_err; }
 
 void fp8pa_set_wait_limit(unsigned int max_iterations) { g_wait_limit.store(max_iterations); }
 
+void fp8pa_set_stall_injection(int on) { g_inject_stall.store(on ? 1 : 0); }
+
 void fp8pa_set_ctas_per_sm(int ctas) { g_ctas_override.store(ctas); }
 
 void fp8pa_set_bf16_dequant_v(int on) { g_dequant_v.store(on ? 1 : 0); }
@@ -422,6 +425,7 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
   p.status = status;
   const unsigned wl = g_wait_limit.load();
   p.wait_limit = wl ? wl : kDefaultWaitLimit;
+  p.inject_stall = g_inject_stall.load();
   const bool timed = g_ev_start && g_ev_stop;
   if (timed && (e = cudaEventRecord(g_ev_start, st)) != cudaSuccess) return cuda_fail(e, "timing event");
   for (int k = 0; k < pl.num_classes; ++k) {

@@ -230,7 +230,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
   uint64_t* o_empty = pv_done + 2;
   uint64_t* v_ready = o_empty + 1;  // tail tile: its V stages have landed (MMA thread -> softmax)
   uint64_t* drain = v_ready + 1;
-  uint64_t* item_full = drain + 1;
+  uint64_t* never = drain + 1;  // nothing arrives on it: the stall-injection test hook waits here
+  uint64_t* item_full = never + 1;
   uint64_t* item_empty = item_full + kItemSlots;
   uint64_t* kt_full = item_empty + kItemSlots;  // BF16 K slot in TMEM written (dequant -> MMA)
   uint64_t* kt_empty = kt_full + 2;             // BF16 K slot consumed (MMA commit -> dequant)
@@ -272,6 +273,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
     mbar_init(o_empty, 4);
     mbar_init(v_ready, 1);
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     for (int i = 0; i < kItemSlots; ++i) {
       mbar_init(&item_full[i], 1);
       mbar_init(&item_empty[i], kDq ? 9 : 5);  // MMA thread + 4 softmax warps (+ 4 dequant warps)
@@ -377,6 +379,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         const bool valid = islot[is].valid != 0;
         mbar_arrive(&item_empty[is]);
         if (!valid) break;
+        if (p.inject_stall && !(ok = pwait(never, 0, lim, abort_flag))) break;
         if (it.t1 <= it.t0) continue;
         const int qb = qit % QB;
         if (!(ok = pwait(&q_full[qb], (qit / QB) & 1, lim, abort_flag))) break;

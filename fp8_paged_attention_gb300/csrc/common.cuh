@@ -51,6 +51,7 @@ struct AttnParams {
   int* work_next;          // dynamic item counter (zeroed by the plan kernel)
   unsigned* status;
   uint32_t wait_limit;
+  int inject_stall;  // test hook: the MMA issuer first waits on a barrier that nothing arrives on
 };
 
 // Visible key range of query i of a sequence (Lq queries, Lk keys); hi < lo when empty.

@@ -229,6 +229,17 @@ const char* fp8pa_last_error(void);
  */
 void fp8pa_set_wait_limit(unsigned int max_iterations);
 
+/*
+ * fp8pa_set_stall_injection — test hook (0 = off, the default).  While on, the
+ * MMA-issuing thread of every attention CTA of later launches first waits on a
+ * barrier that nothing ever arrives on, so that wait always runs out (after the
+ * wait limit above or about two seconds, whichever comes first).  The launch then
+ * takes the timeout path described above: FP8PA_DEV_TIMEOUT is set, the call
+ * itself returns OK, results of that launch are undefined, and the CUDA
+ * context stays usable.
+ */
+void fp8pa_set_stall_injection(int on);
+
 #ifdef __cplusplus
 }
 #endif

@@ -159,6 +159,29 @@ def test_per_batch_head_descales():
     assert lse_error(lse.cpu().numpy(), rl) <= LSE_GATE
 
 
+@pytest.mark.parametrize("fp8,limit", [(True, 0), (True, 64), (False, 0)], ids=["e4m3_default_limit",
+                                                                                "e4m3_limit64", "bf16_default_limit"])
+def test_wait_that_runs_out_sets_timeout_and_context_survives(fp8, limit):
+    """A pipeline wait that can never complete (the stall-injection hook) ends on
+    its bound: the launch reports DEV_TIMEOUT and the next launch is correct."""
+    import fp8_paged_attention_gb300 as fp8pa
+    d, hkv = (256, 16) if fp8 else (512, 4)
+    w = make("stall", [1] * 5 + [70], [300, 900, 1500, 2000, 64, 200], 32, hkv, d, -1, True, fp8, seed=17)
+    fp8pa.reset_device_status()
+    fp8pa.set_wait_limit(limit)
+    fp8pa.set_stall_injection(True)
+    try:
+        run_gpu(w)  # synchronizes: the launch ends, without a CUDA error
+    finally:
+        fp8pa.set_stall_injection(False)
+        fp8pa.set_wait_limit(0)
+    assert fp8pa.get_device_status() & fp8pa.DEV_TIMEOUT
+    fp8pa.reset_device_status()
+    out, lse = run_gpu(w)
+    check(w, out, lse)
+    assert fp8pa.get_device_status() == 0
+
+
 def test_bad_page_id_sets_status_and_reads_zeros():
     import fp8_paged_attention_gb300 as fp8pa
     w = make("badpage", [1, 1], [200, 300], 8, 4, 256, -1, True, True, seed=4)
