@@ -17,11 +17,18 @@
 // decoded item to the other roles through a small ring in shared memory, and
 // issues the TMA loads (Q tile, then K/V page tiles in the order the MMAs
 // consume them); warp 1 allocates tensor memory and issues the MMAs from one
-// thread; warps 2-5 run the softmax, the O rescale and the epilogue.  On the
-// BF16-Q paths warps 6-9 dequantize each E4M3 K stage into BF16 straight into
+// thread; the next one or two warpgroups run the softmax, the O rescale and the
+// epilogue (with two, each owns half the rows of every tile).  On the BF16-Q
+// paths the last four warps dequantize each E4M3 K stage into BF16 straight into
 // tensor memory, where it is the A operand of the QK^T MMA (exact: every E4M3
 // value is a BF16 value); on the literal path they also dequantize V into BF16
 // shared-memory tiles.
+//
+// Softmax per tile: with the running offsets of the previous tiles, P' is
+// computed directly; only when some P' exceeds the lazy bound (a row maximum
+// grew by more than tau), and on the first tile of an item, are the exact
+// per-row tile maxima formed (one warp reduction per row, then across the
+// four warps) and P' recomputed.  Row sums accumulate P' in f32.
 //
 // Paths (template parameter kPath):
 //  kPathE4M3    E4M3 Q: QK^T and PV are kind::f8f6f4 MMAs.
@@ -33,8 +40,8 @@
 // weights out of E4M3's subnormal range) as a pair on one scale:
 // hi = e4m3(P'), lo = e4m3(P' - hi); both PV MMAs accumulate into the same
 // TMEM O, so P carries about 8 significant bits (BF16 carries 8) instead of
-// E4M3's 4.  The row sum accumulates the values the MMAs saw, so O / l is an
-// exact convex combination of V rows.
+// E4M3's 4.  The row sum accumulates the f32 P', which the pair matches to
+// within 2^-8 relative.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -66,7 +73,11 @@ struct AttnCfg {
   // P^T for 128 keys: E4M3 hi term then E4M3 lo term (N x 128 bytes each), or BF16
   static constexpr int kPBytes = kP8 ? 2 * N * 128 : N * 256;
   static constexpr int kBfSlotBytes = 32768;             // BF16 tile of 128 keys x 128 dims
-  static constexpr int kThreads = kDq ? 320 : 192;
+  // softmax warpgroups: each owns N / kNW rows of every tile (two for 64-row tiles)
+  static constexpr int kNW = N == 64 ? 2 : 1;
+  static constexpr int kNR = N / kNW;
+  static constexpr int kDqWarp0 = 2 + 4 * kNW;  // first dequant warp (BF16-Q paths)
+  static constexpr int kThreads = 32 * kDqWarp0 + (kDq ? 128 : 0);
   // opt-in maximum per block; two blocks share the SM's 228 KB minus 1 KB reserved each
   static constexpr int kSmemLimit = kCtas == 1 ? 232448 : 115712;
   // barriers (< 1 KB) + per-row softmax state: red[2][4][N], lred[4][N], 4 x [N] floats
@@ -111,12 +122,32 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Max over the warp; floats ordered through their sign-magnitude integer image.
-__device__ __forceinline__ float warp_max(float v) {
-  int i = __float_as_int(v);
-  int key = i >= 0 ? i : (i ^ 0x7FFFFFFF);
-  int r = __reduce_max_sync(0xFFFFFFFFu, key);
-  return __int_as_float(r >= 0 ? r : (r ^ 0x7FFFFFFF));
+// Max over the warp.
+__device__ __forceinline__ float redux_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// P' pair -> E4M3 pair hi = e4m3(P'), lo = e4m3(P' - hi), each as 16 bits with
+// p0 in the low byte.  P' is rounded to f16 first (11 significant bits); the
+// residual of an f16 and its 4-bit rounding is exact in f16.
+__device__ __forceinline__ void e4m3_hilo(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  uint32_t h, hh, l;
+  uint16_t h8, l8;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(p1), "f"(p0));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h8) : "r"(h));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(h8));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(l) : "r"(h), "r"(hh));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l8) : "r"(l));
+  hi = h8;
+  lo = l8;
 }
 
 __device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t nthreads, bool pred) {
@@ -240,8 +271,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
   float* lred = red + 2 * 4 * N;                      // [4][N] per-warp row sums
   float* m_s = lred + 4 * N;                          // [N] running max (log2 units)
   float* a_s = m_s + N;                               // [N] rescale factor of this tile
-  float* msub_s = a_s + N;                            // [N] exponent offset of this tile
-  float* l_s = msub_s + N;                            // [N] final row sums
+  float* nmsub_s = a_s + N;                           // [N] exponent offset: P' = 2^(x + nmsub)
+  float* l_s = nmsub_s + N;                           // [N] final row sums
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(l_s + N);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -266,17 +297,17 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&s_empty[i], 4 * C::kNW);
+      mbar_init(&p_full[i], 4 * C::kNW);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(o_empty, 4);
+    mbar_init(o_empty, 4 * C::kNW);
     mbar_init(v_ready, 1);
     mbar_init(drain, 1);
     mbar_init(never, 1);
     for (int i = 0; i < kItemSlots; ++i) {
       mbar_init(&item_full[i], 1);
-      mbar_init(&item_empty[i], kDq ? 9 : 5);  // MMA thread + 4 softmax warps (+ 4 dequant warps)
+      mbar_init(&item_empty[i], 1 + 4 * C::kNW + (kDq ? 4 : 0));  // MMA thread, softmax and dequant warps
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -484,13 +515,25 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       mma_commit(drain);
       mbar_wait(drain, 0, kDrainWaitLimit);
     }
-  } else if (warp < 6) {
+  } else if (warp < C::kDqWarp0) {
     // ------------------------------------------------------------------ softmax / correction / epilogue
-    const int wt = threadIdx.x - 64;        // 0..127
-    const int quarter = warp & 3;           // TMEM lane quarter this warp may access
-    const int kl = quarter * 32 + lane;     // key (S) or head-dim (O) lane within the tile
+    // kNW warpgroups; warpgroup wg owns rows [r0, r0 + NR) of every tile and
+    // synchronizes on its own two named barriers.
+    constexpr int NR = C::kNR;
+    const int wg = C::kNW == 1 ? 0 : (warp - 2) >> 2;
+    const int r0 = wg * NR;
+    const uint32_t bar_a = 1 + 2 * wg, bar_b = 2 + 2 * wg;
+    const int wt = threadIdx.x - 64 - 128 * wg;  // 0..127 within the warpgroup
+    const int quarter = warp & 3;                // TMEM lane quarter this warp may access
+    const int kl = quarter * 32 + lane;          // key (S) or head-dim (O) lane within the tile
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float NEG_INF = __int_as_float(0xFF800000);
+    // Largest P' the lazy offsets allow: 2^(kTau + kPShift).
+    constexpr float kPMax = 256.0f;
+    static_assert(C::kTau + C::kPShift == 8.0f, "kPMax");
+    // Offset of a row that has seen no key yet: any unmasked key overflows P' and
+    // sends the tile down the exact-maximum path.
+    constexpr float kNoKeyOffset = 1e30f;
     uint32_t g = 0, sbase = 0, tails = 0;  // sbase: first stage of the item (stream, or V ring)
     bool aborted = false;
     for (uint32_t ik = 0; !aborted; ++ik) {
@@ -507,19 +550,20 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       } else {
         flag_timeout(p, abort_flag);
       }
-      if (bar_red_or(1, 128, !iok)) {  // all four warps leave together
+      if (bar_red_or(bar_a, 128, !iok)) {  // the warpgroup leaves together
         aborted = true;
         break;
       }
       if (!valid) break;
       const int G = p.group;
       const bool split_out = it.nsplit > 1;
+      const int nr = min(NR, it.nrows - r0);  // live rows of this warpgroup (may be <= 0)
       auto row_tok = [&](int n) { return it.q0 + (it.row0 + n) / G; };
       auto row_head = [&](int n) { return it.hk * G + (it.row0 + n) % G; };
       if (it.t1 <= it.t0) {
         // nothing visible: out = 0, lse = -inf
 #pragma unroll 1
-        for (int n = 0; n < it.nrows; ++n) {
+        for (int n = r0; n < r0 + nr; ++n) {
           const size_t r = (size_t)row_tok(n) * p.hq + row_head(n);
           for (int d = wt; d < D; d += 128) {
             if (split_out)
@@ -528,8 +572,9 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
               reinterpret_cast<__nv_bfloat16*>(p.out)[r * D + d] = __float2bfloat16_rn(0.f);
           }
         }
-        if (wt < it.nrows) {
-          const size_t li = (size_t)row_head(wt) * p.total_q + row_tok(wt);
+        if (wt < nr) {
+          const int n = r0 + wt;
+          const size_t li = (size_t)row_head(n) * p.total_q + row_tok(n);
           if (split_out)
             p.lse_part[(size_t)it.split * p.hq * p.total_q + li] = NEG_INF;
           else if (p.lse)
@@ -541,47 +586,46 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       const float kd = load_descale(p.k_descale, p, it);
       const float vd = load_descale(p.v_descale, p, it);
       const float scale = p.softmax_scale_log2 * kd * (kQ8 ? *p.q_descale : 1.0f);
-      if (wt < N) {
-        m_s[wt] = NEG_INF;
-        a_s[wt] = 1.0f;
-        msub_s[wt] = -C::kPShift;
+      if (wt < NR) {
+        m_s[r0 + wt] = NEG_INF;
+        a_s[r0 + wt] = 1.0f;
+        nmsub_s[r0 + wt] = kNoKeyOffset;
       }
-      float lt[N];
+      float lt[NR];  // this thread's partial row sums (its keys only)
 #pragma unroll
-      for (int n = 0; n < N; ++n) lt[n] = 0.f;
+      for (int n = 0; n < NR; ++n) lt[n] = 0.f;
 
       for (int u = 0; u < n_t; ++u, ++g) {
         const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
         const int j = kb + kl;
-        const uint32_t sb = g & 1;
+        const uint32_t sb = g & 1, pb = g & 1;
+        const bool interior = kb >= it.lo_max && kb + kTileKeys - 1 <= it.hi_min;
+        const bool tail = kP8 && kb + kTileKeys > it.Lk;
         bool ok = pwait(&s_full[sb], (g >> 1) & 1, lim, abort_flag);
+        if (ok && g >= 2) ok = pwait(&pv_done[pb], ((g >> 1) - 1) & 1, lim, abort_flag);  // P buffer free
         ok = __all_sync(0xFFFFFFFFu, ok);
-        float x[N];
-        if (ok) {
+        float x[NR];
+        // raw scores of this warpgroup's rows for this thread's key; masked keys at -inf
+        auto load_scores = [&]() {
           tc_fence_after();
-          // rows past nrows are padding (decode tiles hold G * Lq real rows): skip their work
 #pragma unroll
-          for (int c = 0; c < N; c += 16) {
-            if (c < it.nrows) {
+          for (int c = 0; c < NR; c += 16) {
+            if (c < nr) {
               uint32_t r[16];
-              tmem_load16(tmem + lane_base + sb * N + c, r);
+              tmem_load16(tmem + lane_base + sb * N + r0 + c, r);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(r[i]) * scale;
+              for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(r[i]);
             } else {
 #pragma unroll
               for (int i = 0; i < 16; ++i) x[c + i] = NEG_INF;
             }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_empty[sb]);
-          const bool interior = kb >= it.lo_max && kb + kTileKeys - 1 <= it.hi_min;
           if (!interior) {
             // query i sits at p = Lk - Lq + i; rows n and n' share a token when n / G == n' / G
             const int lg = __ffs(G) - 1;
-            const int p0 = it.Lk - it.Lq + (it.row0 >> lg);
+            const int p0 = it.Lk - it.Lq + ((it.row0 + r0) >> lg);
 #pragma unroll
-            for (int n = 0; n < N; ++n) {
+            for (int n = 0; n < NR; ++n) {
               const int pn = p0 + (n >> lg);
               const int lo = p.window_left >= 0 ? max(0, pn - p.window_left) : 0;
               const int hi = p.causal ? min(pn, it.Lk - 1) : it.Lk - 1;
@@ -589,156 +633,178 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
             }
           }
 #pragma unroll
-          for (int n = 0; n < N; ++n)
-            if (n >= it.nrows) x[n] = NEG_INF;
-          float* rb = red + (g & 1) * 4 * N + quarter * N;
+          for (int n = 0; n < NR; ++n)
+            if (n >= nr) x[n] = NEG_INF;
+        };
+        // Fast path: P' = 2^(S * scale - m_used + shift) with the running offsets,
+        // valid unless some P' exceeds 2^(tau + shift), i.e. a row maximum grew by
+        // more than tau; the first tile of an item always needs the exact maxima.
+        bool slow = u == 0;
+        if (ok) {
+          load_scores();
+          if (!slow) {
+            float pm = 0.f;
 #pragma unroll
-          for (int n = 0; n < N; ++n) {
-            if (n < it.nrows) {
-              const float mx = warp_max(x[n]);
-              if (lane == (n & 31)) rb[n] = mx;
+            for (int n = 0; n < NR; n += 2) {
+              const float2 t = __ffma2_rn(make_float2(x[n], x[n + 1]), make_float2(scale, scale),
+                                          make_float2(nmsub_s[r0 + n], nmsub_s[r0 + n + 1]));
+              x[n] = ex2(t.x);
+              x[n + 1] = ex2(t.y);
+              pm = fmax3(pm, x[n], x[n + 1]);
             }
+            slow = pm > kPMax;
           }
         } else {
           flag_timeout(p, abort_flag);
         }
-        if (bar_red_or(1, 128, !ok)) {
-          aborted = true;
-          break;
-        }
-        // row owners fold the four warp maxima into the running max
-        bool resc = false;
-        if (wt < it.nrows) {
-          const float* rr = red + (g & 1) * 4 * N;
-          const float tmax = fmaxf(fmaxf(rr[wt], rr[N + wt]), fmaxf(rr[2 * N + wt], rr[3 * N + wt]));
-          const float mo = m_s[wt];
-          float mn = mo, alpha = 1.0f;
-          if (tmax > mo + C::kTau) {
-            mn = tmax;
-            // a row that has seen no key yet has O = 0 and l = 0: nothing to rescale
-            if (mo != NEG_INF) alpha = ex2(mo - mn);
+        bool rescale = false;
+        if (bar_red_or(bar_a, 128, slow || !ok)) {
+          if (bar_red_or(bar_a, 128, !ok)) {
+            aborted = true;
+            break;
           }
-          m_s[wt] = mn;
-          a_s[wt] = alpha;
-          msub_s[wt] = (mn == NEG_INF ? 0.0f : mn) - C::kPShift;
-          resc = alpha != 1.0f;
-        }
-        const bool rescale = bar_red_or(2, 128, resc);
-        // P = 2^(x - m + shift), quantized; thread-partial row sums of the quantized values
-        const uint32_t pb = g & 1;
-        ok = true;
-        if (g >= 2) ok = pwait(&pv_done[pb], ((g >> 1) - 1) & 1, lim, abort_flag);
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (ok) {
-          uint8_t* pdst = pbuf + pb * C::kPBytes;
-          if (kP8) {
+          // exact tile maxima: the fast-path attempt (if any) overwrote x
+          if (u > 0) load_scores();
 #pragma unroll
-            for (int blk = 0; blk < N / 16; ++blk) {
-              if (blk * 16 >= it.nrows) break;
-              uint32_t hi_w[4], lo_w[4];
+          for (int n = 0; n < NR; n += 2) {
+            const float2 t = __fmul2_rn(make_float2(x[n], x[n + 1]), make_float2(scale, scale));
+            x[n] = t.x;
+            x[n + 1] = t.y;
+          }
+          float* rb = red + (g & 1) * 4 * N + quarter * N + r0;
+          float mine0 = NEG_INF, mine1 = NEG_INF;
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t hw = 0, lw = 0;
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                  const int n0 = blk * 16 + q4 * 4 + h2 * 2;
-                  const float p0 = ex2(x[n0] - msub_s[n0]);
-                  const float p1 = ex2(x[n0 + 1] - msub_s[n0 + 1]);
-                  const __nv_fp8x2_storage_t h8 =
-                      __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
-                  __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h8, __NV_E4M3);
-                  const float2 hv = __half22float2(*reinterpret_cast<__half2*>(&hr));
-                  // residuals are exact in f32 (p and hv agree in their leading bits)
-                  const __nv_fp8x2_storage_t l8 =
-                      __nv_cvt_float2_to_fp8x2(make_float2(p0 - hv.x, p1 - hv.y), __NV_SATFINITE, __NV_E4M3);
-                  __half2_raw lr = __nv_cvt_fp8x2_to_halfraw2(l8, __NV_E4M3);
-                  const float2 lv = __half22float2(*reinterpret_cast<__half2*>(&lr));
-                  if (rescale) {
-                    lt[n0] *= a_s[n0];
-                    lt[n0 + 1] *= a_s[n0 + 1];
-                  }
-                  lt[n0] += hv.x + lv.x;
-                  lt[n0 + 1] += hv.y + lv.y;
-                  hw |= (uint32_t)h8 << (16 * h2);
-                  lw |= (uint32_t)l8 << (16 * h2);
-                }
-                hi_w[q4] = hw;
-                lo_w[q4] = lw;
-              }
-              *reinterpret_cast<uint4*>(pdst + blk * 2048 + kl * 16) = make_uint4(hi_w[0], hi_w[1], hi_w[2], hi_w[3]);
-              *reinterpret_cast<uint4*>(pdst + N * 128 + blk * 2048 + kl * 16) =
-                  make_uint4(lo_w[0], lo_w[1], lo_w[2], lo_w[3]);
-            }
-          } else {
-#pragma unroll
-            for (int blk = 0; blk < N / 8; ++blk) {
-              if (blk * 8 >= it.nrows) break;
-              uint32_t packed[4];
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                const int n0 = blk * 8 + q4 * 2;
-                const float p0 = ex2(x[n0] - msub_s[n0]);
-                const float p1 = ex2(x[n0 + 1] - msub_s[n0 + 1]);
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-                const float2 back = __bfloat1622float2(b2);
-                if (rescale) {
-                  lt[n0] *= a_s[n0];
-                  lt[n0 + 1] *= a_s[n0 + 1];
-                }
-                lt[n0] += back.x;
-                lt[n0 + 1] += back.y;
-                packed[q4] = *reinterpret_cast<uint32_t*>(&b2);
-              }
-              *reinterpret_cast<uint4*>(pdst + blk * 2048 + kl * 16) =
-                  make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          for (int n = 0; n < NR; ++n) {
+            if (n < nr) {
+              const float mx = redux_max(x[n]);
+              if (n < 32) mine0 = lane == n ? mx : mine0;
+              else mine1 = lane == n - 32 ? mx : mine1;
             }
           }
-          // rows of the last page past the sequence end may hold anything (even NaN):
-          // zero those V rows so that 0 * V stays 0 in the PV MMA
-          if (kP8 && kb + kTileKeys > it.Lk) {
-            const int zr = max(0, it.Lk - kb);
-            ok = pwait(v_ready, tails & 1, lim, abort_flag);
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            ++tails;
+          if (lane < nr) rb[lane] = mine0;
+          if (NR > 32 && lane + 32 < nr) rb[lane + 32] = mine1;
+          named_bar_sync(bar_a, 128);
+          // row owners fold the four warp maxima into the running max
+          bool resc = false;
+          if (wt < nr) {
+            const int n = r0 + wt;
+            const float* rr = red + (g & 1) * 4 * N + n;
+            const float tmax = fmaxf(fmaxf(rr[0], rr[N]), fmaxf(rr[2 * N], rr[3 * N]));
+            const float mo = m_s[n];
+            float mn = mo, alpha = 1.0f;
+            if (tmax > mo + C::kTau) {
+              mn = tmax;
+              // a row that has seen no key yet has O = 0 and l = 0: nothing to rescale
+              if (mo != NEG_INF) alpha = ex2(mo - mn);
+            }
+            m_s[n] = mn;
+            a_s[n] = alpha;
+            nmsub_s[n] = mn == NEG_INF ? kNoKeyOffset : C::kPShift - mn;
+            resc = alpha != 1.0f;
+          }
+          rescale = bar_red_or(bar_b, 128, resc);
+#pragma unroll
+          for (int n = 0; n < NR; n += 2) {
+            const float2 t = __fadd2_rn(make_float2(x[n], x[n + 1]), make_float2(nmsub_s[r0 + n], nmsub_s[r0 + n + 1]));
+            x[n] = ex2(t.x);
+            x[n + 1] = ex2(t.y);
+          }
+          if (rescale) {
+#pragma unroll
+            for (int n = 0; n < NR; ++n) lt[n] *= a_s[r0 + n];
+          }
+        }
+        // P^T of this warpgroup's rows, and the row sums of P'
+        uint8_t* pdst = pbuf + pb * C::kPBytes;
+        if (kP8) {
+#pragma unroll
+          for (int blk = 0; blk < NR / 16; ++blk) {
+            if (blk * 16 >= nr) break;
+            uint32_t hi_w[4], lo_w[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int n0 = blk * 16 + q4 * 4;
+              uint32_t h01, l01, h23, l23;
+              e4m3_hilo(x[n0], x[n0 + 1], h01, l01);
+              e4m3_hilo(x[n0 + 2], x[n0 + 3], h23, l23);
+              hi_w[q4] = h01 | (h23 << 16);
+              lo_w[q4] = l01 | (l23 << 16);
+            }
+            const int o = (r0 / 16 + blk) * 2048 + kl * 16;
+            *reinterpret_cast<uint4*>(pdst + o) = make_uint4(hi_w[0], hi_w[1], hi_w[2], hi_w[3]);
+            *reinterpret_cast<uint4*>(pdst + N * 128 + o) = make_uint4(lo_w[0], lo_w[1], lo_w[2], lo_w[3]);
+          }
+        } else {
+#pragma unroll
+          for (int blk = 0; blk < NR / 8; ++blk) {
+            if (blk * 8 >= nr) break;
+            uint32_t packed[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int n0 = blk * 8 + q4 * 2;
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(x[n0], x[n0 + 1]);
+              packed[q4] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(pdst + (r0 / 8 + blk) * 2048 + kl * 16) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          }
+        }
+#pragma unroll
+        for (int n = 0; n < NR; n += 2) {
+          const float2 s = __fadd2_rn(make_float2(lt[n], lt[n + 1]), make_float2(x[n], x[n + 1]));
+          lt[n] = s.x;
+          lt[n + 1] = s.y;
+        }
+        // rows of the last page past the sequence end may hold anything (even NaN):
+        // zero those V rows so that 0 * V stays 0 in the PV MMA
+        if (tail) {
+          const int zr = max(0, it.Lk - kb);
+          ok = pwait(v_ready, tails & 1, lim, abort_flag);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          ++tails;
 #pragma unroll 1
-            for (int c = 0; c < DC && ok; ++c) {
-              const uint32_t vi = kSplit ? sbase + u * DC + c : sbase + v_stage_offset(u, n_t, DC) + c;
-              uint8_t* st = ring + (kSplit ? SK + vi % SV : vi % S) * kStageBytes;
-              for (int x16 = zr * 8 + wt; x16 < kTileKeys * 8; x16 += 128)
-                *reinterpret_cast<uint4*>(st + x16 * 16) = make_uint4(0, 0, 0, 0);
-            }
+          for (int c = 0; c < DC && ok; ++c) {
+            const uint32_t vi = kSplit ? sbase + u * DC + c : sbase + v_stage_offset(u, n_t, DC) + c;
+            uint8_t* st = ring + (kSplit ? SK + vi % SV : vi % S) * kStageBytes;
+            for (int x16 = zr * 8 + wt + 128 * wg; x16 < kTileKeys * 8; x16 += 128 * C::kNW)
+              *reinterpret_cast<uint4*>(st + x16 * 16) = make_uint4(0, 0, 0, 0);
           }
-          fence_proxy_async_smem();
-          // rescale the running O when a row max grew (not needed on an item's first tile)
-          if (ok && rescale && u > 0) {
-            ok = pwait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, lim, abort_flag);
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            if (ok) {
-              tc_fence_after();
+        }
+        fence_proxy_async_smem();
+        // rescale the running O when a row max grew (not needed on an item's first tile)
+        if (ok && rescale && u > 0) {
+          ok = pwait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, lim, abort_flag);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (ok) {
+            tc_fence_after();
 #pragma unroll 1
-              for (int c = 0; c < DC; ++c) {
+            for (int c = 0; c < DC; ++c) {
 #pragma unroll
-                for (int cc = 0; cc < N; cc += 16) {
-                  if (cc >= it.nrows) break;
-                  uint32_t r[16];
-                  const uint32_t ta = tmem + lane_base + 2 * N + c * N + cc;
-                  tmem_load16(ta, r);
+              for (int cc = 0; cc < NR; cc += 16) {
+                if (cc >= nr) break;
+                uint32_t r[16];
+                const uint32_t ta = tmem + lane_base + 2 * N + c * N + r0 + cc;
+                tmem_load16(ta, r);
 #pragma unroll
-                  for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a_s[cc + i]);
-                  tmem_store16(ta, r);
-                }
+                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a_s[r0 + cc + i]);
+                tmem_store16(ta, r);
               }
             }
           }
         }
-        if (!ok) flag_timeout(p, abort_flag);
-        if (bar_red_or(1, 128, !ok)) {
-          aborted = true;
-          break;
+        if (tail || rescale) {
+          if (!ok) flag_timeout(p, abort_flag);
+          if (bar_red_or(bar_a, 128, !ok)) {
+            aborted = true;
+            break;
+          }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[pb]);
+        if (lane == 0) {
+          mbar_arrive(&s_empty[sb]);
+          mbar_arrive(&p_full[pb]);
+        }
       }
       if (aborted) break;
       sbase += (kSplit ? 1 : 2) * n_t * DC;
@@ -746,34 +812,37 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       bool ok = pwait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, lim, abort_flag);
       ok = __all_sync(0xFFFFFFFFu, ok);
 #pragma unroll
-      for (int n = 0; n < N; ++n) {
-        if (n < it.nrows) {
+      for (int n = 0; n < NR; ++n) {
+        if (n < nr) {
           float v = lt[n];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-          if (lane == (n & 31)) lred[quarter * N + n] = v;
+          if (lane == (n & 31)) lred[quarter * N + r0 + n] = v;
         }
       }
       if (!ok) flag_timeout(p, abort_flag);
-      if (bar_red_or(1, 128, !ok)) {
+      if (bar_red_or(bar_a, 128, !ok)) {
         aborted = true;
         break;
       }
-      if (wt < it.nrows) l_s[wt] = (lred[wt] + lred[N + wt]) + (lred[2 * N + wt] + lred[3 * N + wt]);
-      named_bar_sync(2, 128);
+      if (wt < nr) {
+        const int n = r0 + wt;
+        l_s[n] = (lred[n] + lred[N + n]) + (lred[2 * N + n] + lred[3 * N + n]);
+      }
+      named_bar_sync(bar_b, 128);
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < DC; ++c) {
         const int d = c * 128 + kl;
 #pragma unroll
-        for (int cc = 0; cc < N; cc += 16) {
-          if (cc >= it.nrows) break;
+        for (int cc = 0; cc < NR; cc += 16) {
+          if (cc >= nr) break;
           uint32_t r[16];
-          tmem_load16(tmem + lane_base + 2 * N + c * N + cc, r);
+          tmem_load16(tmem + lane_base + 2 * N + c * N + r0 + cc, r);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int n = cc + i;
-            if (n < it.nrows) {
+            const int n = r0 + cc + i;
+            if (cc + i < nr) {
               const float l = l_s[n];
               const float o = l > 0.f ? __uint_as_float(r[i]) / l * vd : 0.f;
               const size_t row = (size_t)row_tok(n) * p.hq + row_head(n);
@@ -785,10 +854,11 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           }
         }
       }
-      if (wt < it.nrows) {
-        const float l = l_s[wt];
-        const float lse = l > 0.f ? (m_s[wt] - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
-        const size_t li = (size_t)row_head(wt) * p.total_q + row_tok(wt);
+      if (wt < nr) {
+        const int n = r0 + wt;
+        const float l = l_s[n];
+        const float lse = l > 0.f ? (m_s[n] - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+        const size_t li = (size_t)row_head(n) * p.total_q + row_tok(n);
         if (split_out)
           p.lse_part[(size_t)it.split * p.hq * p.total_q + li] = lse;
         else if (p.lse)
@@ -801,7 +871,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
   } else {
     // ------------------------------------------------------------------ E4M3 -> BF16 dequant (BF16-Q paths)
     if (kDq) {
-      const int dt = threadIdx.x - 192;  // 0..127
+      const int dt = threadIdx.x - 32 * C::kDqWarp0;  // 0..127
+      constexpr uint32_t kDqBar = 1 + 2 * C::kNW;       // named barrier of the four dequant warps
       const int quarter = warp & 3;
       const int row = quarter * 32 + lane;  // this thread's key row = its TMEM lane
       const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -811,7 +882,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       bool ok = true;
       // the four dequant warps hand a stage back with a single arrive
       auto release = [&](uint64_t* a, uint64_t* b) {
-        named_bar_sync(3, 128);
+        named_bar_sync(kDqBar, 128);
         if (dt == 0) {
           mbar_arrive(a);
           mbar_arrive(b);
@@ -819,8 +890,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       };
       for (uint32_t ik = 0; ok; ++ik) {
         const uint32_t is = ik % kItemSlots;
-        // every wait decision is a vote of all four dequant warps: they share named barrier 3
-        ok = !bar_red_or(3, 128, !pwait(&item_full[is], (ik / kItemSlots) & 1, lim, abort_flag));
+        // every wait decision is a vote of all four dequant warps: they share named barrier kDqBar
+        ok = !bar_red_or(kDqBar, 128, !pwait(&item_full[is], (ik / kItemSlots) & 1, lim, abort_flag));
         if (!ok) break;
         const Item it = islot[is].it;
         const bool valid = islot[is].valid != 0;
@@ -835,7 +906,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
             const uint32_t slot = idx % KR, ks = kidx & 1;
             const bool w_ok = pwait(&ring_full[slot], (idx / KR) & 1, lim, abort_flag) &&
                               pwait(&kt_empty[ks], ((kidx >> 1) & 1) ^ 1, lim, abort_flag);
-            if (bar_red_or(3, 128, !w_ok)) return false;
+            if (bar_red_or(kDqBar, 128, !w_ok)) return false;
             tc_fence_after();
             const uint8_t* src = ring + slot * kStageBytes + row * 128;
             uint4 vin[8];
@@ -873,7 +944,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
             const uint32_t slot = idx % S, bslot = bidx % SBm;
             const bool w_ok = pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag) &&
                               pwait(&bf_empty[bslot], ((bidx / SBm) & 1) ^ 1, lim, abort_flag);
-            if (bar_red_or(3, 128, !w_ok)) return false;
+            if (bar_red_or(kDqBar, 128, !w_ok)) return false;
             const uint8_t* src = ring + slot * kStageBytes;
             uint8_t* dst = bfbuf + bslot * C::kBfSlotBytes;
             uint4 vin[8];
