@@ -322,6 +322,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_wait();  // the work list, Q and the K/V cache are written by earlier kernels
   const uint32_t tmem = *tmem_slot;
   const int n_items = *p.work_count;
   const uint32_t lim = p.wait_limit;

@@ -14,8 +14,10 @@ cudaError_t launch_attn_variant(const AttnParams& p, const CUtensorMap& tm_q, co
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kPath, N, kCtas>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_fwd_kernel<D, kPath, N, kCtas><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p, tm_q, tm_k, tm_v);
-  return cudaGetLastError();
+  // programmatic launch: the prologue (barriers, tensor memory, tensor maps)
+  // overlaps the plan kernel; the kernel waits for it before reading the work list
+  return launch_pdl(attn_fwd_kernel<D, kPath, N, kCtas>, dim3(grid), dim3(C::kThreads), (size_t)C::kSmemBytes,
+                    stream, p, tm_q, tm_k, tm_v);
 }
 
 }  // namespace fp8pa

@@ -41,6 +41,25 @@ cudaError_t launch_quantize_q(const void* q_bf16, void* q_e4m3, const float* q_d
 cudaError_t launch_attn(int head_dim, int path, int rows, int ctas, const AttnParams& p, const CUtensorMap& tm_q,
                         const CUtensorMap& tm_k, const CUtensorMap& tm_v, int sms, cudaStream_t stream);
 
+// Launches `kernel` with programmatic stream serialization: it may start while
+// the previous kernel in the stream is still running, so it must call
+// griddep_wait() before it touches memory that kernel may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Records a message for fp8pa_last_error() on this thread; returns `code`.
 int set_last_error(int code, const char* msg);
 

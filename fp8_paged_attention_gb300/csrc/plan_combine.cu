@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace fp8pa {
 
@@ -41,8 +42,11 @@ __device__ __forceinline__ int seq_lq(const PlanParams& pp, int b) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
-  __shared__ int sums[2][kPlanThreads];
-  const int tid = threadIdx.x;
+  static_assert(kPlanThreads == 32 * 32, "two-level warp scan");
+  ptx::griddep_launch_dependents();  // the attention grid may start its prologue
+  ptx::griddep_wait();               // inputs and the workspace belong to earlier kernels until they finish
+  __shared__ int wsum[2][32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int per = (pp.batch + kPlanThreads - 1) / kPlanThreads;
   const int b0 = min(pp.batch, tid * per), b1 = min(pp.batch, b0 + per);
   int cnt[2] = {0, 0};
@@ -55,19 +59,40 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
         cnt[k] += seq_row_tiles(Lq, pp.group, c.rows) * seq_splits(Lq, Lk, pp.group, pp.window_left, pp.causal, c);
     }
   }
-  sums[0][tid] = cnt[0];
-  sums[1][tid] = cnt[1];
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    const int v0 = tid >= off ? sums[0][tid - off] : 0;
-    const int v1 = tid >= off ? sums[1][tid - off] : 0;
-    __syncthreads();
-    sums[0][tid] += v0;
-    sums[1][tid] += v1;
-    __syncthreads();
+  // exclusive prefix sums of the per-thread counts: within each warp, then over the warp totals
+  int inc[2] = {cnt[0], cnt[1]};
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, inc[k], off);
+      if (lane >= off) inc[k] += v;
+    }
   }
-  int excl[2] = {sums[0][tid] - cnt[0], sums[1][tid] - cnt[1]};
-  const int total[2] = {sums[0][kPlanThreads - 1], sums[1][kPlanThreads - 1]};
+  if (lane == 31) {
+    wsum[0][wid] = inc[0];
+    wsum[1][wid] = inc[1];
+  }
+  __syncthreads();
+  if (wid == 0) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      int v = wsum[k][lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xFFFFFFFFu, v, off);
+        if (lane >= off) v += t;
+      }
+      wsum[k][lane] = v;
+    }
+  }
+  __syncthreads();
+  int excl[2], total[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    excl[k] = inc[k] - cnt[k] + (wid > 0 ? wsum[k][wid - 1] : 0);
+    total[k] = wsum[k][31];
+  }
   if (tid == 0)
     for (int k = 0; k < 2; ++k) {
       pp.counts[k] = k < pp.num_classes ? total[k] * pp.hkv : 0;
@@ -162,8 +187,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(CombinePara
 }  // namespace
 
 cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(pp);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, pp);
 }
 
 cudaError_t launch_combine(const CombineParams& cp, cudaStream_t stream) {

@@ -50,6 +50,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Wait until the grids this one depends on (the previous kernel in the stream)
+// have completed and their memory is visible; a grid launched with programmatic
+// stream serialization must call this before it touches memory they may write.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next grid in the stream start launching (it still waits for this one
+// to complete before it touches memory).
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- fences / barriers
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -6,6 +6,7 @@
 #include <cuda_fp8.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace fp8pa {
 
@@ -23,6 +24,8 @@ __device__ __forceinline__ uint8_t quant_one(uint16_t bits, float d) {
 // 8 elements per thread when both pointers allow 16-byte / 8-byte accesses.
 __global__ void quantize_q_vec8(const uint4* __restrict__ q, uint2* __restrict__ out, const float* __restrict__ qd,
                                 long long n8) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const float d = *qd;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
     const uint4 v = q[i];
@@ -39,6 +42,8 @@ __global__ void quantize_q_vec8(const uint4* __restrict__ q, uint2* __restrict__
 
 __global__ void quantize_q_scalar(const uint16_t* __restrict__ q, uint8_t* __restrict__ out,
                                   const float* __restrict__ qd, long long begin, long long n) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const float d = *qd;
   for (long long i = begin + blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)
@@ -56,9 +61,9 @@ cudaError_t launch_quantize_q(const void* q_bf16, void* q_e4m3, const float* q_d
     const long long n8 = n / 8;
     if (n8 > 0) {
       const long long blocks = (n8 + 255) / 256;
-      quantize_q_vec8<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
-          reinterpret_cast<const uint4*>(q_bf16), reinterpret_cast<uint2*>(q_e4m3), q_descale, n8);
-      cudaError_t e = cudaGetLastError();
+      cudaError_t e = launch_pdl(quantize_q_vec8, dim3((unsigned)(blocks < 4096 ? blocks : 4096)), dim3(256), 0, stream,
+                                 reinterpret_cast<const uint4*>(q_bf16), reinterpret_cast<uint2*>(q_e4m3), q_descale,
+                                 n8);
       if (e != cudaSuccess) return e;
     }
     done = n8 * 8;
@@ -66,9 +71,9 @@ cudaError_t launch_quantize_q(const void* q_bf16, void* q_e4m3, const float* q_d
   if (done < n) {
     const long long rest = n - done;
     const long long blocks = (rest + 255) / 256;
-    quantize_q_scalar<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
-        reinterpret_cast<const uint16_t*>(q_bf16), reinterpret_cast<uint8_t*>(q_e4m3), q_descale, done, n);
-    return cudaGetLastError();
+    return launch_pdl(quantize_q_scalar, dim3((unsigned)(blocks < 4096 ? blocks : 4096)), dim3(256), 0, stream,
+                      reinterpret_cast<const uint16_t*>(q_bf16), reinterpret_cast<uint8_t*>(q_e4m3), q_descale, done,
+                      n);
   }
   return cudaSuccess;
 }
