@@ -73,15 +73,19 @@ struct AttnCfg {
   // P^T for 128 keys: E4M3 hi term then E4M3 lo term (N x 128 bytes each), or BF16
   static constexpr int kPBytes = kP8 ? 2 * N * 128 : N * 256;
   static constexpr int kBfSlotBytes = 32768;             // BF16 tile of 128 keys x 128 dims
+  // One CTA per SM: separate QK^T and PV issuing threads (warps 1 and 2).
+  static constexpr bool kTwoIssuers = kCtas == 1;
   // softmax warpgroups: each owns N / kNW rows of every tile (two for 64-row tiles)
   static constexpr int kNW = N == 64 ? 2 : 1;
   static constexpr int kNR = N / kNW;
-  static constexpr int kDqWarp0 = 2 + 4 * kNW;  // first dequant warp (BF16-Q paths)
+  static constexpr int kSmWarp0 = kTwoIssuers ? 3 : 2;  // first softmax warp
+  static constexpr int kDqWarp0 = kSmWarp0 + 4 * kNW;    // first dequant warp (BF16-Q paths)
   static constexpr int kThreads = 32 * kDqWarp0 + (kDq ? 128 : 0);
   // opt-in maximum per block; two blocks share the SM's 228 KB minus 1 KB reserved each
   static constexpr int kSmemLimit = kCtas == 1 ? 232448 : 115712;
-  // barriers (< 1 KB) + per-row softmax state: red[2][4][N], lred[4][N], 4 x [N] floats
-  static constexpr int kCtrlBytes = 1536 + 64 * N + 64;  // + the item ring
+  // barriers and the item ring (< 1 KB), then per-row state: ooff[N] (8 bytes),
+  // red[2][4][N], lred[4][N] and 4 x [N] floats
+  static constexpr int kCtrlBytes = 1536 + 72 * N + 80;
   static constexpr int kQBufs = kQ8 ? ((2 * kQBytes <= 65536) ? 2 : 1) : ((2 * kQBytes <= 32768) ? 2 : 1);
   static constexpr int kBfSlots = kDqV ? 2 : 0;
   static constexpr int kFixed = kQBufs * kQBytes + 2 * kPBytes + kBfSlots * kBfSlotBytes + kCtrlBytes + 1024;
@@ -93,7 +97,7 @@ struct AttnCfg {
   // for its own.  When K and V have different consumers (dequant warps and MMA
   // thread on the BF16-Q path with E4M3 V) they get a ring each: K stages in
   // slots [0, kKStages), V stages in [kKStages, kStages).
-  static constexpr bool kSplitRing = kPath == kPathBf16;
+  static constexpr bool kSplitRing = kPath == kPathBf16 || (kPath == kPathE4M3 && kTwoIssuers);
   static constexpr int kVStages = kSplitRing ? ((kStages + 1) / 2 > kDC ? (kStages + 1) / 2 : kDC) : kStages;
   static constexpr int kKStages = kSplitRing ? kStages - kVStages : kStages;
   static_assert(kKStages >= 1, "no room for a K ring");
@@ -127,6 +131,32 @@ __device__ __forceinline__ float redux_max(float v) {
   float r;
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
   return r;
+}
+
+// Per-row sums over the warp, transposed: given v[j] in every lane (R rows), lane l
+// returns the sum over all 32 lanes of v[l mod R].  A butterfly that halves the
+// rows at each step: the lane with the step's bit set keeps the upper half.
+template <int R>
+__device__ __forceinline__ float transpose_sum(const float (&v)[R], int lane) {
+  static_assert(R == 16 || R == 32, "rows per warp");
+  float a[R];
+#pragma unroll
+  for (int j = 0; j < R; ++j) a[j] = v[j];
+  if (R == 16) {
+#pragma unroll
+    for (int j = 0; j < R; ++j) a[j] += __shfl_xor_sync(0xFFFFFFFFu, a[j], 16);
+  }
+#pragma unroll
+  for (int off = R / 2; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int j = 0; j < off; ++j) {
+      const float send = upper ? a[j] : a[j + off];
+      const float keep = upper ? a[j + off] : a[j];
+      a[j] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+    }
+  }
+  return a[0];
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -260,20 +290,22 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
   uint64_t* pv_done = p_full + 2;
   uint64_t* o_empty = pv_done + 2;
   uint64_t* v_ready = o_empty + 1;  // tail tile: its V stages have landed (MMA thread -> softmax)
-  uint64_t* drain = v_ready + 1;
-  uint64_t* never = drain + 1;  // nothing arrives on it: the stall-injection test hook waits here
+  uint64_t* drain = v_ready + 1;  // [2]: one per MMA-issuing thread
+  uint64_t* never = drain + 2;    // nothing arrives on it: the stall-injection test hook waits here
   uint64_t* item_full = never + 1;
   uint64_t* item_empty = item_full + kItemSlots;
   uint64_t* kt_full = item_empty + kItemSlots;  // BF16 K slot in TMEM written (dequant -> MMA)
   uint64_t* kt_empty = kt_full + 2;             // BF16 K slot consumed (MMA commit -> dequant)
   ItemSlot* islot = reinterpret_cast<ItemSlot*>(kt_empty + 2);
-  float* red = reinterpret_cast<float*>(islot + kItemSlots);  // [2][4][N] per-warp tile maxima
+  // [N] element offset of each row's output (in out, or in o_part for a split)
+  long long* ooff_s = reinterpret_cast<long long*>((reinterpret_cast<uintptr_t>(islot + kItemSlots) + 15) & ~(uintptr_t)15);
+  float* red = reinterpret_cast<float*>(ooff_s + N);  // [2][4][N] per-warp tile maxima
   float* lred = red + 2 * 4 * N;                      // [4][N] per-warp row sums
   float* m_s = lred + 4 * N;                          // [N] running max (log2 units)
   float* a_s = m_s + N;                               // [N] rescale factor of this tile
   float* nmsub_s = a_s + N;                           // [N] exponent offset: P' = 2^(x + nmsub)
-  float* l_s = nmsub_s + N;                           // [N] final row sums
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(l_s + N);
+  float* inv_s = nmsub_s + N;                         // [N] output scale v_descale / l
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(inv_s + N);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -303,11 +335,12 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
     }
     mbar_init(o_empty, 4 * C::kNW);
     mbar_init(v_ready, 1);
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     mbar_init(never, 1);
     for (int i = 0; i < kItemSlots; ++i) {
       mbar_init(&item_full[i], 1);
-      mbar_init(&item_empty[i], 1 + 4 * C::kNW + (kDq ? 4 : 0));  // MMA thread, softmax and dequant warps
+      mbar_init(&item_empty[i], (C::kTwoIssuers ? 2 : 1) + 4 * C::kNW + (kDq ? 4 : 0));  // MMA, softmax, dequant
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -391,18 +424,26 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       for (uint32_t j = qit > (uint32_t)QB ? qit - QB : 0; j < qit; ++j)
         mbar_wait(&q_full[j % QB], (j / QB) & 1, kDrainWaitLimit);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || (C::kTwoIssuers && warp == 2)) {
+    // ------------------------------------------------------------------ MMA issuers
+    // One CTA per SM: warp 1 issues the QK^T MMAs and warp 2 the PV MMAs, so that
+    // neither waits behind the other's operands.  Two CTAs per SM: warp 1 issues
+    // both, in stage-stream order.
     if (lane == 0) {
+      const bool do_qk = !C::kTwoIssuers || warp == 1;
+      const bool do_pv = !C::kTwoIssuers || warp == 2;
       constexpr uint32_t idesc_qk = make_idesc(kQ8 ? kFmtE4M3 : kFmtBF16, kKMajor, kKMajor, 128, N);
       constexpr uint32_t idesc_pv = make_idesc(kP8 ? kFmtE4M3 : kFmtBF16, kMNMajor, kMNMajor, 128, N);
-      // idx: position in the K/V stage stream (one ring) or in the V ring (split rings);
-      // kidx: BF16 K chunks in TMEM; bidx: BF16 V tiles in shared memory
-      uint32_t idx = 0, kidx = 0, bidx = 0, g = 0, qit = 0;
-      // ring slot and phase parity of E4M3 stage position `pos`; the MMA thread
-      // reads K stages only on the E4M3 path and V stages only from the V ring
+      // E4M3 stages: idx = stage-stream position (one ring), or kq / vq = K and V
+      // ring positions (split rings); kidx: BF16 K chunks in TMEM; bidx: BF16 V
+      // tiles in shared memory
+      uint32_t idx = 0, kq = 0, vq = 0, kidx = 0, bidx = 0, g = 0, qit = 0;
+      auto kslot = [&](uint32_t pos) { return kSplit ? pos % SK : pos % S; };
+      auto kpar = [&](uint32_t pos) { return kSplit ? (pos / SK) & 1 : (pos / S) & 1; };
       auto vslot = [&](uint32_t pos) { return kSplit ? SK + pos % SV : pos % S; };
       auto vpar = [&](uint32_t pos) { return kSplit ? (pos / SV) & 1 : (pos / S) & 1; };
+      uint32_t& kpos = kSplit ? kq : idx;
+      uint32_t& vpos = kSplit ? vq : idx;
       bool ok = true;
       for (uint32_t ik = 0; ok; ++ik) {
         const uint32_t is = ik % kItemSlots;
@@ -414,7 +455,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         if (p.inject_stall && !(ok = pwait(never, 0, lim, abort_flag))) break;
         if (it.t1 <= it.t0) continue;
         const int qb = qit % QB;
-        if (!(ok = pwait(&q_full[qb], (qit / QB) & 1, lim, abort_flag))) break;
+        if (do_qk && !(ok = pwait(&q_full[qb], (qit / QB) & 1, lim, abort_flag))) break;
         tc_fence_after();
         const uint32_t qaddr = smem_u32(qbuf + qb * C::kQBytes);
         // S^T(gg) = K . Q^T into S buffer gg & 1
@@ -425,8 +466,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           const uint32_t d_tmem = tmem + sb * N;
           for (int c = 0; c < DC; ++c) {
             if (kQ8) {
-              const uint32_t slot = idx % S;
-              if (!pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag)) return false;
+              const uint32_t slot = kslot(kpos);
+              if (!pwait(&ring_full[slot], kpar(kpos), lim, abort_flag)) return false;
               tc_fence_after();
               const uint32_t a0 = smem_u32(ring + slot * kStageBytes), b0 = qaddr + c * N * 128;
 #pragma unroll
@@ -434,6 +475,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
                 mma_f8f6f4(d_tmem, make_sdesc(a0 + kk * 32, 16, 1024, kLayoutSW128),
                            make_sdesc(b0 + kk * 32, 16, 1024, kLayoutSW128), idesc_qk, (c | kk) != 0);
               mma_commit(&ring_empty[slot]);
+              ++kpos;
             } else {
               // BF16 K chunk (128 dims = 64 columns) in TMEM slot kidx & 1, written by the dequant warps
               const uint32_t ks = kidx & 1;
@@ -449,7 +491,6 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
               mma_commit(&kt_empty[ks]);
               ++kidx;
             }
-            if (!kSplit) ++idx;
           }
           mma_commit(&s_full[sb]);
           return true;
@@ -461,7 +502,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           const uint32_t pb = gg & 1;
           if (kP8 && tail) {
             for (int c = 0; c < DC; ++c)
-              if (!pwait(&ring_full[vslot(idx + c)], vpar(idx + c), lim, abort_flag)) return false;
+              if (!pwait(&ring_full[vslot(vpos + c)], vpar(vpos + c), lim, abort_flag)) return false;
             mbar_arrive(v_ready);
           }
           if (!pwait(&p_full[pb], (gg >> 1) & 1, lim, abort_flag)) return false;
@@ -471,8 +512,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           for (int c = 0; c < DC; ++c) {
             const uint32_t d_tmem = tmem + 2 * N + c * N;
             if (kP8) {
-              const uint32_t slot = vslot(idx);
-              if (!pwait(&ring_full[slot], vpar(idx), lim, abort_flag)) return false;
+              const uint32_t slot = vslot(vpos);
+              if (!pwait(&ring_full[slot], vpar(vpos), lim, abort_flag)) return false;
               tc_fence_after();
               const uint32_t a0 = smem_u32(ring + slot * kStageBytes);
 #pragma unroll
@@ -483,6 +524,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
                 mma_f8f6f4(d_tmem, va, make_sdesc(paddr + N * 128 + kk * 512, 128, 2048, kLayoutNone), idesc_pv, 1);
               }
               mma_commit(&ring_empty[slot]);
+              ++vpos;
             } else {
               const uint32_t slot = bidx % SBm;
               if (!pwait(&bf_full[slot], (bidx / SBm) & 1, lim, abort_flag)) return false;
@@ -495,36 +537,45 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
               mma_commit(&bf_empty[slot]);
               ++bidx;
             }
-            ++idx;
           }
           mma_commit(&pv_done[pb]);
           return true;
         };
         ++qit;  // pv() reads qit - 1 as this item's ordinal
         const int n = it.t1 - it.t0;
-        ok = qk(g);
-        for (int u = 0; u < n && ok; ++u) {
-          if (u + 1 < n) ok = qk(g + u + 1);
-          if (!ok) break;
-          if (u + 1 == n) mma_commit(&q_empty[qb]);
-          const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
-          ok = pv(g + u, u == 0, kb + kTileKeys > it.Lk);
+        auto is_tail = [&](int u) { return (it.pg_lo + 2 * (it.t0 + u)) * kPage + kTileKeys > it.Lk; };
+        if (C::kTwoIssuers) {
+          if (do_qk) {
+            for (int u = 0; u < n && ok; ++u) ok = qk(g + u);
+            if (ok) mma_commit(&q_empty[qb]);
+          } else {
+            for (int u = 0; u < n && ok; ++u) ok = pv(g + u, u == 0, is_tail(u));
+          }
+        } else {
+          ok = qk(g);
+          for (int u = 0; u < n && ok; ++u) {
+            if (u + 1 < n) ok = qk(g + u + 1);
+            if (!ok) break;
+            if (u + 1 == n) mma_commit(&q_empty[qb]);
+            ok = pv(g + u, u == 0, is_tail(u));
+          }
         }
         g += n;
       }
       if (!ok) flag_timeout(p, abort_flag);
-      mma_commit(drain);
-      mbar_wait(drain, 0, kDrainWaitLimit);
+      uint64_t* my_drain = do_qk ? drain : drain + 1;
+      mma_commit(my_drain);
+      mbar_wait(my_drain, 0, kDrainWaitLimit);
     }
   } else if (warp < C::kDqWarp0) {
     // ------------------------------------------------------------------ softmax / correction / epilogue
     // kNW warpgroups; warpgroup wg owns rows [r0, r0 + NR) of every tile and
     // synchronizes on its own two named barriers.
     constexpr int NR = C::kNR;
-    const int wg = C::kNW == 1 ? 0 : (warp - 2) >> 2;
+    const int wg = C::kNW == 1 ? 0 : (warp - C::kSmWarp0) >> 2;
     const int r0 = wg * NR;
     const uint32_t bar_a = 1 + 2 * wg, bar_b = 2 + 2 * wg;
-    const int wt = threadIdx.x - 64 - 128 * wg;  // 0..127 within the warpgroup
+    const int wt = threadIdx.x - 32 * C::kSmWarp0 - 128 * wg;  // 0..127 within the warpgroup
     const int quarter = warp & 3;                // TMEM lane quarter this warp may access
     const int kl = quarter * 32 + lane;          // key (S) or head-dim (O) lane within the tile
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -812,23 +863,29 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       // ---------------- epilogue: O / l, lse
       bool ok = pwait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, lim, abort_flag);
       ok = __all_sync(0xFFFFFFFFu, ok);
-#pragma unroll
-      for (int n = 0; n < NR; ++n) {
-        if (n < nr) {
-          float v = lt[n];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-          if (lane == (n & 31)) lred[quarter * N + r0 + n] = v;
-        }
+      {
+        const float rs = transpose_sum(lt, lane);  // this warp's sum for row (lane mod NR)
+        if (lane < NR) lred[quarter * N + r0 + lane] = rs;
       }
       if (!ok) flag_timeout(p, abort_flag);
       if (bar_red_or(bar_a, 128, !ok)) {
         aborted = true;
         break;
       }
+      // row owners: output scale vd / l, output offset and lse, once per row
       if (wt < nr) {
         const int n = r0 + wt;
-        l_s[n] = (lred[n] + lred[N + n]) + (lred[2 * N + n] + lred[3 * N + n]);
+        const float l = (lred[n] + lred[N + n]) + (lred[2 * N + n] + lred[3 * N + n]);
+        const int tok = row_tok(n), head = row_head(n);
+        const long long row = (long long)tok * p.hq + head;
+        inv_s[n] = l > 0.f ? vd / l : 0.f;
+        ooff_s[n] = (split_out ? (long long)it.split * p.total_q * p.hq + row : row) * D;
+        const float lse = l > 0.f ? (m_s[n] - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+        const size_t li = (size_t)head * p.total_q + tok;
+        if (split_out)
+          p.lse_part[(size_t)it.split * p.hq * p.total_q + li] = lse;
+        else if (p.lse)
+          p.lse[li] = lse;
       }
       named_bar_sync(bar_b, 128);
       tc_fence_after();
@@ -840,30 +897,18 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           if (cc >= nr) break;
           uint32_t r[16];
           tmem_load16(tmem + lane_base + 2 * N + c * N + r0 + cc, r);
+          if (split_out) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int n = r0 + cc + i;
-            if (cc + i < nr) {
-              const float l = l_s[n];
-              const float o = l > 0.f ? __uint_as_float(r[i]) / l * vd : 0.f;
-              const size_t row = (size_t)row_tok(n) * p.hq + row_head(n);
-              if (split_out)
-                p.o_part[((size_t)it.split * p.total_q * p.hq + row) * D + d] = o;
-              else
-                reinterpret_cast<__nv_bfloat16*>(p.out)[row * D + d] = __float2bfloat16_rn(o);
-            }
+            for (int i = 0; i < 16; ++i)
+              if (cc + i < nr) p.o_part[ooff_s[r0 + cc + i] + d] = __uint_as_float(r[i]) * inv_s[r0 + cc + i];
+          } else {
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (cc + i < nr)
+                out[ooff_s[r0 + cc + i] + d] = __float2bfloat16_rn(__uint_as_float(r[i]) * inv_s[r0 + cc + i]);
           }
         }
-      }
-      if (wt < nr) {
-        const int n = r0 + wt;
-        const float l = l_s[n];
-        const float lse = l > 0.f ? (m_s[n] - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
-        const size_t li = (size_t)row_head(n) * p.total_q + row_tok(n);
-        if (split_out)
-          p.lse_part[(size_t)it.split * p.hq * p.total_q + li] = lse;
-        else if (p.lse)
-          p.lse[li] = lse;
       }
       tc_fence_before();
       __syncwarp();
