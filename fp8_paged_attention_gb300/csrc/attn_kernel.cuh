@@ -362,28 +362,42 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane takes work items, publishes
+    // them and issues the copies, and every wait is a vote of the warp.
+    {
+      const bool leader = elect_one();
+      const int leader_lane = __ffs(__ballot_sync(0xFFFFFFFFu, leader)) - 1;
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xFFFFFFFFu, pwait(bar, parity, lim, abort_flag));
+      };
       // idx: stage stream position (one ring); kq / vq: K and V ring positions (split rings)
       uint32_t idx = 0, kq = 0, vq = 0, qit = 0;
       bool ok = true;
       for (uint32_t ik = 0; ok; ++ik) {
-        const int w = atomicAdd(p.work_next, 1);
+        int w = 0;
+        if (leader) w = atomicAdd(p.work_next, 1);
+        w = __shfl_sync(0xFFFFFFFFu, w, leader_lane);
         const bool valid = w < n_items;
         const uint32_t is = ik % kItemSlots;
-        if (!(ok = pwait(&item_empty[is], ((ik / kItemSlots) & 1) ^ 1, lim, abort_flag))) break;
+        if (!(ok = wait_all(&item_empty[is], ((ik / kItemSlots) & 1) ^ 1))) break;
         Item it{};
         if (valid) it = decode_item(p, p.work[w]);
-        islot[is].it = it;
-        islot[is].valid = valid;
-        mbar_arrive(&item_full[is]);  // release: the slot's contents are visible to waiters
+        if (leader) {
+          islot[is].it = it;
+          islot[is].valid = valid;
+          mbar_arrive(&item_full[is]);  // release: the slot's contents are visible to waiters
+        }
+        __syncwarp();
         if (!valid) break;
         if (it.t1 <= it.t0) continue;
         const int qb = qit % QB;
-        if (!(ok = pwait(&q_empty[qb], ((qit / QB) & 1) ^ 1, lim, abort_flag))) break;
-        mbar_arrive_expect_tx(&q_full[qb], C::kQBytes);
-        for (int c = 0; c < C::kQChunks; ++c)
-          tma_load_3d(qbuf + qb * C::kQBytes + c * N * 128, &tm_q, &q_full[qb], c * C::kQChunkElems,
-                      it.hk * p.group, it.q0 + it.row0 / p.group);
+        if (!(ok = wait_all(&q_empty[qb], ((qit / QB) & 1) ^ 1))) break;
+        if (leader) {
+          mbar_arrive_expect_tx(&q_full[qb], C::kQBytes);
+          for (int c = 0; c < C::kQChunks; ++c)
+            tma_load_3d(qbuf + qb * C::kQBytes + c * N * 128, &tm_q, &q_full[qb], c * C::kQChunkElems,
+                        it.hk * p.group, it.q0 + it.row0 / p.group);
+        }
         ++qit;
         const int n = it.t1 - it.t0;
         auto load_tile = [&](int u, bool is_v) -> bool {
@@ -394,11 +408,13 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
             uint32_t& pos = !kSplit ? idx : is_v ? vq : kq;
             const uint32_t len = !kSplit ? S : is_v ? SV : SK;
             const uint32_t slot = (kSplit && is_v ? SK : 0) + pos % len;
-            if (!pwait(&ring_empty[slot], ((pos / len) & 1) ^ 1, lim, abort_flag)) return false;
-            mbar_arrive_expect_tx(&ring_full[slot], kStageBytes);
-            uint8_t* dst = ring + slot * kStageBytes;
-            tma_load_4d(dst, tm, &ring_full[slot], c * 128, it.hk, 0, pa);
-            tma_load_4d(dst + kStageBytes / 2, tm, &ring_full[slot], c * 128, it.hk, 0, pb);
+            if (!wait_all(&ring_empty[slot], ((pos / len) & 1) ^ 1)) return false;
+            if (leader) {
+              mbar_arrive_expect_tx(&ring_full[slot], kStageBytes);
+              uint8_t* dst = ring + slot * kStageBytes;
+              tma_load_4d(dst, tm, &ring_full[slot], c * 128, it.hk, 0, pa);
+              tma_load_4d(dst + kStageBytes / 2, tm, &ring_full[slot], c * 128, it.hk, 0, pb);
+            }
             ++pos;
           }
           return true;
@@ -409,7 +425,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           if (ok) ok = load_tile(u - 1, true);
         }
       }
-      if (!ok) flag_timeout(p, abort_flag);
+      if (!ok && leader) flag_timeout(p, abort_flag);
       // drain: every issued copy must land before the CTA may exit
       auto drain_ring = [&](uint32_t pos, uint32_t len, uint32_t first) {
         for (uint32_t j = pos > len ? pos - len : 0; j < pos; ++j)
@@ -428,8 +444,14 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
     // ------------------------------------------------------------------ MMA issuers
     // One CTA per SM: warp 1 issues the QK^T MMAs and warp 2 the PV MMAs, so that
     // neither waits behind the other's operands.  Two CTAs per SM: warp 1 issues
-    // both, in stage-stream order.
-    if (lane == 0) {
+    // both, in stage-stream order.  The whole warp runs the loop (so descriptors
+    // and counters stay warp-uniform); one elected lane issues the MMAs, commits
+    // and arrivals, and every wait is a vote of the warp.
+    {
+      const bool leader = elect_one();
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xFFFFFFFFu, pwait(bar, parity, lim, abort_flag));
+      };
       const bool do_qk = !C::kTwoIssuers || warp == 1;
       const bool do_pv = !C::kTwoIssuers || warp == 2;
       constexpr uint32_t idesc_qk = make_idesc(kQ8 ? kFmtE4M3 : kFmtBF16, kKMajor, kKMajor, 128, N);
@@ -447,52 +469,57 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       bool ok = true;
       for (uint32_t ik = 0; ok; ++ik) {
         const uint32_t is = ik % kItemSlots;
-        if (!(ok = pwait(&item_full[is], (ik / kItemSlots) & 1, lim, abort_flag))) break;
+        if (!(ok = wait_all(&item_full[is], (ik / kItemSlots) & 1))) break;
         const Item it = islot[is].it;
         const bool valid = islot[is].valid != 0;
-        mbar_arrive(&item_empty[is]);
+        __syncwarp();
+        if (leader) mbar_arrive(&item_empty[is]);
         if (!valid) break;
-        if (p.inject_stall && !(ok = pwait(never, 0, lim, abort_flag))) break;
+        if (p.inject_stall && !(ok = wait_all(never, 0))) break;
         if (it.t1 <= it.t0) continue;
         const int qb = qit % QB;
-        if (do_qk && !(ok = pwait(&q_full[qb], (qit / QB) & 1, lim, abort_flag))) break;
+        if (do_qk && !(ok = wait_all(&q_full[qb], (qit / QB) & 1))) break;
         tc_fence_after();
         const uint32_t qaddr = smem_u32(qbuf + qb * C::kQBytes);
         // S^T(gg) = K . Q^T into S buffer gg & 1
         auto qk = [&](uint32_t gg) -> bool {
           const uint32_t sb = gg & 1;
-          if (!pwait(&s_empty[sb], ((gg >> 1) & 1) ^ 1, lim, abort_flag)) return false;
+          if (!wait_all(&s_empty[sb], ((gg >> 1) & 1) ^ 1)) return false;
           tc_fence_after();
           const uint32_t d_tmem = tmem + sb * N;
           for (int c = 0; c < DC; ++c) {
             if (kQ8) {
               const uint32_t slot = kslot(kpos);
-              if (!pwait(&ring_full[slot], kpar(kpos), lim, abort_flag)) return false;
+              if (!wait_all(&ring_full[slot], kpar(kpos))) return false;
               tc_fence_after();
               const uint32_t a0 = smem_u32(ring + slot * kStageBytes), b0 = qaddr + c * N * 128;
+              if (leader) {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f8f6f4(d_tmem, make_sdesc(a0 + kk * 32, 16, 1024, kLayoutSW128),
-                           make_sdesc(b0 + kk * 32, 16, 1024, kLayoutSW128), idesc_qk, (c | kk) != 0);
-              mma_commit(&ring_empty[slot]);
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_f8f6f4(d_tmem, make_sdesc(a0 + kk * 32, 16, 1024, kLayoutSW128),
+                             make_sdesc(b0 + kk * 32, 16, 1024, kLayoutSW128), idesc_qk, (c | kk) != 0);
+                mma_commit(&ring_empty[slot]);
+              }
               ++kpos;
             } else {
               // BF16 K chunk (128 dims = 64 columns) in TMEM slot kidx & 1, written by the dequant warps
               const uint32_t ks = kidx & 1;
-              if (!pwait(&kt_full[ks], (kidx >> 1) & 1, lim, abort_flag)) return false;
+              if (!wait_all(&kt_full[ks], (kidx >> 1) & 1)) return false;
               tc_fence_after();
               const uint32_t a_t = tmem + C::kKCol + ks * 64;
+              if (leader) {
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                mma_f16_tmem_a(d_tmem, a_t + kk * 8,
-                               make_sdesc(qaddr + (2 * c + (kk >> 2)) * N * 128 + (kk & 3) * 32, 16, 1024,
-                                          kLayoutSW128),
-                               idesc_qk, (c | kk) != 0);
-              mma_commit(&kt_empty[ks]);
+                for (int kk = 0; kk < 8; ++kk)
+                  mma_f16_tmem_a(d_tmem, a_t + kk * 8,
+                                 make_sdesc(qaddr + (2 * c + (kk >> 2)) * N * 128 + (kk & 3) * 32, 16, 1024,
+                                            kLayoutSW128),
+                                 idesc_qk, (c | kk) != 0);
+                mma_commit(&kt_empty[ks]);
+              }
               ++kidx;
             }
           }
-          mma_commit(&s_full[sb]);
+          if (leader) mma_commit(&s_full[sb]);
           return true;
         };
         // O^T += V^T . P^T(gg).  On a tail tile (keys past Lk) with E4M3 V the
@@ -502,43 +529,48 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           const uint32_t pb = gg & 1;
           if (kP8 && tail) {
             for (int c = 0; c < DC; ++c)
-              if (!pwait(&ring_full[vslot(vpos + c)], vpar(vpos + c), lim, abort_flag)) return false;
-            mbar_arrive(v_ready);
+              if (!wait_all(&ring_full[vslot(vpos + c)], vpar(vpos + c))) return false;
+            if (leader) mbar_arrive(v_ready);
           }
-          if (!pwait(&p_full[pb], (gg >> 1) & 1, lim, abort_flag)) return false;
-          if (first && !pwait(o_empty, ((qit - 1) & 1) ^ 1, lim, abort_flag)) return false;
+          if (!wait_all(&p_full[pb], (gg >> 1) & 1)) return false;
+          if (first && !wait_all(o_empty, ((qit - 1) & 1) ^ 1)) return false;
           tc_fence_after();
           const uint32_t paddr = smem_u32(pbuf + pb * C::kPBytes);
           for (int c = 0; c < DC; ++c) {
             const uint32_t d_tmem = tmem + 2 * N + c * N;
             if (kP8) {
               const uint32_t slot = vslot(vpos);
-              if (!pwait(&ring_full[slot], vpar(vpos), lim, abort_flag)) return false;
+              if (!wait_all(&ring_full[slot], vpar(vpos))) return false;
               tc_fence_after();
               const uint32_t a0 = smem_u32(ring + slot * kStageBytes);
+              if (leader) {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t va = make_sdesc(a0 + kk * 4096, 16384, 1024, kLayoutSW128);
-                mma_f8f6f4(d_tmem, va, make_sdesc(paddr + kk * 512, 128, 2048, kLayoutNone), idesc_pv,
-                           !(first && kk == 0));
-                mma_f8f6f4(d_tmem, va, make_sdesc(paddr + N * 128 + kk * 512, 128, 2048, kLayoutNone), idesc_pv, 1);
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t va = make_sdesc(a0 + kk * 4096, 16384, 1024, kLayoutSW128);
+                  mma_f8f6f4(d_tmem, va, make_sdesc(paddr + kk * 512, 128, 2048, kLayoutNone), idesc_pv,
+                             !(first && kk == 0));
+                  mma_f8f6f4(d_tmem, va, make_sdesc(paddr + N * 128 + kk * 512, 128, 2048, kLayoutNone), idesc_pv,
+                             1);
+                }
+                mma_commit(&ring_empty[slot]);
               }
-              mma_commit(&ring_empty[slot]);
               ++vpos;
             } else {
               const uint32_t slot = bidx % SBm;
-              if (!pwait(&bf_full[slot], (bidx / SBm) & 1, lim, abort_flag)) return false;
+              if (!wait_all(&bf_full[slot], (bidx / SBm) & 1)) return false;
               tc_fence_after();
               const uint32_t a0 = smem_u32(bfbuf + slot * C::kBfSlotBytes);
+              if (leader) {
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                mma_f16(d_tmem, make_sdesc(a0 + kk * 2048, 16384, 1024, kLayoutSW128),
-                        make_sdesc(paddr + kk * 256, 128, 2048, kLayoutNone), idesc_pv, !(first && kk == 0));
-              mma_commit(&bf_empty[slot]);
+                for (int kk = 0; kk < 8; ++kk)
+                  mma_f16(d_tmem, make_sdesc(a0 + kk * 2048, 16384, 1024, kLayoutSW128),
+                          make_sdesc(paddr + kk * 256, 128, 2048, kLayoutNone), idesc_pv, !(first && kk == 0));
+                mma_commit(&bf_empty[slot]);
+              }
               ++bidx;
             }
           }
-          mma_commit(&pv_done[pb]);
+          if (leader) mma_commit(&pv_done[pb]);
           return true;
         };
         ++qit;  // pv() reads qit - 1 as this item's ordinal
@@ -547,7 +579,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         if (C::kTwoIssuers) {
           if (do_qk) {
             for (int u = 0; u < n && ok; ++u) ok = qk(g + u);
-            if (ok) mma_commit(&q_empty[qb]);
+            if (ok && leader) mma_commit(&q_empty[qb]);
           } else {
             for (int u = 0; u < n && ok; ++u) ok = pv(g + u, u == 0, is_tail(u));
           }
@@ -556,15 +588,16 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           for (int u = 0; u < n && ok; ++u) {
             if (u + 1 < n) ok = qk(g + u + 1);
             if (!ok) break;
-            if (u + 1 == n) mma_commit(&q_empty[qb]);
+            if (u + 1 == n && leader) mma_commit(&q_empty[qb]);
             ok = pv(g + u, u == 0, is_tail(u));
           }
         }
         g += n;
       }
-      if (!ok) flag_timeout(p, abort_flag);
+      if (!ok && leader) flag_timeout(p, abort_flag);
       uint64_t* my_drain = do_qk ? drain : drain + 1;
-      mma_commit(my_drain);
+      if (leader) mma_commit(my_drain);
+      __syncwarp();
       mbar_wait(my_drain, 0, kDrainWaitLimit);
     }
   } else if (warp < C::kDqWarp0) {

@@ -50,6 +50,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// One lane of the (converged) warp: true in exactly one lane.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(e));
+  return e != 0;
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Wait until the grids this one depends on (the previous kernel in the stream)
 // have completed and their memory is visible; a grid launched with programmatic
