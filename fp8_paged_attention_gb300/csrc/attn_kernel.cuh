@@ -693,16 +693,17 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         // raw scores of this warpgroup's rows for this thread's key; masked keys at -inf
         auto load_scores = [&]() {
           tc_fence_after();
+          if (NR == 32 && nr > 16) {
+            tmem_load32f(tmem + lane_base + sb * N + r0, x);  // one 32-column load, one wait
+          } else {
 #pragma unroll
-          for (int c = 0; c < NR; c += 16) {
-            if (c < nr) {
-              uint32_t r[16];
-              tmem_load16(tmem + lane_base + sb * N + r0 + c, r);
+            for (int c = 0; c < NR; c += 16) {
+              if (c < nr) {
+                tmem_load16f(tmem + lane_base + sb * N + r0 + c, x + c);
+              } else {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(r[i]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) x[c + i] = NEG_INF;
+                for (int i = 0; i < 16; ++i) x[c + i] = NEG_INF;
+              }
             }
           }
           if (!interior) {
@@ -922,6 +923,20 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       }
       named_bar_sync(bar_b, 128);
       tc_fence_after();
+      // O^T columns of this warpgroup's rows, 16 (or 32) at a time, scaled and stored
+      auto store_rows = [&](const uint32_t* r, int cc, int cnt, int d) {
+        if (split_out) {
+#pragma unroll
+          for (int i = 0; i < cnt; ++i)
+            if (cc + i < nr) p.o_part[ooff_s[r0 + cc + i] + d] = __uint_as_float(r[i]) * inv_s[r0 + cc + i];
+        } else {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+          for (int i = 0; i < cnt; ++i)
+            if (cc + i < nr)
+              out[ooff_s[r0 + cc + i] + d] = __float2bfloat16_rn(__uint_as_float(r[i]) * inv_s[r0 + cc + i]);
+        }
+      };
 #pragma unroll 1
       for (int c = 0; c < DC; ++c) {
         const int d = c * 128 + kl;
@@ -930,17 +945,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           if (cc >= nr) break;
           uint32_t r[16];
           tmem_load16(tmem + lane_base + 2 * N + c * N + r0 + cc, r);
-          if (split_out) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (cc + i < nr) p.o_part[ooff_s[r0 + cc + i] + d] = __uint_as_float(r[i]) * inv_s[r0 + cc + i];
-          } else {
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (cc + i < nr)
-                out[ooff_s[r0 + cc + i] + d] = __float2bfloat16_rn(__uint_as_float(r[i]) * inv_s[r0 + cc + i]);
-          }
+          store_rows(r, cc, 16, d);
         }
       }
       tc_fence_before();

@@ -172,6 +172,26 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 #undef FP8PA_R8
+// The same loads straight into float registers (a 32-bit TMEM column is a float).
+#define FP8PA_F8(o) "=f"(x[o + 0]), "=f"(x[o + 1]), "=f"(x[o + 2]), "=f"(x[o + 3]), \
+                    "=f"(x[o + 4]), "=f"(x[o + 5]), "=f"(x[o + 6]), "=f"(x[o + 7])
+__device__ __forceinline__ void tmem_load16f(uint32_t taddr, float* x) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : FP8PA_F8(0), FP8PA_F8(8)
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_load32f(uint32_t taddr, float* x) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : FP8PA_F8(0), FP8PA_F8(8), FP8PA_F8(16), FP8PA_F8(24)
+      : "r"(taddr)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_store16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
