@@ -148,6 +148,7 @@ struct CallPlan {
   int num_classes;
   ClassInfo cls[2];
   int splits;
+  bool prefill_kernel;  // class 1 runs the rows-on-lanes prefill kernel (128-row tiles)
   size_t items_max[2];
   size_t off_work[2], off_opart, off_lsepart, total;
 };
@@ -206,6 +207,9 @@ int make_plan(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int hea
                 "q dtype bfloat16 with k/v dtype float8_e4m3fn at head_size 256 is not supported "
                 "(head_size 256 takes E4M3 Q; quantize it with quantize_q_fp8)");
   pl.fp8_q = q_dtype == FP8PA_E4M3;
+  // prefill-class tiles at head dim 256 (E4M3 Q) run the rows-on-lanes kernel with 128 rows
+  pl.prefill_kernel = head_dim == 256 && pl.fp8_q;
+  const int prefill_rows = pl.prefill_kernel ? 128 : 64;
   const int g = hq / hkv;
   pl.group = g;
   const long long rmax = (long long)max_seqlen_q * g;
@@ -219,11 +223,11 @@ int make_plan(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int hea
     if (lq0_max >= 1) {
       pl.num_classes = 2;
       pl.cls[0] = ClassInfo{1, lq0_max, 16, 1};
-      pl.cls[1] = ClassInfo{lq0_max + 1, max_seqlen_q, 64, 1};
+      pl.cls[1] = ClassInfo{lq0_max + 1, max_seqlen_q, prefill_rows, 1};
     } else {
       pl.num_classes = 2;  // class 0 empty
       pl.cls[0] = ClassInfo{1, 0, 16, 1};
-      pl.cls[1] = ClassInfo{1, max_seqlen_q, 64, 1};
+      pl.cls[1] = ClassInfo{1, max_seqlen_q, prefill_rows, 1};
       lq0_max = 1;
     }
   }
@@ -435,8 +439,11 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
     p.work_count = counts + k;
     p.work_next = counts + 2 + k;
     const int path = kernel_path(fp8_q);
-    e = launch_attn(head_dim, path, pl.cls[k].rows, ctas_per_sm(head_dim, path, pl.cls[k].rows), p, tm_q[k], tm_k,
-                    tm_v, sms, st);
+    if (k == 1 && pl.prefill_kernel)
+      e = launch_attn_prefill_d256(p, tm_q[k], tm_k, tm_v, sms, st);
+    else
+      e = launch_attn(head_dim, path, pl.cls[k].rows, ctas_per_sm(head_dim, path, pl.cls[k].rows), p, tm_q[k], tm_k,
+                      tm_v, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   }
   if (timed && (e = cudaEventRecord(g_ev_stop, st)) != cudaSuccess) return cuda_fail(e, "timing event");

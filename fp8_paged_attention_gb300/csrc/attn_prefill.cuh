@@ -1,0 +1,484 @@
+// Paged FP8-KV attention forward for prefill row tiles, sm_103a: E4M3 Q, K and
+// V at head dim 256, 128 packed query rows per tile.
+//
+// The decode kernel puts keys on the TMEM lanes (swap-AB) so that a handful of
+// query rows still fills an MMA.  A prefill tile has rows to spare, so here the
+// rows sit on the lanes and every row reduction is thread-local:
+//
+//   S[row, key] = Q[row, :] . K[key, :]     tcgen05.mma  M = 128 rows, N = 128 keys
+//   P'[row, key] = 2^(S * scale - m + 4)    one softmax thread per row
+//   O[row, d] += P[row, key] V[key, d]       tcgen05.mma  A = P from TMEM, N = D
+//
+// Rows pack (query token, query head of the KV group) token-major, as in the
+// decode kernel.  P' is requantized as an E4M3 pair hi = e4m3(P'),
+// lo = e4m3(P' - hi) with both terms accumulated into O, and the running row
+// maximum m moves only when a tile maximum exceeds it by more than 4 (log2
+// units), so P' <= 256.
+//
+// Tensor memory (512 columns): two S buffers of 128 columns; P's hi and lo
+// terms (32 columns each, four keys per column) overwrite the first 64 columns
+// of their S buffer once the row's scores are in registers; O takes D columns.
+//
+// Warps: 0 TMA producer, 1 QK^T issuer (and TMEM owner), 2 PV issuer, 3-6
+// softmax / O correction / epilogue (thread = row).  The producer and the
+// issuers run warp-uniform loops with one elected lane issuing; the softmax
+// warps synchronize with the issuers only through mbarriers.
+#pragma once
+#include "attn_kernel.cuh"
+#include "kernels.h"
+
+namespace fp8pa {
+
+template <int D>
+struct PrefillCfg {
+  static_assert(D == 256, "tensor memory holds two 128-column S buffers and O only for D = 256");
+  static constexpr int kRows = 128;
+  static constexpr int kDC = D / 128;                     // 128-byte chunks of an E4M3 row
+  static constexpr int kQBytes = kDC * kRows * 128;       // chunk c of every row at c * 16 KB
+  static constexpr int kQBufs = 2;
+  static constexpr int kKStageBytes = kStageBytes;        // 128 keys x one 128-byte chunk
+  static constexpr int kVStageBytes = kDC * kStageBytes;  // 128 keys x D bytes, chunk c at c * 16 KB
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 3;
+  static constexpr int kThreads = 7 * 32;
+  static constexpr int kCtrlBytes = 2048;
+  static constexpr int kSmemBytes =
+      kQBufs * kQBytes + kKStages * kKStageBytes + kVStages * kVStageBytes + kCtrlBytes + 1024;
+  static_assert(kSmemBytes <= 232448, "smem");
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kOCol = 256;  // O columns [256, 256 + D)
+  static_assert(kOCol + D <= 512, "TMEM");
+  static constexpr float kTau = 4.0f;
+  static constexpr float kPShift = 4.0f;
+};
+
+template <int D>
+__global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
+    attn_prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+  using C = PrefillCfg<D>;
+  using namespace ptx;
+  using namespace detail;
+  constexpr int DC = C::kDC, SK = C::kKStages, SV = C::kVStages, QB = C::kQBufs;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  // V ring lowest: its MMA operand spans two 16 KB blocks of a stage, and every
+  // byte past a stage still lies inside this CTA's allocation
+  uint8_t* vring = smem;
+  uint8_t* kring = vring + SV * C::kVStageBytes;
+  uint8_t* qbuf = kring + SK * C::kKStageBytes;
+  uint8_t* ctrl = qbuf + QB * C::kQBytes;
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* k_empty = k_full + SK;
+  uint64_t* v_full = k_empty + SK;
+  uint64_t* v_empty = v_full + SV;
+  uint64_t* q_full = v_empty + SV;
+  uint64_t* q_empty = q_full + QB;
+  uint64_t* s_full = q_empty + QB;  // [2] QK^T done: S buffer readable
+  uint64_t* s_free = s_full + 2;    // [2] PV done: S/P buffer reusable, O up to date
+  uint64_t* p_full = s_free + 2;    // [2] P written (four softmax warps)
+  uint64_t* o_empty = p_full + 2;   // epilogue read O (four softmax warps)
+  uint64_t* v_ready = o_empty + 1;  // tail tile: its V stage landed (PV issuer -> softmax)
+  uint64_t* drain = v_ready + 1;    // [2] one per issuer
+  uint64_t* never = drain + 2;      // nothing arrives on it: the stall-injection hook waits here
+  uint64_t* item_full = never + 1;
+  uint64_t* item_empty = item_full + kItemSlots;
+  ItemSlot* islot = reinterpret_cast<ItemSlot*>(item_empty + kItemSlots);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(islot + kItemSlots);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < SV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < QB; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 1);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&drain[i], 1);
+    }
+    mbar_init(o_empty, 4);
+    mbar_init(v_ready, 1);
+    mbar_init(never, 1);
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_empty[i], 2 + 4);  // two issuers, four softmax warps
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  griddep_wait();  // the work list, Q and the K/V cache are written by earlier kernels
+  const uint32_t tmem = *tmem_slot;
+  const int n_items = *p.work_count;
+  const uint32_t lim = p.wait_limit;
+
+  if (warp <= 2) {
+    // ---------------------------------------------------------------- producer and MMA issuers
+    const bool leader = elect_one();
+    const int leader_lane = __ffs(__ballot_sync(0xFFFFFFFFu, leader)) - 1;
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xFFFFFFFFu, pwait(bar, parity, lim, abort_flag));
+    };
+    uint32_t kq = 0, vq = 0, qit = 0, g = 0;  // K / V ring positions, Q tiles, S/P tiles
+    bool ok = true;
+    for (uint32_t ik = 0; ok; ++ik) {
+      const uint32_t is = ik % kItemSlots;
+      Item it{};
+      bool valid;
+      if (warp == 0) {
+        int w = 0;
+        if (leader) w = atomicAdd(p.work_next, 1);
+        w = __shfl_sync(0xFFFFFFFFu, w, leader_lane);
+        valid = w < n_items;
+        if (!(ok = wait_all(&item_empty[is], ((ik / kItemSlots) & 1) ^ 1))) break;
+        if (valid) it = decode_item(p, p.work[w]);
+        if (leader) {
+          islot[is].it = it;
+          islot[is].valid = valid;
+          mbar_arrive(&item_full[is]);  // release: the slot's contents are visible to waiters
+        }
+        __syncwarp();
+      } else {
+        if (!(ok = wait_all(&item_full[is], (ik / kItemSlots) & 1))) break;
+        it = islot[is].it;
+        valid = islot[is].valid != 0;
+        __syncwarp();
+        if (leader) mbar_arrive(&item_empty[is]);
+        if (valid && p.inject_stall && !(ok = wait_all(never, 0))) break;
+      }
+      if (!valid) break;
+      if (it.t1 <= it.t0) continue;
+      const int n = it.t1 - it.t0;
+      const int qb = qit % QB;
+      const uint32_t qpar = (qit / QB) & 1;
+      ++qit;
+      if (warp == 0) {
+        // Q tile, then K(0), [K(1), V(0)], [K(2), V(1)], ..., V(n-1)
+        if (!(ok = wait_all(&q_empty[qb], qpar ^ 1))) break;
+        if (leader) {
+          mbar_arrive_expect_tx(&q_full[qb], C::kQBytes);
+          for (int c = 0; c < DC; ++c)
+            tma_load_3d(qbuf + qb * C::kQBytes + c * C::kRows * 128, &tm_q, &q_full[qb], c * 128, it.hk * p.group,
+                        it.q0 + it.row0 / p.group);
+        }
+        auto load_k = [&](int u) -> bool {
+          const int pg = it.pg_lo + 2 * (it.t0 + u);
+          const int pa = page_id(p, it, pg), pb = page_id(p, it, pg + 1);
+          for (int c = 0; c < DC; ++c) {
+            const uint32_t slot = kq % SK;
+            if (!wait_all(&k_empty[slot], ((kq / SK) & 1) ^ 1)) return false;
+            if (leader) {
+              uint8_t* dst = kring + slot * C::kKStageBytes;
+              mbar_arrive_expect_tx(&k_full[slot], C::kKStageBytes);
+              tma_load_4d(dst, &tm_k, &k_full[slot], c * 128, it.hk, 0, pa);
+              tma_load_4d(dst + C::kKStageBytes / 2, &tm_k, &k_full[slot], c * 128, it.hk, 0, pb);
+            }
+            ++kq;
+          }
+          return true;
+        };
+        auto load_v = [&](int u) -> bool {
+          const int pg = it.pg_lo + 2 * (it.t0 + u);
+          const int pa = page_id(p, it, pg), pb = page_id(p, it, pg + 1);
+          const uint32_t slot = vq % SV;
+          if (!wait_all(&v_empty[slot], ((vq / SV) & 1) ^ 1)) return false;
+          if (leader) {
+            uint8_t* dst = vring + slot * C::kVStageBytes;
+            mbar_arrive_expect_tx(&v_full[slot], C::kVStageBytes);
+            for (int c = 0; c < DC; ++c) {
+              tma_load_4d(dst + c * kStageBytes, &tm_v, &v_full[slot], c * 128, it.hk, 0, pa);
+              tma_load_4d(dst + c * kStageBytes + kStageBytes / 2, &tm_v, &v_full[slot], c * 128, it.hk, 0, pb);
+            }
+          }
+          ++vq;
+          return true;
+        };
+        ok = load_k(0);
+        for (int u = 1; u <= n && ok; ++u) {
+          if (u < n) ok = load_k(u);
+          if (ok) ok = load_v(u - 1);
+        }
+      } else if (warp == 1) {
+        // S(g) = Q . K^T into S buffer g & 1, once PV(g - 2) has released it
+        constexpr uint32_t idesc = make_idesc(kFmtE4M3, kKMajor, kKMajor, 128, 128);
+        if (!(ok = wait_all(&q_full[qb], qpar))) break;
+        tc_fence_after();
+        const uint32_t qaddr = smem_u32(qbuf + qb * C::kQBytes);
+        for (int u = 0; u < n && ok; ++u) {
+          const uint32_t gg = g + u, sb = gg & 1;
+          if (!(ok = wait_all(&s_free[sb], ((gg >> 1) & 1) ^ 1))) break;
+          tc_fence_after();
+          for (int c = 0; c < DC && ok; ++c) {
+            const uint32_t slot = kq % SK;
+            if (!(ok = wait_all(&k_full[slot], (kq / SK) & 1))) break;
+            tc_fence_after();
+            const uint32_t a0 = qaddr + c * C::kRows * 128, b0 = smem_u32(kring + slot * C::kKStageBytes);
+            if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8f6f4(tmem + sb * 128, make_sdesc(a0 + kk * 32, 16, 1024, kLayoutSW128),
+                           make_sdesc(b0 + kk * 32, 16, 1024, kLayoutSW128), idesc, (c | kk) != 0);
+              mma_commit(&k_empty[slot]);
+            }
+            ++kq;
+          }
+          if (ok && leader) mma_commit(&s_full[sb]);
+        }
+        if (ok && leader) mma_commit(&q_empty[qb]);
+      } else {
+        // O += P(g) . V(g): A = P hi and lo terms from TMEM, B = V (MN-major, N = D)
+        constexpr uint32_t idesc = make_idesc(kFmtE4M3, kKMajor, kMNMajor, 128, D);
+        for (int u = 0; u < n && ok; ++u) {
+          const uint32_t gg = g + u, sb = gg & 1;
+          const uint32_t slot = vq % SV, vpar = (vq / SV) & 1;
+          const bool tail = (it.pg_lo + 2 * (it.t0 + u)) * kPage + kTileKeys > it.Lk;
+          if (tail) {
+            // the softmax zeroes this tile's V rows past Lk once the stage has landed
+            if (!(ok = wait_all(&v_full[slot], vpar))) break;
+            if (leader) mbar_arrive(v_ready);
+          }
+          if (!(ok = wait_all(&p_full[sb], (gg >> 1) & 1))) break;
+          if (u == 0 && !(ok = wait_all(o_empty, ((qit - 1) & 1) ^ 1))) break;
+          if (!(ok = wait_all(&v_full[slot], vpar))) break;
+          tc_fence_after();
+          const uint32_t v0 = smem_u32(vring + slot * C::kVStageBytes);
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t vb = make_sdesc(v0 + kk * 4096, kStageBytes, 1024, kLayoutSW128);
+              mma_f8f6f4_tmem_a(tmem + C::kOCol, tmem + sb * 128 + kk * 8, vb, idesc, !(u == 0 && kk == 0));
+              mma_f8f6f4_tmem_a(tmem + C::kOCol, tmem + sb * 128 + 32 + kk * 8, vb, idesc, 1);
+            }
+            mma_commit(&v_empty[slot]);
+            mma_commit(&s_free[sb]);
+          }
+          ++vq;
+        }
+      }
+      g += n;
+    }
+    if (!ok && leader) flag_timeout(p, abort_flag);
+    if (warp == 0) {
+      // every issued copy must land before the CTA may exit
+      for (uint32_t j = kq > (uint32_t)SK ? kq - SK : 0; j < kq; ++j)
+        mbar_wait(&k_full[j % SK], (j / SK) & 1, kDrainWaitLimit);
+      for (uint32_t j = vq > (uint32_t)SV ? vq - SV : 0; j < vq; ++j)
+        mbar_wait(&v_full[j % SV], (j / SV) & 1, kDrainWaitLimit);
+      for (uint32_t j = qit > (uint32_t)QB ? qit - QB : 0; j < qit; ++j)
+        mbar_wait(&q_full[j % QB], (j / QB) & 1, kDrainWaitLimit);
+    } else {
+      uint64_t* my_drain = &drain[warp - 1];
+      if (leader) mma_commit(my_drain);
+      __syncwarp();
+      mbar_wait(my_drain, 0, kDrainWaitLimit);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax, O correction, epilogue
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // this thread's row = its TMEM lane
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const float NEG_INF = __int_as_float(0xFF800000);
+    uint32_t g = 0, vq = 0, tails = 0;
+    auto wait_warp = [&](uint64_t* bar, uint32_t parity) {
+      const bool w_ok = __all_sync(0xFFFFFFFFu, pwait(bar, parity, lim, abort_flag));
+      if (!w_ok) flag_timeout(p, abort_flag);
+      return w_ok;
+    };
+    bool ok = true;
+    for (uint32_t ik = 0; ok; ++ik) {
+      const uint32_t is = ik % kItemSlots;
+      if (!(ok = wait_warp(&item_full[is], (ik / kItemSlots) & 1))) break;
+      const Item it = islot[is].it;
+      const bool valid = islot[is].valid != 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[is]);
+      if (!valid) break;
+      const int G = p.group;
+      const bool live = r < it.nrows;
+      const int tok = it.q0 + (it.row0 + r) / G;
+      const int head = it.hk * G + (it.row0 + r) % G;
+      const size_t orow = (size_t)tok * p.hq + head;
+      const size_t li = (size_t)head * p.total_q + tok;
+      if (it.t1 <= it.t0) {
+        // nothing visible: out = 0, lse = -inf
+        if (live) {
+          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * D);
+          for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+          if (p.lse) p.lse[li] = NEG_INF;
+        }
+        continue;
+      }
+      const int n = it.t1 - it.t0;
+      const float kd = load_descale(p.k_descale, p, it);
+      const float vd = load_descale(p.v_descale, p, it);
+      const float scale = p.softmax_scale_log2 * kd * *p.q_descale;
+      // this row's visible keys [lo_r, hi_r]; an empty range for padding rows
+      const int pq = it.Lk - it.Lq + (it.row0 + r) / G;
+      int lo_r = p.window_left >= 0 ? max(0, pq - p.window_left) : 0;
+      int hi_r = p.causal ? min(pq, it.Lk - 1) : it.Lk - 1;
+      if (!live) {
+        lo_r = 1;
+        hi_r = 0;
+      }
+      float m = NEG_INF, l0 = 0.f, l1 = 0.f;
+      for (int u = 0; u < n; ++u, ++g) {
+        const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
+        const uint32_t sb = g & 1;
+        if (!(ok = wait_warp(&s_full[sb], (g >> 1) & 1))) break;
+        tc_fence_after();
+        float x[128];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_load32f(tmem + lane_base + sb * 128 + 32 * q, x + 32 * q);
+        if (!(kb >= lo_r && kb + kTileKeys - 1 <= hi_r)) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (kb + i < lo_r || kb + i > hi_r) x[i] = NEG_INF;
+        }
+        // tile maximum (raw scores; scale > 0)
+        float t[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) t[i] = fmax3(x[4 * i], x[4 * i + 1], fmaxf(x[4 * i + 2], x[4 * i + 3]));
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+        const float ts = t[0] * scale;
+        float alpha = 1.0f;
+        bool resc = false;
+        if (ts > m + C::kTau) {
+          // a row that has seen no key yet has O = 0 and l = 0: nothing to rescale
+          if (m != NEG_INF) {
+            alpha = ex2(m - ts);
+            resc = true;
+          }
+          m = ts;
+        }
+        const float nm = m == NEG_INF ? 0.0f : C::kPShift - m;
+        if (__any_sync(0xFFFFFFFFu, resc)) {
+          l0 *= alpha;
+          l1 *= alpha;
+          // O *= alpha for this warp's rows once PV(g - 1) has accumulated into O
+          if (u > 0 && !(ok = wait_warp(&s_free[(g - 1) & 1], ((g - 1) >> 1) & 1))) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            float o[32];
+            const uint32_t ta = tmem + lane_base + C::kOCol + 32 * q;
+            tmem_load32f(ta, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_store32f(ta, o);
+          }
+        }
+        // P' = 2^(x * scale - m + shift) as an E4M3 pair, 32 keys (8 columns) at a time,
+        // written over the first 64 columns of this S buffer
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int k = 32 * q + 4 * i;
+            const float2 a = __ffma2_rn(make_float2(x[k], x[k + 1]), make_float2(scale, scale), make_float2(nm, nm));
+            const float2 b =
+                __ffma2_rn(make_float2(x[k + 2], x[k + 3]), make_float2(scale, scale), make_float2(nm, nm));
+            const float p0 = ex2(a.x), p1 = ex2(a.y), p2 = ex2(b.x), p3 = ex2(b.y);
+            l0 += p0 + p2;
+            l1 += p1 + p3;
+            uint32_t h01, l01, h23, l23;
+            e4m3_hilo(p0, p1, h01, l01);
+            e4m3_hilo(p2, p3, h23, l23);
+            hi[i] = h01 | (h23 << 16);
+            lo[i] = l01 | (l23 << 16);
+          }
+          tmem_store8(tmem + lane_base + sb * 128 + 8 * q, hi);
+          tmem_store8(tmem + lane_base + sb * 128 + 32 + 8 * q, lo);
+        }
+        tmem_wait_st();
+        // rows of the last page past the sequence end may hold anything (even NaN):
+        // zero those V rows so that 0 * V stays 0 in the PV MMA
+        if (kb + kTileKeys > it.Lk) {
+          if (!(ok = wait_warp(v_ready, tails & 1))) break;
+          ++tails;
+          const int zr = max(0, it.Lk - kb);
+          uint8_t* st = vring + (vq % SV) * C::kVStageBytes;
+          for (int c = 0; c < DC; ++c)
+            for (int x16 = zr * 8 + r; x16 < kTileKeys * 8; x16 += 128)
+              *reinterpret_cast<uint4*>(st + c * kStageBytes + x16 * 16) = make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
+        }
+        ++vq;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);
+      }
+      if (!ok) break;
+      // ---------------- epilogue: O / l, lse
+      if (!(ok = wait_warp(&s_free[(g - 1) & 1], ((g - 1) >> 1) & 1))) break;
+      tc_fence_after();
+      const float l = l0 + l1;
+      const float inv = l > 0.f ? vd / l : 0.f;
+      __nv_bfloat16* orow_ptr = reinterpret_cast<__nv_bfloat16*>(p.out) + orow * D;
+#pragma unroll 1
+      for (int q = 0; q < D / 32; ++q) {
+        float o[32];
+        tmem_load32f(tmem + lane_base + C::kOCol + 32 * q, o);
+        if (live) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(o[2 * i] * inv, o[2 * i + 1] * inv);
+            w[i] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(orow_ptr + 32 * q);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (live && p.lse)
+        p.lse[li] = l > 0.f ? (m - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_attn_prefill(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, int sms, cudaStream_t stream) {
+  using C = PrefillCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_prefill_kernel<D>, dim3(sms), dim3(C::kThreads), (size_t)C::kSmemBytes, stream, p, tm_q,
+                    tm_k, tm_v);
+}
+
+}  // namespace fp8pa

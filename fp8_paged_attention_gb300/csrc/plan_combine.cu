@@ -98,19 +98,47 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
       pp.counts[k] = k < pp.num_classes ? total[k] * pp.hkv : 0;
       pp.counts[2 + k] = 0;  // the attention kernel's dynamic item counter
     }
-  for (int b = b0; b < b1; ++b) {
-    const int Lq = seq_lq(pp, b);
-    const int Lk = clamp_lk(pp.seqused_k[b], pp.max_pages);
-    for (int k = 0; k < pp.num_classes; ++k) {
-      const ClassInfo& c = pp.cls[k];
-      if (!(Lq > 0 && in_class(Lq, c))) continue;
-      const int rts = seq_row_tiles(Lq, pp.group, c.rows);
-      const int ns = seq_splits(Lq, Lk, pp.group, pp.window_left, pp.causal, c);
-      int4* dst = pp.work[k] + (size_t)excl[k] * pp.hkv;
+  // Items of a sequence: (KV head, row tile, split), split fastest.  A thread
+  // writes its own sequences' short lists; a long list (a prefill sequence)
+  // is written by the whole warp, 32 items per round.
+  constexpr int kLongList = 64;
+  for (int j = 0; j < per; ++j) {
+    const int b = b0 + j;
+    int kc = -1, start = 0, rts = 0, ns = 1;
+    if (b < b1) {
+      const int Lq = seq_lq(pp, b);
+      const int Lk = clamp_lk(pp.seqused_k[b], pp.max_pages);
+      for (int k = 0; k < pp.num_classes; ++k) {
+        const ClassInfo& c = pp.cls[k];
+        if (!(Lq > 0 && in_class(Lq, c))) continue;
+        kc = k;
+        rts = seq_row_tiles(Lq, pp.group, c.rows);
+        ns = seq_splits(Lq, Lk, pp.group, pp.window_left, pp.causal, c);
+        start = excl[k];
+        excl[k] += rts * ns;
+        break;
+      }
+    }
+    const int nitems = kc >= 0 ? rts * ns * pp.hkv : 0;
+    if (kc >= 0 && nitems <= kLongList) {
+      int4* dst = pp.work[kc] + (size_t)start * pp.hkv;
       for (int hk = 0; hk < pp.hkv; ++hk)
         for (int rt = 0; rt < rts; ++rt)
           for (int s = 0; s < ns; ++s) *dst++ = make_int4(b, rt, hk | (s << 16), ns);
-      excl[k] += rts * ns;
+    }
+    for (unsigned lm = __ballot_sync(0xFFFFFFFFu, nitems > kLongList); lm; lm &= lm - 1) {
+      const int src = __ffs(lm) - 1;
+      const int sk = __shfl_sync(0xFFFFFFFFu, kc, src);
+      const int sb = __shfl_sync(0xFFFFFFFFu, b, src);
+      const int sstart = __shfl_sync(0xFFFFFFFFu, start, src);
+      const int srts = __shfl_sync(0xFFFFFFFFu, rts, src);
+      const int sns = __shfl_sync(0xFFFFFFFFu, ns, src);
+      const int per_head = srts * sns;
+      int4* dst = pp.work[sk] + (size_t)sstart * pp.hkv;
+      for (int i = lane; i < per_head * pp.hkv; i += 32) {
+        const int hk = i / per_head, rem = i - hk * per_head;
+        dst[i] = make_int4(sb, rem / sns, hk | ((rem % sns) << 16), sns);
+      }
     }
   }
 }

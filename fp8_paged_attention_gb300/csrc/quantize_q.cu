@@ -24,7 +24,6 @@ __device__ __forceinline__ uint8_t quant_one(uint16_t bits, float d) {
 // 8 elements per thread when both pointers allow 16-byte / 8-byte accesses.
 __global__ void quantize_q_vec8(const uint4* __restrict__ q, uint2* __restrict__ out, const float* __restrict__ qd,
                                 long long n8) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
   const float d = *qd;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
@@ -38,16 +37,20 @@ __global__ void quantize_q_vec8(const uint4* __restrict__ q, uint2* __restrict__
     }
     out[i] = make_uint2(o[0], o[1]);
   }
+  // Let the next kernel (the forward's plan) launch only as this grid drains:
+  // launched earlier, the attention grid behind it would take SM room from the
+  // blocks still quantizing.
+  ptx::griddep_launch_dependents();
 }
 
 __global__ void quantize_q_scalar(const uint16_t* __restrict__ q, uint8_t* __restrict__ out,
                                   const float* __restrict__ qd, long long begin, long long n) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
   const float d = *qd;
   for (long long i = begin + blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)
     out[i] = quant_one(q[i], d);
+  ptx::griddep_launch_dependents();
 }
 
 }  // namespace
