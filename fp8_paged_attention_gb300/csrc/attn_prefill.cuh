@@ -29,6 +29,41 @@
 
 namespace fp8pa {
 
+namespace detail {
+
+// P' pair from its exponent pair: 2^t with t rounded to f16 first (ex2 on f16x2).
+__device__ __forceinline__ uint32_t ex2_f16x2(float t0, float t1) {
+  uint32_t h, e;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(t1), "f"(t0));
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
+  return e;
+}
+
+// f16x2 P' -> E4M3 pair hi = e4m3(P'), lo = e4m3(P' - hi) (exact in f16), 16 bits each.
+__device__ __forceinline__ void e4m3_hilo_f16x2(uint32_t h, uint32_t& hi, uint32_t& lo) {
+  uint32_t hh, l;
+  uint16_t h8, l8;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h8) : "r"(h));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(h8));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(l) : "r"(h), "r"(hh));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l8) : "r"(l));
+  hi = h8;
+  lo = l8;
+}
+
+__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ float2 f16x2_to_f32(uint32_t h) {
+  __half2 v = *reinterpret_cast<__half2*>(&h);
+  return __half22float2(v);
+}
+
+}  // namespace detail
+
 template <int D>
 struct PrefillCfg {
   static_assert(D == 256, "tensor memory holds two 128-column S buffers and O only for D = 256");
@@ -42,8 +77,9 @@ struct PrefillCfg {
   static constexpr int kVStages = 3;
   static constexpr int kThreads = 7 * 32;
   static constexpr int kCtrlBytes = 2048;
-  static constexpr int kSmemBytes =
-      kQBufs * kQBytes + kKStages * kKStageBytes + kVStages * kVStageBytes + kCtrlBytes + 1024;
+  static constexpr int kOStageBytes = 4 * 32 * 64;  // epilogue: 32 rows x 64 bytes per softmax warp
+  static constexpr int kSmemBytes = kQBufs * kQBytes + kKStages * kKStageBytes + kVStages * kVStageBytes +
+                                    kOStageBytes + kCtrlBytes + 1024;
   static_assert(kSmemBytes <= 232448, "smem");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kOCol = 256;  // O columns [256, 256 + D)
@@ -67,7 +103,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   uint8_t* vring = smem;
   uint8_t* kring = vring + SV * C::kVStageBytes;
   uint8_t* qbuf = kring + SK * C::kKStageBytes;
-  uint8_t* ctrl = qbuf + QB * C::kQBytes;
+  uint8_t* ostage = qbuf + QB * C::kQBytes;
+  uint8_t* ctrl = ostage + C::kOStageBytes;
   uint64_t* k_full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* k_empty = k_full + SK;
   uint64_t* v_full = k_empty + SK;
@@ -395,21 +432,25 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t hi[8], lo[8];
+          uint32_t sa = 0, sb2 = 0;  // f16x2 partial row sums of these 32 keys (each <= 16 x 256)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int k = 32 * q + 4 * i;
             const float2 a = __ffma2_rn(make_float2(x[k], x[k + 1]), make_float2(scale, scale), make_float2(nm, nm));
             const float2 b =
                 __ffma2_rn(make_float2(x[k + 2], x[k + 3]), make_float2(scale, scale), make_float2(nm, nm));
-            const float p0 = ex2(a.x), p1 = ex2(a.y), p2 = ex2(b.x), p3 = ex2(b.y);
-            l0 += p0 + p2;
-            l1 += p1 + p3;
-            uint32_t h01, l01, h23, l23;
-            e4m3_hilo(p0, p1, h01, l01);
-            e4m3_hilo(p2, p3, h23, l23);
-            hi[i] = h01 | (h23 << 16);
-            lo[i] = l01 | (l23 << 16);
+            const uint32_t h01 = ex2_f16x2(a.x, a.y), h23 = ex2_f16x2(b.x, b.y);
+            sa = hadd2(sa, h01);
+            sb2 = hadd2(sb2, h23);
+            uint32_t e01, f01, e23, f23;
+            e4m3_hilo_f16x2(h01, e01, f01);
+            e4m3_hilo_f16x2(h23, e23, f23);
+            hi[i] = e01 | (e23 << 16);
+            lo[i] = f01 | (f23 << 16);
           }
+          const float2 fa = f16x2_to_f32(sa), fb = f16x2_to_f32(sb2);
+          l0 += fa.x + fb.x;
+          l1 += fa.y + fb.y;
           tmem_store8(tmem + lane_base + sb * 128 + 8 * q, hi);
           tmem_store8(tmem + lane_base + sb * 128 + 32 + 8 * q, lo);
         }
@@ -437,22 +478,42 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       tc_fence_after();
       const float l = l0 + l1;
       const float inv = l > 0.f ? vd / l : 0.f;
-      __nv_bfloat16* orow_ptr = reinterpret_cast<__nv_bfloat16*>(p.out) + orow * D;
+      // Each 32-column chunk of this warp's 32 rows goes through a 2 KB staging
+      // buffer (row-major, 16-byte pieces swizzled by (row >> 1) & 3), then out as
+      // 64-byte row segments: lane l stores piece l & 3 of row i * 8 + l / 4.
+      uint8_t* stg = ostage + quarter * 2048;
+      __nv_bfloat16* dst_row[4];
+      bool dst_live[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = quarter * 32 + i * 8 + (lane >> 2);
+        dst_live[i] = rr < it.nrows;
+        const size_t row = (size_t)(it.q0 + (it.row0 + rr) / G) * p.hq + it.hk * G + (it.row0 + rr) % G;
+        dst_row[i] = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + (lane & 3) * 8;
+      }
 #pragma unroll 1
       for (int q = 0; q < D / 32; ++q) {
         float o[32];
         tmem_load32f(tmem + lane_base + C::kOCol + 32 * q, o);
-        if (live) {
-          uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(o[2 * i] * inv, o[2 * i + 1] * inv);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(o[8 * c + 2 * i] * inv, o[8 * c + 2 * i + 1] * inv);
             w[i] = *reinterpret_cast<uint32_t*>(&b2);
           }
-          uint4* dst = reinterpret_cast<uint4*>(orow_ptr + 32 * q);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = i * 8 + (lane >> 2), c = lane & 3;
+          const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4));
+          if (dst_live[i]) *reinterpret_cast<uint4*>(dst_row[i] + 32 * q) = v;
+        }
+        __syncwarp();
       }
       if (live && p.lse)
         p.lse[li] = l > 0.f ? (m - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
