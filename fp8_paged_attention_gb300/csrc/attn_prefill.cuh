@@ -418,13 +418,17 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           if (u > 0 && !(ok = wait_warp(&s_free[(g - 1) & 1], ((g - 1) >> 1) & 1))) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int q = 0; q < D / 32; ++q) {
-            float o[32];
-            const uint32_t ta = tmem + lane_base + C::kOCol + 32 * q;
-            tmem_load32f(ta, o);
+          for (int q = 0; q < D / 64; ++q) {
+            float o[64];
+            const uint32_t ta = tmem + lane_base + C::kOCol + 64 * q;
+            tmem_load64f(ta, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_store32f(ta, o);
+            for (int i = 0; i < 64; i += 2) {
+              const float2 v = __fmul2_rn(make_float2(o[i], o[i + 1]), make_float2(alpha, alpha));
+              o[i] = v.x;
+              o[i + 1] = v.y;
+            }
+            tmem_store64f(ta, o);
           }
         }
         // P' = 2^(x * scale - m + shift) as an E4M3 pair, 32 keys (8 columns) at a time,
@@ -492,28 +496,33 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         dst_row[i] = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + (lane & 3) * 8;
       }
 #pragma unroll 1
-      for (int q = 0; q < D / 32; ++q) {
-        float o[32];
-        tmem_load32f(tmem + lane_base + C::kOCol + 32 * q, o);
+      for (int q2 = 0; q2 < D / 64; ++q2) {
+        float o[64];
+        tmem_load64f(tmem + lane_base + C::kOCol + 64 * q2, o);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t w[4];
+        for (int h = 0; h < 2; ++h) {
+          const int q = 2 * q2 + h;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              __nv_bfloat162 b2 =
+                  __floats2bfloat162_rn(o[32 * h + 8 * c + 2 * i] * inv, o[32 * h + 8 * c + 2 * i + 1] * inv);
+              w[i] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          __syncwarp();
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(o[8 * c + 2 * i] * inv, o[8 * c + 2 * i + 1] * inv);
-            w[i] = *reinterpret_cast<uint32_t*>(&b2);
+            const int rr = i * 8 + (lane >> 2), c = lane & 3;
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4));
+            if (dst_live[i]) *reinterpret_cast<uint4*>(dst_row[i] + 32 * q) = v;
           }
-          *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+          __syncwarp();
         }
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int rr = i * 8 + (lane >> 2), c = lane & 3;
-          const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4));
-          if (dst_live[i]) *reinterpret_cast<uint4*>(dst_row[i] + 32 * q) = v;
-        }
-        __syncwarp();
       }
       if (live && p.lse)
         p.lse[li] = l > 0.f ? (m - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;

@@ -220,6 +220,31 @@ __device__ __forceinline__ void tmem_store32f(uint32_t taddr, const float* x) {
       "f"(x[25]), "f"(x[26]), "f"(x[27]), "f"(x[28]), "f"(x[29]), "f"(x[30]), "f"(x[31])
       : "memory");
 }
+__device__ __forceinline__ void tmem_load64f(uint32_t taddr, float* x) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : FP8PA_F8(0), FP8PA_F8(8), FP8PA_F8(16), FP8PA_F8(24), FP8PA_F8(32), FP8PA_F8(40), FP8PA_F8(48),
+        FP8PA_F8(56)
+      : "r"(taddr)
+      : "memory");
+}
+#define FP8PA_FI8(o) "f"(x[o + 0]), "f"(x[o + 1]), "f"(x[o + 2]), "f"(x[o + 3]), \
+                     "f"(x[o + 4]), "f"(x[o + 5]), "f"(x[o + 6]), "f"(x[o + 7])
+__device__ __forceinline__ void tmem_store64f(uint32_t taddr, const float* x) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,"
+      "%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
+      "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      FP8PA_FI8(0), FP8PA_FI8(8), FP8PA_FI8(16), FP8PA_FI8(24), FP8PA_FI8(32), FP8PA_FI8(40), FP8PA_FI8(48),
+      FP8PA_FI8(56)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_store16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
