@@ -67,6 +67,11 @@ CASES = [
     ("noncausal_window_hd256", [3, 70], [200, 70], 4, 2, 256, 50, False, True),
     ("noncausal_hd512_bf16", [2, 40], [300, 40], 8, 1, 512, -1, False, False),
     ("mha_group1_hd256", [5, 1], [77, 300], 2, 2, 256, -1, True, True),
+    # prefill-class tiles (128 packed rows at hd256): rows and whole sequences with no visible key,
+    # one and eight query heads per KV head
+    ("prefill_empty_rows_hd256", [20, 12, 30], [10, 0, 30], 4, 2, 256, -1, True, True),
+    ("prefill_group1_hd256", [40, 130], [40, 200], 2, 2, 256, -1, True, True),
+    ("prefill_group8_window_hd256", [20, 50], [100, 50], 16, 2, 256, 30, True, True),
     ("group16_hd512", [1, 2], [500, 130], 16, 1, 512, -1, True, False),
 ]
 
@@ -180,6 +185,43 @@ def test_wait_that_runs_out_sets_timeout_and_context_survives(fp8, limit):
     out, lse = run_gpu(w)
     check(w, out, lse)
     assert fp8pa.get_device_status() == 0
+
+
+def test_per_batch_head_descales_prefill_tiles():
+    w = make("descale_pf", [40, 70], [200, 70], 8, 2, 256, -1, True, True, seed=13)
+    kd = torch.tensor([[w.k_descale, w.k_descale * 0.5], [w.k_descale * 2, w.k_descale]], dtype=torch.float32,
+                      device="cuda")
+    vd = torch.tensor([[w.v_descale * 3, w.v_descale], [w.v_descale, w.v_descale * 0.25]], dtype=torch.float32,
+                      device="cuda")
+    out, lse = run_gpu(w, k_descale=kd.reshape(-1), v_descale=vd.reshape(-1), descale_batch_stride=2,
+                       descale_head_stride=1)
+    prob = oracle_problem(w, k_descale=kd.cpu().numpy().ravel(), v_descale=vd.cpu().numpy().ravel(),
+                          descale_batch_stride=2, descale_head_stride=1)
+    ro, rl = oracle.paged_attention(prob)
+    g = out.float().cpu().numpy()
+    tok_seq = np.repeat(np.arange(2), w.lq)
+    G = 4
+    for t in range(w.total_q):
+        for h in range(8):
+            s = w.v_channel_scale[h // G] * float(vd[tok_seq[t], h // G] / w.v_descale)
+            assert np.max(np.abs(g[t, h] - ro[t, h]) / np.maximum(s, np.abs(ro[t, h]))) <= TOL[True][0]
+    assert lse_error(lse.cpu().numpy(), rl) <= LSE_GATE
+
+
+def test_bad_page_id_in_prefill_tiles_sets_status():
+    import fp8_paged_attention_gb300 as fp8pa
+    w = make("badpage_pf", [40, 50], [200, 300], 4, 2, 256, -1, True, True, seed=6)
+    bt = w.block_table.clone()
+    bt[1, 1] = 1 << 20
+    fp8pa.reset_device_status()
+    out, lse = run_gpu(synth.Workload(**{**w.__dict__, "block_table": bt}))
+    assert fp8pa.get_device_status() & fp8pa.DEV_BAD_PAGE
+    assert torch.isfinite(out.float()).all()
+    # sequence 0 does not reference the bad entry
+    ro, rl = oracle.paged_attention(oracle_problem(w))
+    e = unit_scale_errors(out.float().cpu().numpy()[:40], ro[:40], w)
+    assert e["max"] <= TOL[True][0]
+    fp8pa.reset_device_status()
 
 
 def test_bad_page_id_sets_status_and_reads_zeros():
