@@ -25,6 +25,7 @@ SOURCES = [
     "quantize_q.cu",
     "attn_fp8_d256.cu",
     "attn_prefill_d256.cu",
+    "attn_prefill_d512.cu",
     "attn_fp8_d512.cu",
     "attn_bf16_d512.cu",
     "attn_bf16dqv_d512.cu",

@@ -207,8 +207,9 @@ int make_plan(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int hea
                 "q dtype bfloat16 with k/v dtype float8_e4m3fn at head_size 256 is not supported "
                 "(head_size 256 takes E4M3 Q; quantize it with quantize_q_fp8)");
   pl.fp8_q = q_dtype == FP8PA_E4M3;
-  // prefill-class tiles at head dim 256 (E4M3 Q) run the rows-on-lanes kernel with 128 rows
-  pl.prefill_kernel = head_dim == 256 && pl.fp8_q;
+  // prefill-class tiles with E4M3 Q run the rows-on-lanes kernel with 128 rows (at head
+  // dim 512 as two work items per row tile, one per 256-wide slice of the output dims)
+  pl.prefill_kernel = pl.fp8_q;
   const int prefill_rows = pl.prefill_kernel ? 128 : 64;
   const int g = hq / hkv;
   pl.group = g;
@@ -236,10 +237,11 @@ int make_plan(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int hea
               : pl.num_classes > 1 ? 1
                                    : auto_splits(batch, hkv, max_pages, window_left, lq0_max, device_sms());
   pl.cls[0].max_splits = pl.splits;
+  pl.cls[1].dhalves = pl.prefill_kernel && head_dim == 512 ? 2 : 1;
   // workspace layout: [counts][class-0 items][class-1 items][o_part][lse_part]
   pl.items_max[0] = (size_t)hkv * batch * pl.splits;
   pl.items_max[1] =
-      pl.num_classes > 1 ? (size_t)hkv * ((size_t)((long long)total_q * g + 63) / 64 + (size_t)batch) : 0;
+      pl.num_classes > 1 ? (size_t)hkv * ((size_t)((long long)total_q * g + 63) / 64 + 2 * (size_t)batch) : 0;
   size_t off = 256;
   for (int k = 0; k < 2; ++k) {
     pl.off_work[k] = off;
@@ -440,7 +442,8 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
     p.work_next = counts + 2 + k;
     const int path = kernel_path(fp8_q);
     if (k == 1 && pl.prefill_kernel)
-      e = launch_attn_prefill_d256(p, tm_q[k], tm_k, tm_v, sms, st);
+      e = head_dim == 256 ? launch_attn_prefill_d256(p, tm_q[k], tm_k, tm_v, sms, st)
+                          : launch_attn_prefill_d512(p, tm_q[k], tm_k, tm_v, sms, st);
     else
       e = launch_attn(head_dim, path, pl.cls[k].rows, ctas_per_sm(head_dim, path, pl.cls[k].rows), p, tm_q[k], tm_k,
                       tm_v, sms, st);

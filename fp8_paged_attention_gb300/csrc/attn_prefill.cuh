@@ -1,5 +1,5 @@
 // Paged FP8-KV attention forward for prefill row tiles, sm_103a: E4M3 Q, K and
-// V at head dim 256, 128 packed query rows per tile.
+// V at head dim 256 or 512, 128 packed query rows per tile.
 //
 // The decode kernel puts keys on the TMEM lanes (swap-AB) so that a handful of
 // query rows still fills an MMA.  A prefill tile has rows to spare, so here the
@@ -17,7 +17,10 @@
 //
 // Tensor memory (512 columns): two S buffers of 128 columns; P's hi and lo
 // terms (32 columns each, four keys per column) overwrite the first 64 columns
-// of their S buffer once the row's scores are in registers; O takes D columns.
+// of their S buffer once the row's scores are in registers; O takes 256
+// columns.  At head dim 512 the output dims come in two slices of 256, each a
+// work item of its own: both compute the full S and P, each accumulates O for
+// its slice against that slice of V.
 //
 // Warps: 0 TMA producer, 1 QK^T issuer (and TMEM owner), 2 PV issuer, 3-6
 // softmax / O correction / epilogue (thread = row).  The producer and the
@@ -66,15 +69,18 @@ __device__ __forceinline__ float2 f16x2_to_f32(uint32_t h) {
 
 template <int D>
 struct PrefillCfg {
-  static_assert(D == 256, "tensor memory holds two 128-column S buffers and O only for D = 256");
+  static_assert(D == 256 || D == 512, "head dim");
   static constexpr int kRows = 128;
-  static constexpr int kDC = D / 128;                     // 128-byte chunks of an E4M3 row
+  static constexpr int kDC = D / 128;                     // 128-byte chunks of an E4M3 row (Q, K)
+  static constexpr int kDO = 256;                         // output dims per work item
+  static constexpr int kSlices = D / kDO;                 // work items per row tile
+  static constexpr int kVC = kDO / 128;                   // V chunks per work item and tile
   static constexpr int kQBytes = kDC * kRows * 128;       // chunk c of every row at c * 16 KB
-  static constexpr int kQBufs = 2;
+  static constexpr int kQBufs = D == 256 ? 2 : 1;
   static constexpr int kKStageBytes = kStageBytes;        // 128 keys x one 128-byte chunk
-  static constexpr int kVStageBytes = kDC * kStageBytes;  // 128 keys x D bytes, chunk c at c * 16 KB
-  static constexpr int kKStages = 3;
-  static constexpr int kVStages = 3;
+  static constexpr int kVStageBytes = kVC * kStageBytes;  // 128 keys x kDO bytes, chunk c at c * 16 KB
+  static constexpr int kKStages = D == 256 ? 3 : 5;
+  static constexpr int kVStages = D == 256 ? 3 : 2;
   static constexpr int kThreads = 7 * 32;
   static constexpr int kCtrlBytes = 2048;
   static constexpr int kOStageBytes = 4 * 32 * 64;  // epilogue: 32 rows x 64 bytes per softmax warp
@@ -82,8 +88,8 @@ struct PrefillCfg {
                                     kOStageBytes + kCtrlBytes + 1024;
   static_assert(kSmemBytes <= 232448, "smem");
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kOCol = 256;  // O columns [256, 256 + D)
-  static_assert(kOCol + D <= 512, "TMEM");
+  static constexpr int kOCol = 256;  // O columns [256, 256 + kDO)
+  static_assert(kOCol + kDO <= 512, "TMEM");
   static constexpr float kTau = 4.0f;
   static constexpr float kPShift = 4.0f;
 };
@@ -95,7 +101,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   using C = PrefillCfg<D>;
   using namespace ptx;
   using namespace detail;
-  constexpr int DC = C::kDC, SK = C::kKStages, SV = C::kVStages, QB = C::kQBufs;
+  constexpr int DC = C::kDC, SK = C::kKStages, SV = C::kVStages, QB = C::kQBufs, VC = C::kVC, DO = C::kDO;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   // V ring lowest: its MMA operand spans two 16 KB blocks of a stage, and every
@@ -242,9 +248,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           if (leader) {
             uint8_t* dst = vring + slot * C::kVStageBytes;
             mbar_arrive_expect_tx(&v_full[slot], C::kVStageBytes);
-            for (int c = 0; c < DC; ++c) {
-              tma_load_4d(dst + c * kStageBytes, &tm_v, &v_full[slot], c * 128, it.hk, 0, pa);
-              tma_load_4d(dst + c * kStageBytes + kStageBytes / 2, &tm_v, &v_full[slot], c * 128, it.hk, 0, pb);
+            for (int c = 0; c < VC; ++c) {
+              const int cv = (it.dhalf * VC + c) * 128;  // this item's slice of the head dims
+              tma_load_4d(dst + c * kStageBytes, &tm_v, &v_full[slot], cv, it.hk, 0, pa);
+              tma_load_4d(dst + c * kStageBytes + kStageBytes / 2, &tm_v, &v_full[slot], cv, it.hk, 0, pb);
             }
           }
           ++vq;
@@ -283,8 +290,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         }
         if (ok && leader) mma_commit(&q_empty[qb]);
       } else {
-        // O += P(g) . V(g): A = P hi and lo terms from TMEM, B = V (MN-major, N = D)
-        constexpr uint32_t idesc = make_idesc(kFmtE4M3, kKMajor, kMNMajor, 128, D);
+        // O += P(g) . V(g): A = P hi and lo terms from TMEM, B = V slice (MN-major, N = kDO)
+        constexpr uint32_t idesc = make_idesc(kFmtE4M3, kKMajor, kMNMajor, 128, DO);
         for (int u = 0; u < n && ok; ++u) {
           const uint32_t gg = g + u, sb = gg & 1;
           const uint32_t slot = vq % SV, vpar = (vq / SV) & 1;
@@ -359,9 +366,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       if (it.t1 <= it.t0) {
         // nothing visible: out = 0, lse = -inf
         if (live) {
-          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * D);
-          for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
-          if (p.lse) p.lse[li] = NEG_INF;
+          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * D + it.dhalf * DO);
+          for (int i = 0; i < DO / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+          if (p.lse && it.dhalf == 0) p.lse[li] = NEG_INF;
         }
         continue;
       }
@@ -418,7 +425,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           if (u > 0 && !(ok = wait_warp(&s_free[(g - 1) & 1], ((g - 1) >> 1) & 1))) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int q = 0; q < D / 64; ++q) {
+          for (int q = 0; q < DO / 64; ++q) {
             float o[64];
             const uint32_t ta = tmem + lane_base + C::kOCol + 64 * q;
             tmem_load64f(ta, o);
@@ -466,7 +473,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           ++tails;
           const int zr = max(0, it.Lk - kb);
           uint8_t* st = vring + (vq % SV) * C::kVStageBytes;
-          for (int c = 0; c < DC; ++c)
+          for (int c = 0; c < VC; ++c)
             for (int x16 = zr * 8 + r; x16 < kTileKeys * 8; x16 += 128)
               *reinterpret_cast<uint4*>(st + c * kStageBytes + x16 * 16) = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
@@ -493,10 +500,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         const int rr = quarter * 32 + i * 8 + (lane >> 2);
         dst_live[i] = rr < it.nrows;
         const size_t row = (size_t)(it.q0 + (it.row0 + rr) / G) * p.hq + it.hk * G + (it.row0 + rr) % G;
-        dst_row[i] = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + (lane & 3) * 8;
+        dst_row[i] = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + it.dhalf * DO + (lane & 3) * 8;
       }
 #pragma unroll 1
-      for (int q2 = 0; q2 < D / 64; ++q2) {
+      for (int q2 = 0; q2 < DO / 64; ++q2) {
         float o[64];
         tmem_load64f(tmem + lane_base + C::kOCol + 64 * q2, o);
 #pragma unroll
@@ -524,7 +531,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           __syncwarp();
         }
       }
-      if (live && p.lse)
+      if (live && p.lse && it.dhalf == 0)
         p.lse[li] = l > 0.f ? (m - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
       tc_fence_before();
       __syncwarp();

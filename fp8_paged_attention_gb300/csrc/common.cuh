@@ -24,7 +24,13 @@ struct ClassInfo {
   int lq_min, lq_max;
   int rows;        // N: rows per tile (multiple of 16)
   int max_splits;  // split-KV count cap for single-row-tile sequences
+  int dhalves;     // > 1: each row tile is dhalves work items, one per slice of the output dims
 };
+
+// Work items per (sequence, KV head, row tile): output-dim slices, else key splits.
+__host__ __device__ __forceinline__ int unit_items(int split_count, const ClassInfo& c) {
+  return c.dhalves > 1 ? c.dhalves : split_count;
+}
 
 struct AttnParams {
   // problem
@@ -89,6 +95,7 @@ struct Item {
   int t0, t1;            // 128-key tiles [t0, t1) of this split; tile t starts at key (pg_lo + 2t) * 64
   int lo_max, hi_min;    // keys in [lo_max, hi_min] are visible to every valid row
   int hi_max;            // last key visible to any row (for tail sanitation)
+  int dhalf;             // slice of the output dims this item computes (classes with dhalves > 1)
 };
 
 // Work item encoding: {b, row_tile, hk | split << 16, nsplit}.
@@ -99,6 +106,12 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int4 w) {
   it.hk = w.z & 0xFFFF;
   it.split = w.z >> 16;
   it.nsplit = w.w;
+  it.dhalf = 0;
+  if (p.cls.dhalves > 1) {  // the item index selects an output-dim slice; every key is visible to it
+    it.dhalf = it.split;
+    it.split = 0;
+    it.nsplit = 1;
+  }
   it.q0 = p.cu_seqlens_q[it.b];
   it.Lq = p.cu_seqlens_q[it.b + 1] - it.q0;
   int lk = p.seqused_k[it.b];

@@ -60,9 +60,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
-// Prefill row tiles (128 packed rows, rows on the TMEM lanes), E4M3 Q at head dim 256:
-// one persistent CTA per SM.
+// Prefill row tiles (128 packed rows, rows on the TMEM lanes), E4M3 Q at head dim 256
+// or 512 (the latter with two output-dim slices per row tile): one persistent CTA per SM.
 cudaError_t launch_attn_prefill_d256(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                     const CUtensorMap& tm_v, int sms, cudaStream_t stream);
+cudaError_t launch_attn_prefill_d512(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                      const CUtensorMap& tm_v, int sms, cudaStream_t stream);
 
 // Records a message for fp8pa_last_error() on this thread; returns `code`.

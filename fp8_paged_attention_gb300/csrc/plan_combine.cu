@@ -56,7 +56,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
     for (int k = 0; k < pp.num_classes; ++k) {
       const ClassInfo& c = pp.cls[k];
       if (Lq > 0 && in_class(Lq, c))
-        cnt[k] += seq_row_tiles(Lq, pp.group, c.rows) * seq_splits(Lq, Lk, pp.group, pp.window_left, pp.causal, c);
+        cnt[k] += seq_row_tiles(Lq, pp.group, c.rows) *
+                  unit_items(seq_splits(Lq, Lk, pp.group, pp.window_left, pp.causal, c), c);
     }
   }
   // exclusive prefix sums of the per-thread counts: within each warp, then over the warp totals
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
         if (!(Lq > 0 && in_class(Lq, c))) continue;
         kc = k;
         rts = seq_row_tiles(Lq, pp.group, c.rows);
-        ns = seq_splits(Lq, Lk, pp.group, pp.window_left, pp.causal, c);
+        ns = unit_items(seq_splits(Lq, Lk, pp.group, pp.window_left, pp.causal, c), c);
         start = excl[k];
         excl[k] += rts * ns;
         break;

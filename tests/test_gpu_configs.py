@@ -53,7 +53,8 @@ def sampled_check(w, out, lse, n_seq=12, chunk_tokens=48, seed=0):
 
 
 @pytest.mark.parametrize("name", ["swa_decode_hd256", "full_decode_hd512_bf16q", "full_decode_hd512_fp8q",
-                                  "spec_verify_hd512", "mixed_hd256_swa", "mixed_hd512_causal"])
+                                  "spec_verify_hd512", "mixed_hd256_swa", "mixed_hd512_causal",
+                                  "mixed_hd512_causal_fp8q"])
 def test_full_size_config_sampled(name):
     w = synth.make_config(name, device="cuda")
     out, lse = run_gpu(w)
