@@ -208,6 +208,19 @@ def test_per_batch_head_descales_prefill_tiles():
     assert lse_error(lse.cpu().numpy(), rl) <= LSE_GATE
 
 
+@pytest.mark.parametrize("d,sharp", [(256, 8.0), (256, 0.1), (512, 8.0), (512, 0.1)],
+                         ids=["hd256_sharp", "hd256_flat", "hd512_sharp", "hd512_flat"])
+def test_prefill_tiles_sharp_and_flat_softmax(d, sharp):
+    """Prefill tiles under a sharp softmax (scores scaled by 8: a few keys carry
+    each row's mass, where P's E4M3 rounding matters most) and a flat one
+    (scaled by 0.1: every weight small).  Both match the oracle."""
+    hq = 8 if d == 256 else 16
+    w = make("sharp", [70, 130], [300, 130], hq, 2, d, -1, True, True, seed=41)
+    w = synth.Workload(**{**w.__dict__, "softmax_scale": w.softmax_scale * sharp})
+    out, lse = run_gpu(w)
+    check(w, out, lse)
+
+
 def test_bad_page_id_in_prefill_tiles_sets_status():
     import fp8_paged_attention_gb300 as fp8pa
     w = make("badpage_pf", [40, 50], [200, 300], 4, 2, 256, -1, True, True, seed=6)
