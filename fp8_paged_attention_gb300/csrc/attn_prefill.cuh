@@ -22,10 +22,11 @@
 // work item of its own: both compute the full S and P, each accumulates O for
 // its slice against that slice of V.
 //
-// Warps: 0 TMA producer, 1 QK^T issuer (and TMEM owner), 2 PV issuer, 3-6
-// softmax / O correction / epilogue (thread = row).  The producer and the
-// issuers run warp-uniform loops with one elected lane issuing; the softmax
-// warps synchronize with the issuers only through mbarriers.
+// Warps: 0 TMA producer, 1 QK^T issuer (and TMEM owner), 2 PV issuer, 3-10
+// softmax / O correction / epilogue in two warpgroups (a pair of warps per row
+// quarter, each thread half of a row's keys and output dims).  The producer and
+// the issuers run warp-uniform loops with one elected lane issuing; they and the
+// softmax warps synchronize only through mbarriers.
 #pragma once
 #include "attn_kernel.cuh"
 #include "kernels.h"
@@ -79,13 +80,14 @@ struct PrefillCfg {
   static constexpr int kQBufs = D == 256 ? 2 : 1;
   static constexpr int kKStageBytes = kStageBytes;        // 128 keys x one 128-byte chunk
   static constexpr int kVStageBytes = kVC * kStageBytes;  // 128 keys x kDO bytes, chunk c at c * 16 KB
-  static constexpr int kKStages = D == 256 ? 3 : 5;
-  static constexpr int kVStages = D == 256 ? 3 : 2;
-  static constexpr int kThreads = 7 * 32;
-  static constexpr int kCtrlBytes = 2048;
-  static constexpr int kOStageBytes = 4 * 32 * 64;  // epilogue: 32 rows x 64 bytes per softmax warp
+  static constexpr int kKStages = D == 256 ? 3 : 4;
+  static constexpr int kVStages = 2;
+  static constexpr int kThreads = 11 * 32;  // producer, 2 issuers, 2 softmax warpgroups
+  static constexpr int kCtrlBytes = 1024;
+  static constexpr int kXchgBytes = 3 * 1024;       // pair exchange: half maxima [2][2][128], row sums [2][128]
+  static constexpr int kOStageBytes = 8 * 32 * 64;  // epilogue: 32 rows x 64 bytes per softmax warp
   static constexpr int kSmemBytes = kQBufs * kQBytes + kKStages * kKStageBytes + kVStages * kVStageBytes +
-                                    kOStageBytes + kCtrlBytes + 1024;
+                                    kOStageBytes + kXchgBytes + kCtrlBytes + 1024;
   static_assert(kSmemBytes <= 232448, "smem");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kOCol = 256;  // O columns [256, 256 + kDO)
@@ -110,7 +112,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   uint8_t* kring = vring + SV * C::kVStageBytes;
   uint8_t* qbuf = kring + SK * C::kKStageBytes;
   uint8_t* ostage = qbuf + QB * C::kQBytes;
-  uint8_t* ctrl = ostage + C::kOStageBytes;
+  uint8_t* xchg = ostage + C::kOStageBytes;
+  uint8_t* ctrl = xchg + C::kXchgBytes;
   uint64_t* k_full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* k_empty = k_full + SK;
   uint64_t* v_full = k_empty + SK;
@@ -119,8 +122,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   uint64_t* q_empty = q_full + QB;
   uint64_t* s_full = q_empty + QB;  // [2] QK^T done: S buffer readable
   uint64_t* s_free = s_full + 2;    // [2] PV done: S/P buffer reusable, O up to date
-  uint64_t* p_full = s_free + 2;    // [2] P written (four softmax warps)
-  uint64_t* o_empty = p_full + 2;   // epilogue read O (four softmax warps)
+  uint64_t* p_full = s_free + 2;    // [2] P written (eight softmax warps)
+  uint64_t* o_empty = p_full + 2;   // epilogue read O (eight softmax warps)
   uint64_t* v_ready = o_empty + 1;  // tail tile: its V stage landed (PV issuer -> softmax)
   uint64_t* drain = v_ready + 1;    // [2] one per issuer
   uint64_t* never = drain + 2;      // nothing arrives on it: the stall-injection hook waits here
@@ -147,15 +150,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 1);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&p_full[i], 8);
       mbar_init(&drain[i], 1);
     }
-    mbar_init(o_empty, 4);
+    mbar_init(o_empty, 8);
     mbar_init(v_ready, 1);
     mbar_init(never, 1);
     for (int i = 0; i < kItemSlots; ++i) {
       mbar_init(&item_full[i], 1);
-      mbar_init(&item_empty[i], 2 + 4);  // two issuers, four softmax warps
+      mbar_init(&item_empty[i], 2 + 8);  // two issuers, eight softmax warps
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -338,20 +341,33 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- softmax, O correction, epilogue
+    // Two warpgroups.  The warp pair of lane quarter q (one warp per group) owns
+    // rows 32q .. 32q + 31; warpgroup hw takes keys [64 hw, 64 hw + 64) of every
+    // tile and output dims [hw * kDO / 2, (hw + 1) * kDO / 2).  A pair exchanges
+    // its half-tile maxima (and finally its row sums) through shared memory on
+    // named barrier 1 + q, and every early exit is a vote on that barrier, so the
+    // two warps of a pair always leave together.
+    const int hw = (warp - 3) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // this thread's row = its TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t pair_bar = 1 + quarter;
     const float NEG_INF = __int_as_float(0xFF800000);
+    constexpr int HO = DO / 2;  // output dims per warpgroup
+    float* xmax = reinterpret_cast<float*>(xchg);  // [2][2][128] half-tile maxima, by tile parity
+    float* lsum = xmax + 512;                      // [2][128] half row sums
     uint32_t g = 0, vq = 0, tails = 0;
-    auto wait_warp = [&](uint64_t* bar, uint32_t parity) {
+    auto wait_w = [&](uint64_t* bar, uint32_t parity) {
       const bool w_ok = __all_sync(0xFFFFFFFFu, pwait(bar, parity, lim, abort_flag));
       if (!w_ok) flag_timeout(p, abort_flag);
       return w_ok;
     };
-    bool ok = true;
-    for (uint32_t ik = 0; ok; ++ik) {
+    auto pair_fail = [&](bool ok_here) { return bar_red_or(pair_bar, 64, !ok_here); };
+    bool aborted = false;
+    for (uint32_t ik = 0; !aborted; ++ik) {
       const uint32_t is = ik % kItemSlots;
-      if (!(ok = wait_warp(&item_full[is], (ik / kItemSlots) & 1))) break;
+      const bool iok = wait_w(&item_full[is], (ik / kItemSlots) & 1);
+      if (pair_fail(iok)) break;
       const Item it = islot[is].it;
       const bool valid = islot[is].valid != 0;
       __syncwarp();
@@ -363,12 +379,13 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       const int head = it.hk * G + (it.row0 + r) % G;
       const size_t orow = (size_t)tok * p.hq + head;
       const size_t li = (size_t)head * p.total_q + tok;
+      const int dbase = it.dhalf * DO + hw * HO;  // first output dim of this warpgroup
       if (it.t1 <= it.t0) {
         // nothing visible: out = 0, lse = -inf
         if (live) {
-          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * D + it.dhalf * DO);
-          for (int i = 0; i < DO / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
-          if (p.lse && it.dhalf == 0) p.lse[li] = NEG_INF;
+          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * D + dbase);
+          for (int i = 0; i < HO / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+          if (p.lse && it.dhalf == 0 && hw == 0) p.lse[li] = NEG_INF;
         }
         continue;
       }
@@ -385,28 +402,38 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         hi_r = 0;
       }
       float m = NEG_INF, l0 = 0.f, l1 = 0.f;
+      bool sticky = true;  // waits after a tile's vote that failed; reported at the next vote
       for (int u = 0; u < n; ++u, ++g) {
-        const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
+        const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage + 64 * hw;  // first key of this half
         const uint32_t sb = g & 1;
-        if (!(ok = wait_warp(&s_full[sb], (g >> 1) & 1))) break;
-        tc_fence_after();
-        float x[128];
+        const bool sok = wait_w(&s_full[sb], (g >> 1) & 1);
+        float x[64];
+        if (sok) {
+          tc_fence_after();
+          tmem_load64f(tmem + lane_base + sb * 128 + 64 * hw, x);
+        } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_load32f(tmem + lane_base + sb * 128 + 32 * q, x + 32 * q);
-        if (!(kb >= lo_r && kb + kTileKeys - 1 <= hi_r)) {
+          for (int i = 0; i < 64; ++i) x[i] = NEG_INF;
+        }
+        if (!(kb >= lo_r && kb + 63 <= hi_r)) {
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
+          for (int i = 0; i < 64; ++i)
             if (kb + i < lo_r || kb + i > hi_r) x[i] = NEG_INF;
         }
-        // tile maximum (raw scores; scale > 0)
-        float t[32];
+        // half-tile maximum (raw scores; scale > 0), then the pair's
+        float t[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) t[i] = fmax3(x[4 * i], x[4 * i + 1], fmaxf(x[4 * i + 2], x[4 * i + 3]));
+        for (int i = 0; i < 16; ++i) t[i] = fmax3(x[4 * i], x[4 * i + 1], fmaxf(x[4 * i + 2], x[4 * i + 3]));
 #pragma unroll
-        for (int w = 16; w >= 1; w >>= 1)
+        for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
           for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
-        const float ts = t[0] * scale;
+        xmax[(sb * 2 + hw) * 128 + r] = t[0];
+        if (pair_fail(sok && sticky)) {
+          aborted = true;
+          break;
+        }
+        const float ts = fmaxf(t[0], xmax[(sb * 2 + (hw ^ 1)) * 128 + r]) * scale;
         float alpha = 1.0f;
         bool resc = false;
         if (ts > m + C::kTau) {
@@ -421,13 +448,13 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         if (__any_sync(0xFFFFFFFFu, resc)) {
           l0 *= alpha;
           l1 *= alpha;
-          // O *= alpha for this warp's rows once PV(g - 1) has accumulated into O
-          if (u > 0 && !(ok = wait_warp(&s_free[(g - 1) & 1], ((g - 1) >> 1) & 1))) break;
+          // this warpgroup's O columns *= alpha once PV(g - 1) has accumulated into O
+          if (u > 0) sticky = wait_w(&s_free[(g - 1) & 1], ((g - 1) >> 1) & 1) && sticky;
           tc_fence_after();
 #pragma unroll 1
-          for (int q = 0; q < DO / 64; ++q) {
+          for (int q = 0; q < HO / 64; ++q) {
             float o[64];
-            const uint32_t ta = tmem + lane_base + C::kOCol + 64 * q;
+            const uint32_t ta = tmem + lane_base + C::kOCol + hw * HO + 64 * q;
             tmem_load64f(ta, o);
 #pragma unroll
             for (int i = 0; i < 64; i += 2) {
@@ -438,12 +465,13 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             tmem_store64f(ta, o);
           }
         }
-        // P' = 2^(x * scale - m + shift) as an E4M3 pair, 32 keys (8 columns) at a time,
-        // written over the first 64 columns of this S buffer
+        // P' = 2^(x * scale - m + shift) as an E4M3 pair, 32 keys (8 columns) at a time;
+        // this half's words are columns [16 hw, 16 hw + 16) of the hi and lo terms, which
+        // overwrite the first 64 columns of this S buffer (the pair's scores are in registers)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
           uint32_t hi[8], lo[8];
-          uint32_t sa = 0, sb2 = 0;  // f16x2 partial row sums of these 32 keys (each <= 16 x 256)
+          uint32_t sa = 0, sb2 = 0;  // f16x2 partial row sums of these 32 keys
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int k = 32 * q + 4 * i;
@@ -462,19 +490,20 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           const float2 fa = f16x2_to_f32(sa), fb = f16x2_to_f32(sb2);
           l0 += fa.x + fb.x;
           l1 += fa.y + fb.y;
-          tmem_store8(tmem + lane_base + sb * 128 + 8 * q, hi);
-          tmem_store8(tmem + lane_base + sb * 128 + 32 + 8 * q, lo);
+          tmem_store8(tmem + lane_base + sb * 128 + 16 * hw + 8 * q, hi);
+          tmem_store8(tmem + lane_base + sb * 128 + 32 + 16 * hw + 8 * q, lo);
         }
         tmem_wait_st();
         // rows of the last page past the sequence end may hold anything (even NaN):
         // zero those V rows so that 0 * V stays 0 in the PV MMA
-        if (kb + kTileKeys > it.Lk) {
-          if (!(ok = wait_warp(v_ready, tails & 1))) break;
+        const int kt = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
+        if (kt + kTileKeys > it.Lk) {
+          sticky = wait_w(v_ready, tails & 1) && sticky;
           ++tails;
-          const int zr = max(0, it.Lk - kb);
+          const int zr = max(0, it.Lk - kt);
           uint8_t* st = vring + (vq % SV) * C::kVStageBytes;
           for (int c = 0; c < VC; ++c)
-            for (int x16 = zr * 8 + r; x16 < kTileKeys * 8; x16 += 128)
+            for (int x16 = zr * 8 + hw * 128 + r; x16 < kTileKeys * 8; x16 += 256)
               *reinterpret_cast<uint4*>(st + c * kStageBytes + x16 * 16) = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
         }
@@ -483,16 +512,18 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[sb]);
       }
-      if (!ok) break;
+      if (aborted) break;
       // ---------------- epilogue: O / l, lse
-      if (!(ok = wait_warp(&s_free[(g - 1) & 1], ((g - 1) >> 1) & 1))) break;
+      const bool eok = wait_w(&s_free[(g - 1) & 1], ((g - 1) >> 1) & 1) && sticky;
+      lsum[hw * 128 + r] = l0 + l1;
+      if (pair_fail(eok)) break;
       tc_fence_after();
-      const float l = l0 + l1;
+      const float l = lsum[r] + lsum[128 + r];
       const float inv = l > 0.f ? vd / l : 0.f;
       // Each 32-column chunk of this warp's 32 rows goes through a 2 KB staging
       // buffer (row-major, 16-byte pieces swizzled by (row >> 1) & 3), then out as
       // 64-byte row segments: lane l stores piece l & 3 of row i * 8 + l / 4.
-      uint8_t* stg = ostage + quarter * 2048;
+      uint8_t* stg = ostage + (warp - 3) * 2048;
       __nv_bfloat16* dst_row[4];
       bool dst_live[4];
 #pragma unroll
@@ -500,22 +531,22 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         const int rr = quarter * 32 + i * 8 + (lane >> 2);
         dst_live[i] = rr < it.nrows;
         const size_t row = (size_t)(it.q0 + (it.row0 + rr) / G) * p.hq + it.hk * G + (it.row0 + rr) % G;
-        dst_row[i] = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + it.dhalf * DO + (lane & 3) * 8;
+        dst_row[i] = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + dbase + (lane & 3) * 8;
       }
 #pragma unroll 1
-      for (int q2 = 0; q2 < DO / 64; ++q2) {
+      for (int q2 = 0; q2 < HO / 64; ++q2) {
         float o[64];
-        tmem_load64f(tmem + lane_base + C::kOCol + 64 * q2, o);
+        tmem_load64f(tmem + lane_base + C::kOCol + hw * HO + 64 * q2, o);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int q = 2 * q2 + h;
+        for (int hh = 0; hh < 2; ++hh) {
+          const int q = 2 * q2 + hh;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               __nv_bfloat162 b2 =
-                  __floats2bfloat162_rn(o[32 * h + 8 * c + 2 * i] * inv, o[32 * h + 8 * c + 2 * i + 1] * inv);
+                  __floats2bfloat162_rn(o[32 * hh + 8 * c + 2 * i] * inv, o[32 * hh + 8 * c + 2 * i + 1] * inv);
               w[i] = *reinterpret_cast<uint32_t*>(&b2);
             }
             *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
@@ -531,7 +562,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           __syncwarp();
         }
       }
-      if (live && p.lse && it.dhalf == 0)
+      if (live && p.lse && it.dhalf == 0 && hw == 0)
         p.lse[li] = l > 0.f ? (m - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
       tc_fence_before();
       __syncwarp();
