@@ -39,7 +39,7 @@ import synth  # noqa: E402
 
 DEFAULT_CONFIG = "swa_decode_hd256"
 METRIC = "paged FP8 attn: prefill TFLOP/s & decode KV GB/s, % of GB300 roofline"
-KERNEL_SOURCES = ["attn_kernel.cuh", "common.cuh", "ptx.cuh", "attn_launch.cuh"]
+KERNEL_SOURCES = ["attn_kernel.cuh", "attn_prefill.cuh", "common.cuh", "ptx.cuh", "attn_launch.cuh"]
 
 
 def dist_env():
@@ -325,7 +325,9 @@ def run_ours(args):
         peak_src = (peaks["source"] + " MEASURED_PEAKS.json bf16_tflops (burst)" +
                     (" x 2, the nominal FP8/BF16 dense ratio" if w.fp8_q else ""))
         roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
-                    "frac": round(achieved / peak, 4), "traffic": ncu_traffic(w.name), "kernel": "attn_fwd_kernel",
+                    "frac": round(achieved / peak, 4), "traffic": ncu_traffic(w.name),
+                    # prefill tiles with E4M3 Q run the rows-on-lanes kernel
+                    "kernel": "attn_prefill_kernel" if w.fp8_q else "attn_fwd_kernel",
                     "kernel_ms": round(k_avg_ms, 5), "peak_source": peak_src}
     else:
         unit = "GB/s"
