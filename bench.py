@@ -238,6 +238,23 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------------------------ replicas across ranks
+
+def slowest_rank_ms(ms: float, world: int, device) -> float:
+    """The whole job's time of a replicated (weak-scaling) run: the maximum over
+    ranks of each rank's elapsed milliseconds."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(work_per_step: float, world: int, steps: int, ms_total: float, tflops: bool) -> float:
+    """Whole-job throughput: the work of every rank's steps over the slowest rank's time."""
+    return world * work_per_step * steps / (ms_total * 1e-3) / (1e12 if tflops else 1e9)
+
+
 # ------------------------------------------------------------------ GPU leg
 
 def run_ours(args):
@@ -306,10 +323,7 @@ def run_ours(args):
     clock_info = clocks.stop()
     ms_total = t_start.elapsed_time(t_stop)
     k_ms = [a.elapsed_time(b) for a, b in zip(k_start, k_stop)]
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = slowest_rank_ms(ms_total, world, dev)
     ms_step = ms_total / args.steps
     kv_bytes = w.kv_bytes_algorithmic()
     peaks = measured_peaks()
@@ -319,7 +333,7 @@ def run_ours(args):
         # a prefill chunk alone: causal/window-visible QK^T + PV flops against the dense tensor peak
         flops = w.flops_algorithmic()
         unit = "TFLOP/s"
-        value = world * flops * args.steps / (ms_total * 1e-3) / 1e12
+        value = job_rate(flops, world, args.steps, ms_total, True)
         achieved = flops / (k_avg_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"] * (2.0 if w.fp8_q else 1.0)
         peak_src = (peaks["source"] + " MEASURED_PEAKS.json bf16_tflops (burst)" +
@@ -331,7 +345,7 @@ def run_ours(args):
                     "kernel_ms": round(k_avg_ms, 5), "peak_source": peak_src}
     else:
         unit = "GB/s"
-        value = world * kv_bytes * args.steps / (ms_total * 1e-3) / 1e9
+        value = job_rate(kv_bytes, world, args.steps, ms_total, False)
         achieved = kv_bytes / (k_avg_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": unit,
                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(w.name),
@@ -340,7 +354,7 @@ def run_ours(args):
 
     def rate(n_steps, ms):
         work = w.flops_algorithmic() if tensor_bound else kv_bytes
-        return world * work * n_steps / (ms * 1e-3) / (1e12 if tensor_bound else 1e9)
+        return job_rate(work, world, n_steps, ms, tensor_bound)
 
     # ---------------- end to end through the public API, host buffers
     e2e = None
@@ -375,10 +389,7 @@ def run_ours(args):
         b.record(stream)
         torch.cuda.synchronize()
         e_ms = a.elapsed_time(b)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = slowest_rank_ms(e_ms, world, dev)
         e2e = {"value": round(rate(n_e2e, e_ms), 3), "unit": unit,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
                "ms_per_step": round(e_ms / n_e2e, 5),
