@@ -31,14 +31,15 @@ def test_two_gloo_ranks_take_the_slowest_time_and_all_the_work(tmp_path):
         ms = bench.slowest_rank_ms(10.0 + 5.0 * rank, world, "cpu")
         rate = bench.job_rate(2.0e9, world, 10, ms, False)
         dist.barrier()
-        print(json.dumps({{"rank": rank, "world": world, "ms": ms, "rate": rate}}), flush=True)
+        with open(os.path.join({str(tmp_path)!r}, f"rank{{rank}}.json"), "w") as f:
+            json.dump({{"rank": rank, "world": world, "ms": ms, "rate": rate}}, f)
         dist.destroy_process_group()
     """))
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr=127.0.0.1", f"--master-port={_free_port()}", str(script)]
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=180, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
-    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    lines = [json.loads((tmp_path / f"rank{k}.json").read_text()) for k in range(2)]
     assert sorted(l["rank"] for l in lines) == [0, 1]
     for l in lines:
         assert l["world"] == 2
