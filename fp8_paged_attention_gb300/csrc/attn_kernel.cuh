@@ -86,7 +86,10 @@ struct AttnCfg {
   // barriers and the item ring (< 1 KB), then per-row state: ooff[N] (8 bytes),
   // red[2][4][N], lred[4][N] and 4 x [N] floats
   static constexpr int kCtrlBytes = 1536 + 72 * N + 80;
-  static constexpr int kQBufs = kQ8 ? ((2 * kQBytes <= 65536) ? 2 : 1) : ((2 * kQBytes <= 32768) ? 2 : 1);
+  // Two CTAs per SM: one Q buffer, and the room goes to the stage ring (the next
+  // item's Q loads while this item's last tiles and epilogue run).
+  static constexpr int kQBufs =
+      kCtas == 2 ? 1 : kQ8 ? ((2 * kQBytes <= 65536) ? 2 : 1) : ((2 * kQBytes <= 32768) ? 2 : 1);
   static constexpr int kBfSlots = kDqV ? 2 : 0;
   static constexpr int kFixed = kQBufs * kQBytes + 2 * kPBytes + kBfSlots * kBfSlotBytes + kCtrlBytes + 1024;
   static constexpr int kStages = (kSmemLimit - kFixed) / kStageBytes > 16 ? 16 : (kSmemLimit - kFixed) / kStageBytes;
