@@ -75,6 +75,12 @@ def _load():
             lib.or_e4m3_encode_array.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
             lib.or_quantize_q.restype = None
             lib.or_quantize_q.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p]
+            lib.or_kv_cache_write.restype = ctypes.c_int64
+            lib.or_kv_cache_write.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int64,
+            ]
             lib.or_visible_range.restype = ctypes.c_int
             lib.or_visible_range.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)] * 2
             lib.or_paged_attention.restype = ctypes.c_int
@@ -119,6 +125,34 @@ def quantize_q(q_bf16_bits, q_descale: float) -> np.ndarray:
     out = np.empty(q.shape, dtype=np.uint8)
     lib.or_quantize_q(q.ctypes.data, q.size, float(q_descale), out.ctypes.data)
     return out
+
+
+def kv_cache_write(key_bits, value_bits, slot_mapping, k_descale: float, v_descale: float, k_cache, v_cache):
+    """Quantize and scatter new keys and values into the paged cache, in place.
+
+    key_bits, value_bits: uint16 bf16 bit patterns [T, Hkv, D] (or [T, row] with
+    any token stride); slot_mapping: int64 [T]; k_cache, v_cache: uint8
+    [num_pages, 64, Hkv, D], modified in place.  Returns the number of slots
+    past the cache (skipped)."""
+    lib = _load()
+    k = np.asarray(key_bits)
+    v = np.asarray(value_bits)
+    assert k.dtype == np.uint16 and v.dtype == np.uint16
+    assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    num_pages, page, hkv, d = k_cache.shape
+    assert page == PAGE and v_cache.shape == k_cache.shape
+    T = k.shape[0]
+    k2 = k.reshape(T, -1)
+    v2 = v.reshape(T, -1)
+    assert k2.shape[1] == hkv * d and v2.shape[1] == hkv * d
+    # rows may be strided (a view into a wider buffer); elements within a row are contiguous
+    assert k2.strides[1] == 2 and v2.strides[1] == 2
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    assert sm.shape == (T,)
+    return int(lib.or_kv_cache_write(k2.ctypes.data, v2.ctypes.data, k2.strides[0] // 2, v2.strides[0] // 2,
+                                     sm.ctypes.data, T, hkv, d, float(k_descale), float(v_descale),
+                                     k_cache.ctypes.data, v_cache.ctypes.data, num_pages))
 
 
 def visible_range(Lq: int, Lk: int, i: int, window_left: int, causal: bool):

@@ -29,8 +29,16 @@
  *    hi = p when causal (else Lk - 1), clipped to Lk - 1.  lse = m + ln(l),
  *    natural log; an empty visible set gives o = 0 and lse = -inf.
  *
- * Everything is fp64 except the one place the method fixes fp32 (the quotient
- * q / q_descale before rounding to E4M3).  No blocking, fusion or reordering:
+ *  - KV-cache write: the kernels that reshape newly generated keys and values
+ *    and write them into the paged cache, FP8 conversion included ("Why FP8 is
+ *    slower than BF16", the KV-cache writes row of the profiling table and the
+ *    paragraph after it).  Reading used: token t goes to slot s = slot_mapping[t]
+ *    (page s / 64, row s % 64 of the [pages][64][Hkv][D] cache), a negative slot
+ *    is a padding token that writes nothing, and each element is quantized like
+ *    Q: E4M3_RNE_sat(fl32(x / descale)) with the per-tensor K or V descale.
+ *
+ * Everything is fp64 except the places the method fixes fp32 (the quotients
+ * q / q_descale and x / k_descale, x / v_descale before rounding to E4M3).  No blocking, fusion or reordering:
  * one query row at a time, keys in increasing order.
  */
 #include <math.h>
@@ -138,6 +146,47 @@ void or_quantize_q(const uint16_t* q_bf16, int64_t n, float q_descale, uint8_t* 
     else
       out[i] = or_e4m3_encode(v);
   }
+}
+
+/* ------------------------------------------------------------------ KV-cache write */
+
+/* One element: the same rule as or_quantize_q (fp32 quotient, RNE-saturating
+ * E4M3, a NaN quotient to 0x7F with the input's sign). */
+static uint8_t quant_elem(uint16_t bits, float descale) {
+  float x = bf16_bits_to_float(bits);
+  float v = (float)((double)x / (double)descale);
+  if (isnan(v)) return (uint8_t)(0x7F | ((bits >> 8) & 0x80));
+  return or_e4m3_encode(v);
+}
+
+/* Writes token t of key/value (bf16 bit patterns, row t at t * token_stride
+ * elements, num_heads_kv * head_dim contiguous elements per row) into slot
+ * slot_mapping[t] of k_cache / v_cache ([num_pages][64][num_heads_kv][head_dim]
+ * bytes).  Negative slots are skipped; slots at or past num_pages * 64 are
+ * counted and skipped.  Returns the number of such bad slots. */
+int64_t or_kv_cache_write(const uint16_t* key, const uint16_t* value, int64_t key_token_stride,
+                          int64_t value_token_stride, const int64_t* slot_mapping, int64_t num_tokens,
+                          int num_heads_kv, int head_dim, float k_descale, float v_descale, uint8_t* k_cache,
+                          uint8_t* v_cache, int64_t num_pages) {
+  int64_t t, bad = 0;
+  const int64_t row = (int64_t)num_heads_kv * head_dim;
+  for (t = 0; t < num_tokens; ++t) {
+    const int64_t s = slot_mapping[t];
+    int64_t page, off, e;
+    if (s < 0) continue;
+    if (s >= num_pages * OR_PAGE) {
+      ++bad;
+      continue;
+    }
+    page = s / OR_PAGE;
+    off = s % OR_PAGE;
+    for (e = 0; e < row; ++e) {
+      const int64_t dst = (page * OR_PAGE + off) * row + e;
+      k_cache[dst] = quant_elem(key[t * key_token_stride + e], k_descale);
+      v_cache[dst] = quant_elem(value[t * value_token_stride + e], v_descale);
+    }
+  }
+  return bad;
 }
 
 /* ------------------------------------------------------------------ attention */

@@ -442,3 +442,147 @@ def test_tiny_prefill_config_is_finite():
     w = synth.make_config("tiny_prefill_hd256")
     out, lse = oracle.paged_attention(oracle_problem(w))
     assert out.shape == (256, 4, 256) and np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+# ------------------------------------------------------------------ KV-cache write
+
+def _bf16_from_f32(a):
+    """Exact bf16 bit patterns of float32 values that bf16 represents exactly."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    assert np.all(u & 0xFFFF == 0), "value not exact in bf16"
+    return (u >> 16).astype(np.uint16)
+
+
+def _write_case(seed, T=40, hkv=2, d=16, pages=6, pad_every=5):
+    rng = np.random.default_rng(seed)
+    slots = rng.permutation(pages * oracle.PAGE)[:T].astype(np.int64)
+    slots[::pad_every] = -1
+    return rng, slots
+
+
+def test_kv_write_roundtrip_of_exact_codes_lands_in_slot_order():
+    # x = decode(c) * 2^-3 is exact in bf16 and x / 2^-3 = decode(c), so every
+    # finite code must come back unchanged, at its token's slot
+    rng, slots = _write_case(1)
+    T, hkv, d, pages = 40, 2, 16, 6
+    codes = rng.choice(FINITE, size=(T, hkv, d))
+    codes_v = rng.choice(FINITE, size=(T, hkv, d))
+    ds = 0.125
+    k = _bf16_from_f32(oracle.e4m3_decode(codes) * ds)
+    v = _bf16_from_f32(oracle.e4m3_decode(codes_v) * ds)
+    kc = np.full((pages, 64, hkv, d), 0x7F, np.uint8)
+    vc = np.full((pages, 64, hkv, d), 0x7F, np.uint8)
+    assert oracle.kv_cache_write(k, v, slots, ds, ds, kc, vc) == 0
+    flat_k, flat_v = kc.reshape(-1, hkv, d), vc.reshape(-1, hkv, d)
+    written = np.zeros(pages * 64, bool)
+    for t in range(T):
+        if slots[t] < 0:
+            continue
+        written[slots[t]] = True
+        assert np.array_equal(flat_k[slots[t]], codes[t]), t
+        assert np.array_equal(flat_v[slots[t]], codes_v[t]), t
+    assert np.all(flat_k[~written] == 0x7F) and np.all(flat_v[~written] == 0x7F)
+
+
+def test_kv_write_then_attention_matches_directly_paged_cache():
+    # a sequence written token by token into scattered slots, read back through a
+    # block table of those pages by the attention oracle, equals the same codes
+    # laid out by the independent test helper
+    rng = np.random.default_rng(2)
+    Lk, hkv, d, G = 150, 2, 32, 2
+    n_pages = (Lk + 63) // 64
+    pool = 9
+    phys = rng.permutation(pool)[:n_pages]
+    slots = np.array([phys[t // 64] * 64 + t % 64 for t in range(Lk)], np.int64)
+    ds_k, ds_v = 0.25, 0.5
+    ck = rng.choice(FINITE, size=(Lk, hkv, d))
+    cv = rng.choice(FINITE, size=(Lk, hkv, d))
+    k = _bf16_from_f32(oracle.e4m3_decode(ck) * ds_k)
+    v = _bf16_from_f32(oracle.e4m3_decode(cv) * ds_v)
+    kc = np.full((pool, 64, hkv, d), 0x7F, np.uint8)
+    vc = np.full((pool, 64, hkv, d), 0x7F, np.uint8)
+    order = rng.permutation(Lk)
+    assert oracle.kv_cache_write(k[order], v[order], slots[order], ds_k, ds_v, kc, vc) == 0
+    bt = np.full((1, n_pages), pool - 1, np.int32)
+    bt[0, :] = phys
+    q = rng.normal(size=(3, hkv * G, d)).astype(np.float32)
+    qb = _bf16_from_f32(q.astype(np.float32).view(np.uint32).__and__(0xFFFF0000).view(np.float32))
+    common = dict(q=qb, q_is_e4m3=False, cu_seqlens_q=np.array([0, 3], np.int32), seqused_k=np.array([Lk], np.int32),
+                  num_heads_kv=hkv, q_descale=1.0, k_descale=ds_k, v_descale=ds_v, softmax_scale=0.2,
+                  window_left=-1, causal=True)
+    got, lse_got = oracle.paged_attention(oracle.AttnProblem(k_cache=kc, v_cache=vc, block_table=bt, **common))
+    kc2, vc2, bt2 = paged_from_logical([ck], [cv], [Lk], np.random.default_rng(3))
+    want, lse_want = oracle.paged_attention(oracle.AttnProblem(k_cache=kc2, v_cache=vc2, block_table=bt2, **common))
+    assert np.array_equal(got, want) and np.array_equal(lse_got, lse_want)
+
+
+def test_kv_write_padding_slots_write_nothing():
+    rng = np.random.default_rng(4)
+    T, hkv, d, pages = 12, 1, 8, 2
+    k = rng.integers(0, 1 << 16, size=(T, hkv, d), dtype=np.uint16)
+    kc = np.full((pages, 64, hkv, d), 0x5A, np.uint8)
+    vc = np.full((pages, 64, hkv, d), 0x5A, np.uint8)
+    assert oracle.kv_cache_write(k, k, np.full(T, -1, np.int64), 1.0, 1.0, kc, vc) == 0
+    assert np.all(kc == 0x5A) and np.all(vc == 0x5A)
+
+
+def test_kv_write_is_independent_of_token_order():
+    rng, slots = _write_case(5)
+    T, hkv, d, pages = 40, 2, 16, 6
+    k = _bf16_from_f32(rng.normal(size=(T, hkv, d)).astype(np.float32).view(np.uint32).__and__(0xFFFF0000)
+                       .view(np.float32))
+    v = _bf16_from_f32(rng.normal(size=(T, hkv, d)).astype(np.float32).view(np.uint32).__and__(0xFFFF0000)
+                       .view(np.float32))
+    a = [np.zeros((pages, 64, hkv, d), np.uint8) for _ in range(4)]
+    oracle.kv_cache_write(k, v, slots, 0.03, 0.07, a[0], a[1])
+    p = rng.permutation(T)
+    oracle.kv_cache_write(k[p], v[p], slots[p], 0.03, 0.07, a[2], a[3])
+    assert np.array_equal(a[0], a[2]) and np.array_equal(a[1], a[3])
+
+
+def test_kv_write_codes_are_nearest_e4m3_of_fp32_quotient():
+    # brute force: each written code decodes to a finite E4M3 value nearest to
+    # fl32(x / descale) (ties to the even code, |quotient| >= 464 saturates to 448)
+    rng = np.random.default_rng(6)
+    T, hkv, d = 64, 1, 16
+    x = (rng.normal(size=(T, hkv, d)) * rng.choice([1e-3, 1, 40, 3000], size=(T, 1, 1))).astype(np.float32)
+    kb = _bf16_from_f32(x.view(np.uint32).__and__(0xFFFF0000).view(np.float32))
+    ds = np.float32(0.37)
+    kc = np.zeros((1, 64, hkv, d), np.uint8)
+    vc = np.zeros_like(kc)
+    oracle.kv_cache_write(kb, kb, np.arange(T, dtype=np.int64), float(ds), float(ds), kc, vc)
+    vals = oracle.e4m3_decode(FINITE)
+    xs = (kb.astype(np.uint32) << 16).view(np.float32)
+    quot = (xs.astype(np.float64) / np.float64(ds)).astype(np.float32).astype(np.float64).reshape(-1)
+    got = kc.reshape(-1)
+    for qv, c in zip(quot, got):
+        dist = np.abs(vals - np.clip(qv, -448.0, 448.0))
+        best = dist.min()
+        assert abs(oracle.e4m3_decode([c])[0] - np.clip(qv, -448.0, 448.0)) == best
+        if (dist == best).sum() > 1 and qv != 0:
+            assert int(c) & 1 == 0, (qv, hex(c))
+
+
+def test_kv_write_counts_and_skips_slots_past_the_cache():
+    rng = np.random.default_rng(7)
+    T, hkv, d, pages = 6, 1, 8, 1
+    k = rng.integers(0, 0x3F00, size=(T, hkv, d), dtype=np.uint16)
+    slots = np.array([0, 64, 5, 1000, -1, 63], np.int64)
+    kc = np.full((pages, 64, hkv, d), 0x11, np.uint8)
+    vc = np.full_like(kc, 0x11)
+    assert oracle.kv_cache_write(k, k, slots, 1.0, 1.0, kc, vc) == 2
+    untouched = [s for s in range(64) if s not in (0, 5, 63)]
+    assert np.all(kc[0, untouched] == 0x11)
+
+
+def test_kv_write_reads_strided_token_rows():
+    rng = np.random.default_rng(8)
+    T, hkv, d, pages = 20, 2, 8, 1
+    wide = rng.integers(0, 0x3F00, size=(T, 3 * hkv * d), dtype=np.uint16)
+    k = wide[:, hkv * d:2 * hkv * d]
+    v = wide[:, 2 * hkv * d:]
+    slots = rng.permutation(64)[:T].astype(np.int64)
+    a = [np.zeros((pages, 64, hkv, d), np.uint8) for _ in range(4)]
+    oracle.kv_cache_write(k, v, slots, 0.5, 0.25, a[0], a[1])
+    oracle.kv_cache_write(np.ascontiguousarray(k), np.ascontiguousarray(v), slots, 0.5, 0.25, a[2], a[3])
+    assert np.array_equal(a[0], a[2]) and np.array_equal(a[1], a[3])
