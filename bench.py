@@ -6,7 +6,9 @@ workloads), the device-side plan, the attention kernel(s) and the split-KV
 combine, through the library's C ABI.  Inputs are resident in HBM when the
 timed region starts.  The metric is KV-cache bytes read per second
 (algorithmic bytes: the K and V rows of every (sequence, KV head) visible
-key range, counted once), the decode roofline.
+key range, counted once), the decode roofline.  The kv_write_* workloads
+time the paged KV-cache write instead (bf16 K/V read plus E4M3 bytes written,
+per second).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
@@ -40,6 +42,7 @@ import synth  # noqa: E402
 DEFAULT_CONFIG = "swa_decode_hd256"
 METRIC = "paged FP8 attn: prefill TFLOP/s & decode KV GB/s, % of GB300 roofline"
 KERNEL_SOURCES = ["attn_kernel.cuh", "attn_prefill.cuh", "common.cuh", "ptx.cuh", "attn_launch.cuh"]
+KV_WRITE_SOURCES = ["kv_cache_write.cu"]
 
 
 def dist_env():
@@ -56,23 +59,23 @@ def measured_peaks():
         return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, source="fallback")
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, "fp8_paged_attention_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(config: str):
-    """DRAM bytes per launch of the attention kernel from the committed ncu
+def ncu_traffic(config: str, sources=None):
+    """DRAM bytes per launch of the workload's main kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(config)
-        if e and e.get("kernel_source_sha") == kernel_source_hash():
+        if e and e.get("kernel_source_sha") == kernel_source_hash(sources):
             return e.get("dram_bytes_per_launch")
     except Exception:
         pass
@@ -207,9 +210,63 @@ def oracle_timing(w: synth.Workload, budget_s: float, seed: int = 0, tflops: boo
     return rate, cores, desc, t
 
 
+def kv_write_oracle_timing(w, budget_s: float, seed: int = 0):
+    """Time the oracle's KV-cache write on a bounded sample of the workload's
+    tokens.  Returns (GB/s of algorithmic bytes, cores, description, seconds)."""
+    import oracle  # test/benchmark infrastructure only
+    rng = np.random.default_rng(seed)
+    kb = w.key.cpu().view(torch.int16).numpy().view(np.uint16)
+    vb = w.value.cpu().view(torch.int16).numpy().view(np.uint16)
+    sm = w.slot_mappings[0].cpu().numpy()
+    per_token = w.num_heads_kv * w.head_dim * 2 * 3
+    order = rng.permutation(w.num_tokens)
+
+    def run(idx):
+        pages = np.unique(sm[idx] // synth.PAGE)
+        local = {int(p): i for i, p in enumerate(pages)}
+        slots = np.array([local[int(x) // synth.PAGE] * synth.PAGE + int(x) % synth.PAGE for x in sm[idx]], np.int64)
+        kc = np.zeros((len(pages), synth.PAGE, w.num_heads_kv, w.head_dim), np.uint8)
+        vc = np.zeros_like(kc)
+        k, v = np.ascontiguousarray(kb[idx]), np.ascontiguousarray(vb[idx])
+        t0 = time.perf_counter()
+        oracle.kv_cache_write(k, v, slots, w.k_descale, w.v_descale, kc, vc)
+        return time.perf_counter() - t0
+
+    pilot = order[:64]
+    t = run(pilot)
+    n = int(min(w.num_tokens, max(64, budget_s / max(t, 1e-9) * len(pilot))))
+    idx = order[:n]
+    t = run(idx)
+    desc = (f"{n} of {w.num_tokens} tokens of {w.name} ({n * per_token / 1e6:.1f} MB of algorithmic bytes) "
+            f"in {t:.2f} s, one thread")
+    return n * per_token / t / 1e9, 1, desc, t
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
+        return 0
+    if args.config in synth.KV_WRITE_CONFIG_NAMES:
+        w = synth.make_kv_write_config(args.config)
+        total_steps = args.steps + args.warmup
+        per_step = max(0.05, min(30.0, 150.0 / max(1, total_steps)))
+        vals, t_all, desc, cores = [], 0.0, "", 1
+        for i in range(total_steps):
+            r, cores, desc, t = kv_write_oracle_timing(w, per_step, seed=i)
+            if i >= args.warmup:
+                vals.append(r)
+                t_all += t
+        value = statistics.median(vals)
+        line = {
+            "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_all / max(1, len(vals)), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 -> e4m3",
+            "data": "synthetic", "config": {"workload": w.name, "sample": "per step: " + desc},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line))
         return 0
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     w = synth.make_config(args.config, device=dev)
@@ -465,13 +522,136 @@ def run_ours(args):
     return 0
 
 
+def run_kv_write(args):
+    """The paged KV-cache write of a mixed batch's new tokens: one launch of
+    fp8pa_kv_cache_write per step.  Metric: algorithmic bytes (bf16 K/V read,
+    E4M3 written) per second against the HBM copy peak."""
+    rank, local_rank, world = dist_env()
+    import fp8_paged_attention_gb300 as fp8pa  # the CUDA library; raises if it cannot load
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    probe = synth.make_kv_write_config(args.config)
+    per_copy = probe.bytes_algorithmic()
+    n_rot = 1 if per_copy >= 3 * l2_bytes else -(-3 * l2_bytes // per_copy)
+    w = synth.make_kv_write_config(args.config, device=dev, copies=n_rot)
+    keys = [w.key] + [w.key.clone() for _ in range(n_rot - 1)]
+    vals = [w.value] + [w.value.clone() for _ in range(n_rot - 1)]
+    shape = (w.num_pages, synth.PAGE, w.num_heads_kv, w.head_dim)
+    k_cache = torch.empty(shape, dtype=torch.uint8, device=dev)
+    v_cache = torch.empty(shape, dtype=torch.uint8, device=dev)
+    kd = torch.tensor([w.k_descale], dtype=torch.float32, device=dev)
+    vd = torch.tensor([w.v_descale], dtype=torch.float32, device=dev)
+    work = w.bytes_algorithmic()
+
+    def step(i, key=None, value=None, slots=None):
+        r = i % n_rot
+        fp8pa.kv_cache_write(keys[r] if key is None else key, vals[r] if value is None else value, k_cache, v_cache,
+                             w.slot_mappings[r] if slots is None else slots, kd, vd)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(args.warmup + i)
+        ev[i][1].record(stream)
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clock_info = clocks.stop()
+    ms_total = slowest_rank_ms(t_start.elapsed_time(t_stop), world, dev)
+    k_avg_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    value = job_rate(work, world, args.steps, ms_total, False)
+    peaks = measured_peaks()
+    achieved = work / (k_avg_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": round(peaks["hbm_gbs"], 1), "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": ncu_traffic(w.name, KV_WRITE_SOURCES), "kernel": "kv_cache_write_kernel",
+                "kernel_ms": round(k_avg_ms, 5),
+                "peak_source": peaks["source"] + " MEASURED_PEAKS.json hbm_gbs (copy)"}
+    # e2e: each step uploads its keys, values and slot mapping from pinned host
+    # memory and reads the device status word back
+    e2e = None
+    if not args.no_e2e:
+        h_k, h_v = w.key.cpu().pin_memory(), w.value.cpu().pin_memory()
+        h_s = [m.cpu().pin_memory() for m in w.slot_mappings]
+        d_k, d_v = torch.empty_like(w.key), torch.empty_like(w.value)
+        d_s = torch.empty_like(w.slot_mappings[0])
+        h_status = torch.zeros(1, dtype=torch.int32).pin_memory()
+        lib = fp8pa.load_library()
+
+        def e2e_step(i):
+            d_k.copy_(h_k, non_blocking=True)
+            d_v.copy_(h_v, non_blocking=True)
+            d_s.copy_(h_s[i % n_rot], non_blocking=True)
+            step(i, d_k, d_v, d_s)
+            lib.fp8pa_get_device_status(h_status.data_ptr(), stream.cuda_stream)
+
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        n_e2e = max(10, args.steps // 4)
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        a.record(stream)
+        for i in range(n_e2e):
+            e2e_step(i)
+        e.record(stream)
+        torch.cuda.synchronize()
+        e_ms = slowest_rank_ms(a.elapsed_time(e), world, dev)
+        h2d = sum(t.numel() * t.element_size() for t in (h_k, h_v, h_s[0]))
+        e2e = {"value": round(job_rate(work, world, n_e2e, e_ms, False), 3), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4, "steps": n_e2e,
+               "ms_per_step": round(e_ms / n_e2e, 5),
+               "note": "the cache is resident state; per step the keys, values and slot mapping go up and the "
+                       "device status word comes back"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r, cores, desc, _t = kv_write_oracle_timing(synth.make_kv_write_config(args.config), args.cpu_budget)
+        cpu = {"value": round(r, 6), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        l2_note = (f"inputs rotated over {n_rot} copies of {per_copy / 1e6:.1f} MB read and written "
+                   f"({n_rot * per_copy / 1e6:.0f} MB, over 3x the {l2_bytes / 1e6:.0f} MB L2)" if n_rot > 1 else
+                   f"inputs larger than L2: {per_copy / 1e6:.0f} MB per step")
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_total / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 -> e4m3", "data": "synthetic",
+            "config": {"workload": w.name, "num_tokens": w.num_tokens, "num_heads_kv": w.num_heads_kv,
+                       "head_dim": w.head_dim, "kv": "e4m3, 64-token pages", "bytes_per_step": work,
+                       "parallelism": f"replicas x{world}", "l2": l2_note},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+            "clocks": clock_info,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=synth.CONFIG_NAMES)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=synth.CONFIG_NAMES + synth.KV_WRITE_CONFIG_NAMES)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
@@ -482,6 +662,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.config in synth.KV_WRITE_CONFIG_NAMES:
+        return run_kv_write(args)
     return run_ours(args)
 
 

@@ -19,6 +19,7 @@ from . import _build
 __all__ = [
     "build", "load_library", "library_path", "quantize_q_fp8", "fp8_paged_attn_fwd", "workspace_size",
     "num_splits", "kernel_launches", "set_timing_events", "set_ctas_per_sm", "set_bf16_dequant_v", "get_device_status", "reset_device_status",
+    "kv_cache_write", "DEV_BAD_SLOT",
     "set_wait_limit", "set_stall_injection", "FP8PA_BF16", "FP8PA_E4M3",
     "DEV_BAD_PAGE", "DEV_TIMEOUT", "DEV_BAD_LENGTH", "PAGE_SIZE", "Fp8paError",
 ]
@@ -28,6 +29,7 @@ FP8PA_E4M3 = 1
 DEV_BAD_PAGE = 1
 DEV_TIMEOUT = 2
 DEV_BAD_LENGTH = 4
+DEV_BAD_SLOT = 8
 PAGE_SIZE = 64
 
 _lock = threading.Lock()
@@ -61,6 +63,11 @@ def load_library():
         c = ctypes
         lib.quantize_q_fp8.restype = c.c_int
         lib.quantize_q_fp8.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_longlong, c.c_void_p]
+        lib.fp8pa_kv_cache_write.restype = c.c_int
+        lib.fp8pa_kv_cache_write.argtypes = [
+            c.c_void_p, c.c_void_p, c.c_longlong, c.c_longlong, c.c_void_p, c.c_void_p, c.c_int, c.c_void_p,
+            c.c_longlong, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p,
+        ]
         lib.fp8pa_workspace_size.restype = c.c_size_t
         lib.fp8pa_workspace_size.argtypes = [c.c_int] * 10
         lib.fp8pa_num_splits.restype = c.c_int
@@ -167,6 +174,36 @@ def quantize_q_fp8(q: torch.Tensor, q_descale: torch.Tensor, out: torch.Tensor |
         out = torch.empty(q.shape, dtype=torch.uint8, device=q.device)
     _check(lib.quantize_q_fp8(_ptr(q), _ptr(out), _ptr(q_descale), q.numel(), _stream_ptr(stream)))
     return out
+
+
+def kv_cache_write(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   slot_mapping: torch.Tensor, k_descale: torch.Tensor, v_descale: torch.Tensor, stream=None):
+    """Quantize new keys and values to E4M3 and write them into the paged cache.
+
+    key, value: bf16 [T, Hkv, D] CUDA tensors whose rows may be strided (a view
+    into a fused QKV buffer); k_cache, v_cache: uint8 [num_pages, 64, Hkv, D];
+    slot_mapping: int64 [T] (slot = page * 64 + row, negative = padding);
+    descales: one f32 each on the device.  Writes in place; returns nothing.
+    """
+    lib = load_library()
+    for name, t in (("key", key), ("value", value)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 3:
+            raise ValueError(f"{name} must be a CUDA bfloat16 [T, Hkv, D] tensor")
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{name}: each token row must be contiguous")
+    num_pages, page, hkv, d = k_cache.shape
+    if page != PAGE_SIZE or tuple(v_cache.shape) != tuple(k_cache.shape) or k_cache.dtype != torch.uint8:
+        raise ValueError("k_cache / v_cache must be uint8 [num_pages, 64, Hkv, D]")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("k_cache / v_cache must be contiguous")
+    T = key.shape[0]
+    if tuple(key.shape) != (T, hkv, d) or tuple(value.shape) != (T, hkv, d):
+        raise ValueError("key / value must be [T, Hkv, D] with the cache's Hkv and D")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != T or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous int64 tensor of T entries")
+    _check(lib.fp8pa_kv_cache_write(_ptr(key), _ptr(value), key.stride(0), value.stride(0), _ptr(k_cache),
+                                    _ptr(v_cache), num_pages, _ptr(slot_mapping), T, hkv, d, _ptr(k_descale),
+                                    _ptr(v_descale), _stream_ptr(stream)))
 
 
 def fp8_paged_attn_fwd(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q, q_descale,

@@ -311,6 +311,34 @@ int quantize_q_fp8(const void* q_bf16, void* q_e4m3, const float* q_descale, lon
   return FP8PA_OK;
 }
 
+int fp8pa_kv_cache_write(const void* key, const void* value, long long key_token_stride,
+                         long long value_token_stride, uint8_t* k_cache, uint8_t* v_cache, int num_pages,
+                         const int64_t* slot_mapping, long long num_tokens, int num_heads_kv, int head_dim,
+                         const float* k_descale, const float* v_descale, fp8pa_stream_t stream) {
+  if (num_tokens < 0) return fail(FP8PA_EINVAL, "kv_cache_write: num_tokens must be >= 0 (got %lld)", num_tokens);
+  if (num_tokens == 0) return FP8PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping || !k_descale || !v_descale)
+    return fail(FP8PA_EINVAL, "kv_cache_write: null pointer");
+  if (num_heads_kv < 1 || head_dim < 1 || num_pages < 0)
+    return fail(FP8PA_EINVAL, "kv_cache_write: num_heads_kv, head_dim must be >= 1 and num_pages >= 0");
+  const long long row = (long long)num_heads_kv * head_dim;
+  if (row % 8 != 0 || row > (1LL << 30))
+    return fail(FP8PA_EINVAL, "kv_cache_write: num_heads_kv * head_dim = %lld is not a multiple of 8", row);
+  if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 || value_token_stride % 8)
+    return fail(FP8PA_EINVAL, "kv_cache_write: token strides must be >= num_heads_kv * head_dim and multiples of 8");
+  if (reinterpret_cast<uintptr_t>(key) % 16 || reinterpret_cast<uintptr_t>(value) % 16 ||
+      reinterpret_cast<uintptr_t>(k_cache) % 8 || reinterpret_cast<uintptr_t>(v_cache) % 8)
+    return fail(FP8PA_EINVAL, "kv_cache_write: key/value need 16-byte and the caches 8-byte alignment");
+  unsigned* status = status_ptr();
+  if (!status) return fail(FP8PA_ECUDA, "kv_cache_write: device status word unavailable");
+  cudaError_t e = launch_kv_cache_write(key, value, key_token_stride, value_token_stride, k_cache, v_cache,
+                                        reinterpret_cast<const long long*>(slot_mapping), num_tokens, (int)row,
+                                        (long long)num_pages * FP8PA_PAGE_SIZE, k_descale, v_descale, status,
+                                        device_sms(), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_cache_write launch");
+  return FP8PA_OK;
+}
+
 size_t fp8pa_workspace_size(int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv,
                             int head_dim, int q_dtype, int max_pages_per_seq, int window_left, int num_splits) {
   CallPlan pl;

@@ -1,0 +1,92 @@
+// Paged KV-cache write: newly generated keys and values are quantized to E4M3
+// and scattered into their 64-token pages ("Why FP8 is slower than BF16": the
+// KV-cache writes row of the profiling table, the kernels that reshape and write
+// new keys and values into the paged cache, FP8 conversion included).
+//
+// Token t goes to slot s = slot_mapping[t], i.e. row s % 64 of page s / 64 of
+// the [pages][64][Hkv][D] cache; a negative slot is a padding token.  Each
+// element is quantized like Q: E4M3_RNE_sat(fl32(x / descale)), an IEEE fp32
+// division then the hardware round-to-nearest-even saturating conversion, a NaN
+// quotient mapped to 0x7F with the input's sign.
+//
+// The op is HBM-bound (2 bytes read, 1 written per element).  One unit is one
+// (token, tensor) row: Hkv * D contiguous bf16 elements in, the same number of
+// contiguous bytes out.  A warp runs one unit at a time, four 16-byte vectors
+// per lane in flight per pass, and fetches the slot of its next unit while it
+// converts the current one; units go to warps with the stride of the grid.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "fp8pa.h"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "quant_e4m3.cuh"
+
+namespace fp8pa {
+
+namespace {
+
+constexpr int kWarps = 8;  // warps per block
+constexpr int kPerLane = 4;  // vectors per lane per pass
+
+__global__ void __launch_bounds__(32 * kWarps) kv_cache_write_kernel(
+    const uint16_t* __restrict__ key, const uint16_t* __restrict__ value, long long key_stride,
+    long long value_stride, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+    const long long* __restrict__ slot_mapping, long long num_tokens, int row_vecs, long long num_slots,
+    const float* __restrict__ k_descale, const float* __restrict__ v_descale, unsigned* status) {
+  ptx::griddep_wait();
+  const float dk = *k_descale, dv = *v_descale;
+  const float rk = __frcp_rn(dk), rv = __frcp_rn(dv);
+  const bool fast = quant::fast_ok(dk) && quant::fast_ok(dv);
+  const int lane = threadIdx.x & 31;
+  const long long units = 2 * num_tokens;
+  const long long stride = (long long)gridDim.x * kWarps;
+  auto token_of = [&](long long u) { return u >= num_tokens ? u - num_tokens : u; };
+  long long u = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  long long sl = u < units ? slot_mapping[token_of(u)] : -1;
+  for (; u < units; u += stride) {
+    const long long un = u + stride;
+    const long long sl_next = un < units ? slot_mapping[token_of(un)] : -1;  // in flight during this unit
+    const bool is_v = u >= num_tokens;
+    const long long t = token_of(u);
+    if (sl >= num_slots) {
+      if (lane == 0 && !is_v) atomicOr(status, (unsigned)FP8PA_DEV_BAD_SLOT);
+    } else if (sl >= 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(is_v ? value + t * value_stride : key + t * key_stride);
+      uint2* dst = reinterpret_cast<uint2*>((is_v ? v_cache : k_cache) + sl * (long long)row_vecs * 8);
+      const float d = is_v ? dv : dk, r = is_v ? rv : rk;
+      auto q2 = [&](uint32_t w) { return fast ? quant::fast_pair(w, r, d) : quant::exact_pair(w, d); };
+      auto q8 = [&](uint4 a) { return make_uint2(q2(a.x) | (q2(a.y) << 16), q2(a.z) | (q2(a.w) << 16)); };
+      for (int c0 = lane; c0 < row_vecs; c0 += 32 * kPerLane) {
+        uint4 a[kPerLane];
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k)
+          if (c0 + 32 * k < row_vecs) a[k] = __ldcs(src + c0 + 32 * k);
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k)
+          if (c0 + 32 * k < row_vecs) dst[c0 + 32 * k] = q8(a[k]);
+      }
+    }
+    sl = sl_next;
+  }
+  ptx::griddep_launch_dependents();
+}
+
+}  // namespace
+
+cudaError_t launch_kv_cache_write(const void* key, const void* value, long long key_stride, long long value_stride,
+                                  uint8_t* k_cache, uint8_t* v_cache, const long long* slot_mapping,
+                                  long long num_tokens, int row_elems, long long num_slots, const float* k_descale,
+                                  const float* v_descale, unsigned* status, int sms, cudaStream_t stream) {
+  if (num_tokens <= 0) return cudaSuccess;
+  const long long units = 2 * num_tokens;
+  const long long cap = 4LL * sms;  // resident blocks (56 registers a thread: four per SM)
+  const long long want = (units + kWarps - 1) / kWarps;
+  const unsigned blocks = (unsigned)(want < cap ? want : cap);
+  return launch_pdl(kv_cache_write_kernel, dim3(blocks), dim3(32 * kWarps), 0, stream,
+                    reinterpret_cast<const uint16_t*>(key), reinterpret_cast<const uint16_t*>(value), key_stride,
+                    value_stride, k_cache, v_cache, slot_mapping, num_tokens, row_elems / 8, num_slots, k_descale,
+                    v_descale, status);
+}
+
+}  // namespace fp8pa

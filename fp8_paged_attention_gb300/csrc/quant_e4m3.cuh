@@ -1,0 +1,55 @@
+// bf16 -> E4M3 codes by the rule E4M3_RNE_sat(fl32(x / d)), two elements at a time.
+//
+// Exact form: an IEEE fp32 division, then the hardware round-to-nearest-even
+// saturating conversion; a NaN quotient gives 0x7F with the input's sign bit.
+//
+// Fast form, bit-identical: q = x * r with r = fl32(1 / d) is within 3 units of
+// 2^-24 (relative) of x / d, and so is fl32(x / d).  Rounding to E4M3 is
+// monotone, so when q * (1 - 2^-21) and q * (1 + 2^-21) round to the same code,
+// the correctly rounded quotient, which lies between them, rounds to that code
+// too.  Otherwise (a quotient within a few ulps of an E4M3 rounding boundary, or
+// a NaN) the exact form decides.  Tiny quotients (below fp32's normal range) all
+// round to a zero code either way; q overflowing to infinity only where x / d
+// exceeds 448 saturates to the same code.  The fast form needs r to carry the
+// relative error bound, hence the normal-range test on d.
+#pragma once
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace fp8pa {
+namespace quant {
+
+__device__ __forceinline__ uint32_t exact_one(uint16_t bits, float d) {
+  const float v = __fdiv_rn(__uint_as_float((uint32_t)bits << 16), d);
+  if (v != v) return (uint32_t)(0x7F | ((bits >> 8) & 0x80));
+  return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Two bf16 values (low half first) -> two codes (low byte first).
+__device__ __forceinline__ uint32_t exact_pair(uint32_t w, float d) {
+  return exact_one((uint16_t)w, d) | (exact_one((uint16_t)(w >> 16), d) << 8);
+}
+
+// d in a range where fl32(1 / d) is a normal number with its usual error bound
+__device__ __forceinline__ bool fast_ok(float d) { return fabsf(d) > 1e-30f && fabsf(d) < 1e30f; }
+
+__device__ __forceinline__ uint32_t cvt_pair(float lo, float hi) {
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(hi), "f"(lo));
+  return c;
+}
+
+__device__ __forceinline__ uint32_t fast_pair(uint32_t w, float r, float d) {
+  const float2 q = __fmul2_rn(make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)),
+                              make_float2(r, r));
+  const float dn = 1.0f - 0x1p-21f, up = 1.0f + 0x1p-21f;
+  const float2 a = __fmul2_rn(q, make_float2(dn, dn)), b = __fmul2_rn(q, make_float2(up, up));
+  const uint32_t ca = cvt_pair(a.x, a.y), cb = cvt_pair(b.x, b.y);
+  // E4M3 NaN codes come only from NaN inputs (the conversion saturates): exact form
+  const bool nan_code = (ca & 0x7F) == 0x7F || (ca & 0x7F00) == 0x7F00;
+  if (ca == cb && !nan_code) return ca;
+  return exact_pair(w, d);
+}
+
+}  // namespace quant
+}  // namespace fp8pa

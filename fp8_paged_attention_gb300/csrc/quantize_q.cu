@@ -1,41 +1,28 @@
 // Q -> E4M3 quantization (the sliding-window layers quantize Q to FP8, vLLM
-// PR 63139, Overview).  q8 = RNE_saturate_e4m3(fl32(q / q_descale)): an IEEE
-// fp32 division, then the hardware round-to-nearest-even, saturating E4M3
-// conversion; a NaN quotient is mapped explicitly to 0x7F with the input's sign bit.
+// PR 63139, Overview).  q8 = RNE_saturate_e4m3(fl32(q / q_descale)), computed
+// bit-identically without a division per element in all but rare cases (see
+// quant_e4m3.cuh); a NaN quotient gives 0x7F with the input's sign bit.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "quant_e4m3.cuh"
 
 namespace fp8pa {
 
 namespace {
 
-// A NaN quotient (NaN input, 0/0, inf/inf) gives 0x7F carrying the sign bit of
-// the bf16 input; the division itself may return a NaN of either sign.
-__device__ __forceinline__ uint8_t quant_one(uint16_t bits, float d) {
-  const float x = __uint_as_float((uint32_t)bits << 16);
-  const float v = __fdiv_rn(x, d);
-  if (v != v) return (uint8_t)(0x7F | ((bits >> 8) & 0x80));
-  return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
-}
-
 // 8 elements per thread when both pointers allow 16-byte / 8-byte accesses.
 __global__ void quantize_q_vec8(const uint4* __restrict__ q, uint2* __restrict__ out, const float* __restrict__ qd,
                                 long long n8) {
   ptx::griddep_wait();
-  const float d = *qd;
+  const float d = *qd, r = __frcp_rn(d);
+  const bool fast = quant::fast_ok(d);
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
     const uint4 v = q[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[2] = {0, 0};
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint16_t bits = (uint16_t)(w[k >> 1] >> (16 * (k & 1)));
-      o[k >> 2] |= (uint32_t)quant_one(bits, d) << (8 * (k & 3));
-    }
-    out[i] = make_uint2(o[0], o[1]);
+    auto q2 = [&](uint32_t w) { return fast ? quant::fast_pair(w, r, d) : quant::exact_pair(w, d); };
+    out[i] = make_uint2(q2(v.x) | (q2(v.y) << 16), q2(v.z) | (q2(v.w) << 16));
   }
   // Let the next kernel (the forward's plan) launch only as this grid drains:
   // launched earlier, the attention grid behind it would take SM room from the
@@ -49,7 +36,7 @@ __global__ void quantize_q_scalar(const uint16_t* __restrict__ q, uint8_t* __res
   const float d = *qd;
   for (long long i = begin + blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)
-    out[i] = quant_one(q[i], d);
+    out[i] = (uint8_t)quant::exact_one(q[i], d);
   ptx::griddep_launch_dependents();
 }
 

@@ -50,7 +50,8 @@ typedef enum { FP8PA_BF16 = 0, FP8PA_E4M3 = 1 } fp8pa_dtype;
 enum {
   FP8PA_DEV_BAD_PAGE = 1,   /* a block-table entry outside [0, num_pages): that page read as zeros */
   FP8PA_DEV_TIMEOUT = 2,    /* a bounded pipeline wait ran out; the kernel stopped early */
-  FP8PA_DEV_BAD_LENGTH = 4  /* seqused_k[b] > 64 * max_pages_per_seq or < 0: clamped */
+  FP8PA_DEV_BAD_LENGTH = 4, /* seqused_k[b] > 64 * max_pages_per_seq or < 0: clamped */
+  FP8PA_DEV_BAD_SLOT = 8    /* fp8pa_kv_cache_write: a slot >= 64 * num_pages; that token was skipped */
 };
 
 /* Tokens per KV-cache page.  Fixed: the cache is laid out in 64-token pages
@@ -69,6 +70,40 @@ enum {
  */
 int quantize_q_fp8(const void* q_bf16, void* q_e4m3, const float* q_descale, long long n_elems,
                    fp8pa_stream_t stream);
+
+/*
+ * fp8pa_kv_cache_write — quantize newly generated keys and values to E4M3 and
+ * write them into the paged cache ("Why FP8 is slower than BF16": the
+ * KV-cache writes row of the profiling table, the kernels that reshape and
+ * write new keys and values into the paged cache, FP8 conversion included).
+ *
+ *   for every token t with s = slot_mapping[t] >= 0:
+ *     k_cache[s / 64][s % 64][h][d] = RNE_saturate_e4m3( fl32( key[t][h][d] / *k_descale ) )
+ *     v_cache[s / 64][s % 64][h][d] = RNE_saturate_e4m3( fl32( value[t][h][d] / *v_descale ) )
+ *
+ * with the rounding of quantize_q_fp8 (IEEE fp32 division, round to nearest
+ * even, saturation to +-448, NaN to 0x7F with the input's sign bit).
+ *
+ * key, value: bf16, token t's num_heads_kv * head_dim elements contiguous at
+ *   element offset t * key_token_stride (value_token_stride); 16-byte aligned,
+ *   strides multiples of 8 elements (a slice of a fused QKV buffer qualifies).
+ * k_cache, v_cache: uint8 [num_pages][64][num_heads_kv][head_dim], 8-byte
+ *   aligned, the layout fp8_paged_attn_fwd reads.
+ * slot_mapping: int64 [num_tokens] on the device; a negative slot is a padding
+ *   token and writes nothing; a slot >= 64 * num_pages is skipped and sets
+ *   FP8PA_DEV_BAD_SLOT in the device status word.
+ * k_descale, v_descale: one f32 each on the device (per tensor).
+ * Caller owns every buffer; nothing is allocated; graph-capturable (one
+ * launch, no host synchronisation).  Two tokens mapped to one slot race: the
+ * caller gives distinct slots.
+ * Errors: EINVAL for null pointers, num_tokens < 0, num_heads_kv or head_dim
+ * < 1, num_heads_kv * head_dim not a multiple of 8, misaligned pointers or
+ * strides; ECUDA when the launch fails.  num_tokens == 0 is a no-op.
+ */
+int fp8pa_kv_cache_write(const void* key, const void* value, long long key_token_stride,
+                         long long value_token_stride, uint8_t* k_cache, uint8_t* v_cache, int num_pages,
+                         const int64_t* slot_mapping, long long num_tokens, int num_heads_kv, int head_dim,
+                         const float* k_descale, const float* v_descale, fp8pa_stream_t stream);
 
 /*
  * fp8_paged_attn_fwd_noalloc — the same forward as fp8_paged_attn_fwd (same

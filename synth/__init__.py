@@ -23,6 +23,12 @@ prefill, a sliding-window decode at head dim 256, a full-attention decode at
 head dim 512 (BF16 Q, and FP8 Q), a chunked-prefill mixed batch (head dim 256
 with a 1024-key window; head dim 512 causal) and a speculative-verify batch
 whose 25600-token prefix pages are shared by all sequences.
+
+The KV-cache write workloads draw the new keys and values of the mixed batch's
+8128 tokens with the same K/V recipe (bf16 here, before any quantization), and
+a slot mapping: the chunk's 4096 tokens fill 64 whole pages, and each decode
+token takes the next row of its own sequence's last page (a random row of its
+own page).
 """
 from __future__ import annotations
 
@@ -335,3 +341,73 @@ def subproblem_pages(w: Workload, seqs: Sequence[int]):
     cu[1:] = np.cumsum(lq)
     return dict(q=q, k=k, v=v, block_table=nbt, cu_seqlens_q=cu, seqused_k=w.lk[seqs].astype(np.int32),
                 tokens=np.asarray(tok, dtype=np.int64))
+
+
+# ------------------------------------------------------------------ KV-cache write inputs
+
+def kv_like_values(T: int, hkv: int, d: int, g: torch.Generator) -> torch.Tensor:
+    """bf16 [T, Hkv, D] new keys or values: N(0, 1) with max(1, round(0.01 D))
+    channels per KV head scaled by 8 (the K/V recipe above), on the CPU."""
+    x = torch.randn((T, hkv, d), generator=g, dtype=torch.float32)
+    n = max(1, int(round(0.01 * d)))
+    for h in range(hkv):
+        idx = torch.randperm(d, generator=g)[:n]
+        x[:, h, idx] *= 8.0
+    return x.to(torch.bfloat16)
+
+
+@dataclasses.dataclass
+class KVWriteWorkload:
+    name: str
+    key: torch.Tensor                 # bf16 [T, Hkv, D]
+    value: torch.Tensor
+    slot_mappings: list               # int64 [T] per copy, disjoint slot sets
+    num_pages: int                    # pages of the cache all copies write into
+    k_descale: float
+    v_descale: float
+    num_heads_kv: int
+    head_dim: int
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.key.shape[0])
+
+    def bytes_algorithmic(self) -> int:
+        """bf16 read plus E4M3 written, for K and V: 3 bytes per element."""
+        return self.num_tokens * self.num_heads_kv * self.head_dim * 2 * 3
+
+
+KV_WRITE_CONFIG_NAMES = [
+    "kv_write_mixed_hd256",  # the 8128 new tokens of the hd256 mixed batch: Hkv 16, D 256
+    "kv_write_mixed_hd512",  # the same tokens at D 512, Hkv 4
+]
+
+
+def make_kv_write_config(name: str, device="cpu", copies: int = 1, seed: int = 7) -> KVWriteWorkload:
+    """New keys and values of the mixed batch's step: a 4096-token chunk appended
+    to a sequence (64 whole pages) and 4032 decode tokens, each the next row of
+    its own sequence's last page.  Every copy gets its own pages, so copies never
+    share a slot."""
+    hkv, d = {"kv_write_mixed_hd256": (16, 256), "kv_write_mixed_hd512": (4, 512)}[name]
+    n_chunk, n_dec = 4096, 4032
+    T = n_chunk + n_dec
+    per_copy = n_chunk // PAGE + n_dec
+    pool = copies * per_copy
+    g = torch.Generator().manual_seed(seed)
+    key = kv_like_values(T, hkv, d, g)
+    value = kv_like_values(T, hkv, d, g)
+    rng = np.random.default_rng(np.random.PCG64(seed))
+    pages = rng.permutation(pool).astype(np.int64)
+    maps = []
+    for c in range(copies):
+        own = pages[c * per_copy:(c + 1) * per_copy]
+        chunk = own[: n_chunk // PAGE]
+        dec = own[n_chunk // PAGE:]
+        sm = np.empty(T, np.int64)
+        sm[:n_chunk] = chunk[np.arange(n_chunk) // PAGE] * PAGE + np.arange(n_chunk) % PAGE
+        sm[n_chunk:] = dec * PAGE + rng.integers(0, PAGE, size=n_dec)
+        maps.append(torch.from_numpy(sm).to(device))
+    kd = float(np.float32(np.float32(key.float().abs().amax().item()) / np.float32(448.0)))
+    vd = float(np.float32(np.float32(value.float().abs().amax().item()) / np.float32(448.0)))
+    return KVWriteWorkload(name=name, key=key.to(device), value=value.to(device), slot_mappings=maps, num_pages=pool,
+                           k_descale=kd, v_descale=vd, num_heads_kv=hkv, head_dim=d)

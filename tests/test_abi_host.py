@@ -97,3 +97,23 @@ def test_workspace_and_splits_are_host_functions():
     assert fp8pa.workspace_size(1, 1, 1, 32, 16, 128, E4M3, 4, -1, 0) == 0
     assert fp8pa.workspace_size(1, 1, 1, 32, 16, 256, BF16, 4, -1, 0) == 0
     assert fp8pa.num_splits(1, 1, 1, 30, 16, 256, E4M3, 4, -1, 0) == 0
+
+
+def _kvw(**kw):
+    import fp8_paged_attention_gb300 as fp8pa
+    lib = fp8pa.load_library()
+    a = dict(key=16, value=16, ks=256, vs=256, kc=8, vc=8, pages=4, slots=8, T=3, hkv=1, d=256, kd=4, vd=4)
+    a.update(kw)
+    return lib.fp8pa_kv_cache_write(a["key"], a["value"], a["ks"], a["vs"], a["kc"], a["vc"], a["pages"], a["slots"],
+                                    a["T"], a["hkv"], a["d"], a["kd"], a["vd"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(key=0), dict(slots=0), dict(kd=0), dict(T=-1), dict(hkv=0), dict(d=6),
+                                dict(ks=255), dict(vs=8), dict(key=24), dict(kc=4)])
+def test_kv_cache_write_rejects_bad_arguments_before_launch(kw):
+    # every check runs on the host before any device access (the pointers here are not device memory)
+    assert _kvw(**kw) == 1  # FP8PA_EINVAL
+
+
+def test_kv_cache_write_zero_tokens_is_a_noop():
+    assert _kvw(T=0) == 0
