@@ -42,7 +42,7 @@ import synth  # noqa: E402
 DEFAULT_CONFIG = "swa_decode_hd256"
 METRIC = "paged FP8 attn: prefill TFLOP/s & decode KV GB/s, % of GB300 roofline"
 KERNEL_SOURCES = ["attn_kernel.cuh", "attn_prefill.cuh", "common.cuh", "ptx.cuh", "attn_launch.cuh"]
-KV_WRITE_SOURCES = ["kv_cache_write.cu"]
+KV_WRITE_SOURCES = ["kv_cache_write.cu", "quant_e4m3.cuh"]
 
 
 def dist_env():
