@@ -81,6 +81,9 @@ def _load():
                 ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_int64,
             ]
+            lib.or_lse_combine.restype = None
+            lib.or_lse_combine.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
             lib.or_visible_range.restype = ctypes.c_int
             lib.or_visible_range.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)] * 2
             lib.or_paged_attention.restype = ctypes.c_int
@@ -153,6 +156,22 @@ def kv_cache_write(key_bits, value_bits, slot_mapping, k_descale: float, v_desca
     return int(lib.or_kv_cache_write(k2.ctypes.data, v2.ctypes.data, k2.strides[0] // 2, v2.strides[0] // 2,
                                      sm.ctypes.data, T, hkv, d, float(k_descale), float(v_descale),
                                      k_cache.ctypes.data, v_cache.ctypes.data, num_pages))
+
+
+def lse_combine(o_parts_bits, lse_parts):
+    """Merge attention partials over disjoint key sets by their LSE.
+
+    o_parts_bits: uint16 bf16 patterns [P, total_q, Hq, D]; lse_parts: f32
+    [P, Hq, total_q].  Returns (out fp64 [total_q, Hq, D], lse fp64 [Hq, total_q])."""
+    lib = _load()
+    o = np.ascontiguousarray(o_parts_bits, dtype=np.uint16)
+    ls = np.ascontiguousarray(lse_parts, dtype=np.float32)
+    P, T, hq, d = o.shape
+    assert ls.shape == (P, hq, T)
+    out = np.empty((T, hq, d), dtype=np.float64)
+    lse = np.empty((hq, T), dtype=np.float64)
+    lib.or_lse_combine(o.ctypes.data, ls.ctypes.data, P, T, hq, d, out.ctypes.data, lse.ctypes.data)
+    return out, lse
 
 
 def visible_range(Lq: int, Lk: int, i: int, window_left: int, causal: bool):

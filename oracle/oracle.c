@@ -37,6 +37,15 @@
  *    is a padding token that writes nothing, and each element is quantized like
  *    Q: E4M3_RNE_sat(fl32(x / descale)) with the per-tensor K or V descale.
  *
+ *  - Combining attention partials by their LSE: the context call of
+ *    decode-context parallelism, in which each rank attends over its shard of
+ *    the keys and returns its output and LSE ("[Kernel] Integrate FA4 SM90 FP8
+ *    MMA for Gemma-4 full attention", review thread on DCP: the non-causal
+ *    context call run as local attention with a window covering every key,
+ *    and a DCP=2 emulation).  With parts s over disjoint key sets,
+ *    L = ln sum_s exp(LSE_s) and O = sum_s exp(LSE_s - L) O_s; parts with
+ *    LSE = -inf add nothing, and a row with no part gives O = 0, L = -inf.
+ *
  * Everything is fp64 except the places the method fixes fp32 (the quotients
  * q / q_descale and x / k_descale, x / v_descale before rounding to E4M3).  No blocking, fusion or reordering:
  * one query row at a time, keys in increasing order.
@@ -187,6 +196,47 @@ int64_t or_kv_cache_write(const uint16_t* key, const uint16_t* value, int64_t ke
     }
   }
   return bad;
+}
+
+/* ------------------------------------------------------------------ LSE combine */
+
+/* o_parts: bf16 bit patterns [num_parts][total_q][hq][d]; lse_parts: f32
+ * [num_parts][hq][total_q] (natural log).  out: fp64 [total_q][hq][d];
+ * lse: fp64 [hq][total_q]. */
+void or_lse_combine(const uint16_t* o_parts, const float* lse_parts, int num_parts, int64_t total_q, int hq, int d,
+                    double* out, double* lse) {
+  int64_t t;
+  int h, s, e;
+  const int64_t rows = total_q * hq;
+  for (t = 0; t < total_q; ++t) {
+    for (h = 0; h < hq; ++h) {
+      double m = -INFINITY, sum = 0.0, L;
+      double* o = out + (t * hq + h) * d;
+      for (e = 0; e < d; ++e) o[e] = 0.0;
+      for (s = 0; s < num_parts; ++s) {
+        const double ls = lse_parts[(int64_t)s * rows + (int64_t)h * total_q + t];
+        if (ls > m) m = ls;
+      }
+      if (m == -INFINITY) {
+        lse[(int64_t)h * total_q + t] = -INFINITY;
+        continue;
+      }
+      for (s = 0; s < num_parts; ++s) {
+        const double ls = lse_parts[(int64_t)s * rows + (int64_t)h * total_q + t];
+        if (ls != -INFINITY) sum += exp(ls - m);
+      }
+      L = m + log(sum);
+      lse[(int64_t)h * total_q + t] = L;
+      for (s = 0; s < num_parts; ++s) {
+        const double ls = lse_parts[(int64_t)s * rows + (int64_t)h * total_q + t];
+        const uint16_t* os = o_parts + ((int64_t)s * rows + t * hq + h) * d;
+        double wgt;
+        if (ls == -INFINITY) continue;
+        wgt = exp(ls - L);
+        for (e = 0; e < d; ++e) o[e] += wgt * (double)bf16_bits_to_float(os[e]);
+      }
+    }
+  }
 }
 
 /* ------------------------------------------------------------------ attention */

@@ -586,3 +586,86 @@ def test_kv_write_reads_strided_token_rows():
     oracle.kv_cache_write(k, v, slots, 0.5, 0.25, a[0], a[1])
     oracle.kv_cache_write(np.ascontiguousarray(k), np.ascontiguousarray(v), slots, 0.5, 0.25, a[2], a[3])
     assert np.array_equal(a[0], a[2]) and np.array_equal(a[1], a[3])
+
+
+# ------------------------------------------------------------------ LSE combine
+
+def _to_bf16_bits(a):
+    """Round fp64 values to bf16 (round to nearest even) and return the bit patterns."""
+    f = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (f + 0x7FFF + ((f >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def _noncausal_problem(seed, lk, hkv=2, G=2, d=32, lq=3):
+    rng = np.random.default_rng(seed)
+    kl = [rng.choice(FINITE[FINITE < 0x70], size=(n, hkv, d)) for n in lk]
+    vl = [rng.choice(FINITE[FINITE < 0x70], size=(n, hkv, d)) for n in lk]
+    q = _to_bf16_bits(rng.normal(size=(lq * len(lk), hkv * G, d)))
+    return rng, kl, vl, q
+
+
+def _attend(q, kl, vl, lk, lq, hkv, seed):
+    kc, vc, bt = paged_from_logical(kl, vl, lk, np.random.default_rng(seed))
+    prob = oracle.AttnProblem(q=q, q_is_e4m3=False, k_cache=kc, v_cache=vc, block_table=bt,
+                              cu_seqlens_q=cu_from_lq([lq] * len(lk)), seqused_k=np.array(lk, np.int32),
+                              num_heads_kv=hkv, q_descale=1.0, k_descale=0.5, v_descale=0.25, softmax_scale=0.3,
+                              window_left=-1, causal=False)
+    return oracle.paged_attention(prob)
+
+
+def test_lse_combine_of_key_shards_is_the_whole_softmax():
+    # attention over two disjoint key shards, each returned as bf16 O and f32 LSE,
+    # combines to the attention over all keys (within the bf16 rounding of the parts)
+    lk, lq, hkv = [150, 70], 3, 2
+    rng, kl, vl, q = _noncausal_problem(21, lk, hkv=hkv, lq=lq)
+    full, lse_full = _attend(q, kl, vl, lk, lq, hkv, 1)
+    cut = [64, 64]
+    a, la = _attend(q, [k[:c] for k, c in zip(kl, cut)], [v[:c] for v, c in zip(vl, cut)], cut, lq, hkv, 2)
+    rest = [n - c for n, c in zip(lk, cut)]
+    b, lb = _attend(q, [k[c:] for k, c in zip(kl, cut)], [v[c:] for v, c in zip(vl, cut)], rest, lq, hkv, 3)
+    parts = np.stack([_to_bf16_bits(a), _to_bf16_bits(b)])
+    lses = np.stack([la, lb]).astype(np.float32)
+    out, lse = oracle.lse_combine(parts, lses)
+    scale = np.abs(full).max()
+    assert np.abs(out - full).max() <= 2.0 ** -8 * scale
+    assert np.abs(lse - lse_full).max() <= 1e-5
+
+
+def test_lse_combine_single_part_and_two_equal_parts():
+    rng = np.random.default_rng(22)
+    o = _to_bf16_bits(rng.normal(size=(1, 5, 4, 16)))
+    l = rng.normal(size=(1, 4, 5)).astype(np.float32)
+    out, lse = oracle.lse_combine(o, l)
+    dec = (o[0].astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(out, dec.astype(np.float64)) and np.array_equal(lse, l[0].astype(np.float64))
+    # two parts with the same LSE c: L = c + ln 2, O = (O1 + O2) / 2
+    o2 = _to_bf16_bits(rng.normal(size=(2, 5, 4, 16)))
+    l2 = np.repeat(l, 2, axis=0)
+    out, lse = oracle.lse_combine(o2, l2)
+    d2 = (o2.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.allclose(out, (d2[0] + d2[1]) / 2, rtol=0, atol=1e-12)
+    assert np.allclose(lse, l[0].astype(np.float64) + math.log(2.0), rtol=0, atol=1e-12)
+
+
+def test_lse_combine_empty_parts():
+    rng = np.random.default_rng(23)
+    o = _to_bf16_bits(rng.normal(size=(3, 4, 2, 8)))
+    l = rng.normal(size=(3, 2, 4)).astype(np.float32)
+    l[1] = -np.inf              # an empty shard adds nothing
+    out, lse = oracle.lse_combine(o, l)
+    out2, lse2 = oracle.lse_combine(o[[0, 2]], l[[0, 2]])
+    assert np.allclose(out, out2, rtol=0, atol=1e-14) and np.allclose(lse, lse2, rtol=0, atol=1e-14)
+    l[:] = -np.inf              # no key anywhere: O = 0, lse = -inf
+    out, lse = oracle.lse_combine(o, l)
+    assert np.all(out == 0) and np.all(lse == -np.inf)
+
+
+def test_lse_combine_is_independent_of_part_order():
+    rng = np.random.default_rng(24)
+    o = _to_bf16_bits(rng.normal(size=(4, 6, 2, 8)))
+    l = (rng.normal(size=(4, 2, 6)) * 5).astype(np.float32)
+    a = oracle.lse_combine(o, l)
+    p = [2, 0, 3, 1]
+    b = oracle.lse_combine(o[p], l[p])
+    assert np.allclose(a[0], b[0], rtol=0, atol=1e-12) and np.allclose(a[1], b[1], rtol=0, atol=1e-12)
