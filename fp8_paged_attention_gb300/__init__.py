@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "build", "load_library", "library_path", "quantize_q_fp8", "fp8_paged_attn_fwd", "workspace_size",
     "num_splits", "kernel_launches", "set_timing_events", "set_ctas_per_sm", "set_bf16_dequant_v", "get_device_status", "reset_device_status",
-    "kv_cache_write", "DEV_BAD_SLOT",
+    "kv_cache_write", "DEV_BAD_SLOT", "lse_combine",
     "set_wait_limit", "set_stall_injection", "FP8PA_BF16", "FP8PA_E4M3",
     "DEV_BAD_PAGE", "DEV_TIMEOUT", "DEV_BAD_LENGTH", "PAGE_SIZE", "Fp8paError",
 ]
@@ -68,6 +68,9 @@ def load_library():
             c.c_void_p, c.c_void_p, c.c_longlong, c.c_longlong, c.c_void_p, c.c_void_p, c.c_int, c.c_void_p,
             c.c_longlong, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p,
         ]
+        lib.fp8pa_lse_combine.restype = c.c_int
+        lib.fp8pa_lse_combine.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_longlong, c.c_int, c.c_int, c.c_void_p,
+                                          c.c_void_p, c.c_void_p]
         lib.fp8pa_workspace_size.restype = c.c_size_t
         lib.fp8pa_workspace_size.argtypes = [c.c_int] * 10
         lib.fp8pa_num_splits.restype = c.c_int
@@ -174,6 +177,28 @@ def quantize_q_fp8(q: torch.Tensor, q_descale: torch.Tensor, out: torch.Tensor |
         out = torch.empty(q.shape, dtype=torch.uint8, device=q.device)
     _check(lib.quantize_q_fp8(_ptr(q), _ptr(out), _ptr(q_descale), q.numel(), _stream_ptr(stream)))
     return out
+
+
+def lse_combine(o_parts: torch.Tensor, lse_parts: torch.Tensor, out=None, lse=None, stream=None):
+    """Merge attention partials over disjoint key shards by their LSE.
+
+    o_parts: bf16 [P, total_q, Hq, D]; lse_parts: f32 [P, Hq, total_q] (each
+    part's fp8_paged_attn_fwd out and lse).  Returns (out bf16 [total_q, Hq, D],
+    lse f32 [Hq, total_q]).
+    """
+    lib = load_library()
+    if o_parts.dtype != torch.bfloat16 or not o_parts.is_cuda or o_parts.dim() != 4 or not o_parts.is_contiguous():
+        raise ValueError("o_parts must be a contiguous CUDA bfloat16 [P, total_q, Hq, D] tensor")
+    P, T, hq, d = o_parts.shape
+    if lse_parts.dtype != torch.float32 or tuple(lse_parts.shape) != (P, hq, T) or not lse_parts.is_contiguous():
+        raise ValueError("lse_parts must be a contiguous float32 [P, Hq, total_q] tensor")
+    if out is None:
+        out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=o_parts.device)
+    _check(lib.fp8pa_lse_combine(_ptr(o_parts), _ptr(lse_parts), P, T, hq, d, _ptr(out), _ptr(lse),
+                                 _stream_ptr(stream)))
+    return out, lse
 
 
 def kv_cache_write(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

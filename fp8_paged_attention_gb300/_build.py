@@ -27,6 +27,7 @@ SOURCES = [
     "attn_prefill_d256.cu",
     "attn_prefill_d512.cu",
     "kv_cache_write.cu",
+    "lse_combine.cu",
     "attn_fp8_d512.cu",
     "attn_bf16_d512.cu",
     "attn_bf16dqv_d512.cu",

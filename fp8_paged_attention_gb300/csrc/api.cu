@@ -311,6 +311,22 @@ int quantize_q_fp8(const void* q_bf16, void* q_e4m3, const float* q_descale, lon
   return FP8PA_OK;
 }
 
+int fp8pa_lse_combine(const void* o_parts, const float* lse_parts, int num_parts, long long total_q,
+                      int num_heads_q, int head_dim, void* out, float* lse_out, fp8pa_stream_t stream) {
+  if (total_q < 0) return fail(FP8PA_EINVAL, "lse_combine: total_q must be >= 0 (got %lld)", total_q);
+  if (num_parts < 1 || num_heads_q < 1 || head_dim < 8 || head_dim % 8)
+    return fail(FP8PA_EINVAL, "lse_combine: need num_parts >= 1, num_heads_q >= 1, head_dim a multiple of 8");
+  if (total_q == 0) return FP8PA_OK;
+  if (!o_parts || !lse_parts || !out) return fail(FP8PA_EINVAL, "lse_combine: null pointer");
+  if (reinterpret_cast<uintptr_t>(o_parts) % 16 || reinterpret_cast<uintptr_t>(out) % 16 ||
+      reinterpret_cast<uintptr_t>(lse_parts) % 4 || reinterpret_cast<uintptr_t>(lse_out) % 4)
+    return fail(FP8PA_EINVAL, "lse_combine: o_parts and out need 16-byte, lse buffers 4-byte alignment");
+  cudaError_t e = launch_lse_combine(o_parts, lse_parts, num_parts, total_q, num_heads_q, head_dim, out, lse_out,
+                                     device_sms(), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "lse_combine launch");
+  return FP8PA_OK;
+}
+
 int fp8pa_kv_cache_write(const void* key, const void* value, long long key_token_stride,
                          long long value_token_stride, uint8_t* k_cache, uint8_t* v_cache, int num_pages,
                          const int64_t* slot_mapping, long long num_tokens, int num_heads_kv, int head_dim,

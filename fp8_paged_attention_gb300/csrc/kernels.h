@@ -33,6 +33,8 @@ cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& cp, cudaStream_t stream);
 cudaError_t launch_quantize_q(const void* q_bf16, void* q_e4m3, const float* q_descale, long long n,
                               cudaStream_t stream);
+cudaError_t launch_lse_combine(const void* o_parts, const float* lse_parts, int parts, long long total_q, int hq,
+                               int head_dim, void* out, float* lse_out, int sms, cudaStream_t stream);
 cudaError_t launch_kv_cache_write(const void* key, const void* value, long long key_stride, long long value_stride,
                                   uint8_t* k_cache, uint8_t* v_cache, const long long* slot_mapping,
                                   long long num_tokens, int row_elems, long long num_slots, const float* k_descale,

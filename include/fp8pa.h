@@ -106,6 +106,31 @@ int fp8pa_kv_cache_write(const void* key, const void* value, long long key_token
                          const float* k_descale, const float* v_descale, fp8pa_stream_t stream);
 
 /*
+ * fp8pa_lse_combine — merge attention partials computed over disjoint key
+ * shards, as the context call of decode-context parallelism returns them (the
+ * pages' review thread on DCP: each rank runs the non-causal context call over
+ * its shard of the keys as local attention with a window covering every key,
+ * and returns O and LSE).  Per (token, head) row:
+ *
+ *   L = ln sum_s exp(lse_parts[s]),   out = sum_s exp(lse_parts[s] - L) * o_parts[s]
+ *
+ * Parts with LSE = -inf add nothing; a row with no part gives out = 0 and
+ * L = -inf.  Arithmetic in f32; out rounded to bf16.
+ *
+ * o_parts: bf16 [num_parts][total_q][num_heads_q][head_dim] (the out of each
+ *   part's fp8_paged_attn_fwd call), 16-byte aligned.
+ * lse_parts: f32 [num_parts][num_heads_q][total_q] (each call's lse), natural log.
+ * out: bf16 [total_q][num_heads_q][head_dim], 16-byte aligned; lse_out: f32
+ *   [num_heads_q][total_q] or NULL.  out must not overlap o_parts.
+ * Caller owns every buffer; nothing is allocated; graph-capturable.
+ * Errors: EINVAL for null pointers, num_parts < 1, total_q < 0, num_heads_q
+ * < 1, head_dim not a positive multiple of 8, misaligned pointers; ECUDA when
+ * the launch fails.  total_q == 0 is a no-op.
+ */
+int fp8pa_lse_combine(const void* o_parts, const float* lse_parts, int num_parts, long long total_q,
+                      int num_heads_q, int head_dim, void* out, float* lse_out, fp8pa_stream_t stream);
+
+/*
  * fp8_paged_attn_fwd_noalloc — the same forward as fp8_paged_attn_fwd (same
  * arguments, layouts and results) for callers that cannot allocate device
  * memory at call time: for instance an inference engine that reserves nearly

@@ -117,3 +117,16 @@ def test_kv_cache_write_rejects_bad_arguments_before_launch(kw):
 
 def test_kv_cache_write_zero_tokens_is_a_noop():
     assert _kvw(T=0) == 0
+
+
+@pytest.mark.parametrize("args", [(0, 16, 2, 4, 8, 64, 16, 16), (16, 0, 2, 4, 8, 64, 16, 16), (16, 16, 0, 4, 8, 64, 16, 16),
+                                  (16, 16, 2, -1, 8, 64, 16, 16), (16, 16, 2, 4, 8, 60, 16, 16),
+                                  (24, 16, 2, 4, 8, 64, 16, 16), (16, 16, 2, 4, 8, 64, 8, 16)])
+def test_lse_combine_rejects_bad_arguments_before_launch(args):
+    lib = fp8pa.load_library()
+    o, l, p, t, h, d, out, lo = args
+    assert lib.fp8pa_lse_combine(o, l, p, t, h, d, out, lo, None) == 1  # FP8PA_EINVAL
+
+
+def test_lse_combine_zero_tokens_is_a_noop():
+    assert fp8pa.load_library().fp8pa_lse_combine(16, 16, 2, 0, 8, 64, 16, 16, None) == 0
