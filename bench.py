@@ -43,6 +43,7 @@ DEFAULT_CONFIG = "swa_decode_hd256"
 METRIC = "paged FP8 attn: prefill TFLOP/s & decode KV GB/s, % of GB300 roofline"
 KERNEL_SOURCES = ["attn_kernel.cuh", "attn_prefill.cuh", "common.cuh", "ptx.cuh", "attn_launch.cuh"]
 KV_WRITE_SOURCES = ["kv_cache_write.cu", "quant_e4m3.cuh"]
+COMBINE_SOURCES = ["lse_combine.cu"]
 
 
 def dist_env():
@@ -242,9 +243,50 @@ def kv_write_oracle_timing(w, budget_s: float, seed: int = 0):
     return n * per_token / t / 1e9, 1, desc, t
 
 
+def combine_oracle_timing(w, budget_s: float):
+    """Time the oracle's LSE combine on a bounded sample of rows (tokens)."""
+    import oracle  # test/benchmark infrastructure only
+    P, T, hq, d = w.o_parts.shape
+    ob = w.o_parts.cpu().view(torch.int16).numpy().view(np.uint16)
+    lb = w.lse_parts.cpu().numpy()
+    per_tok = (P + 1) * hq * (2 * d + 4)
+
+    def run(n):
+        o = np.ascontiguousarray(ob[:, :n])
+        ls = np.ascontiguousarray(lb[:, :, :n])
+        t0 = time.perf_counter()
+        oracle.lse_combine(o, ls)
+        return time.perf_counter() - t0
+
+    t = run(16)
+    n = int(min(T, max(16, budget_s / max(t, 1e-9) * 16)))
+    t = run(n)
+    desc = f"{n} of {T} tokens of {w.name} ({n * per_tok / 1e6:.1f} MB of algorithmic bytes) in {t:.2f} s, one thread"
+    return n * per_tok / t / 1e9, 1, desc, t
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
+        return 0
+    if args.config in synth.COMBINE_CONFIG_NAMES:
+        w = synth.make_combine_config(args.config)
+        total_steps = args.steps + args.warmup
+        per_step = max(0.05, min(30.0, 150.0 / max(1, total_steps)))
+        vals, t_all, desc, cores = [], 0.0, "", 1
+        for i in range(total_steps):
+            r, cores, desc, t = combine_oracle_timing(w, per_step)
+            if i >= args.warmup:
+                vals.append(r)
+                t_all += t
+        value = statistics.median(vals)
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_all / max(1, len(vals)), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample": "per step: " + desc},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return 0
     if args.config in synth.KV_WRITE_CONFIG_NAMES:
         w = synth.make_kv_write_config(args.config)
@@ -645,13 +687,108 @@ def run_kv_write(args):
     return 0
 
 
+def run_combine(args):
+    """The LSE combine of two DCP shards' partials: one launch of
+    fp8pa_lse_combine per step.  Metric: algorithmic bytes per second against
+    the HBM copy peak."""
+    rank, local_rank, world = dist_env()
+    import fp8_paged_attention_gb300 as fp8pa  # the CUDA library; raises if it cannot load
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    w = synth.make_combine_config(args.config, device=dev)
+    P, T, hq, d = w.o_parts.shape
+    work = w.bytes_algorithmic()
+    out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((hq, T), dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        fp8pa.lse_combine(w.o_parts, w.lse_parts, out=out, lse=lse)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        fp8pa.lse_combine(w.o_parts, w.lse_parts, out=out, lse=lse)
+        ev[i][1].record(stream)
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clock_info = clocks.stop()
+    ms_total = slowest_rank_ms(t_start.elapsed_time(t_stop), world, dev)
+    k_avg_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    peaks = measured_peaks()
+    achieved = work / (k_avg_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": round(peaks["hbm_gbs"], 1), "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(w.name, COMBINE_SOURCES),
+                "kernel": "lse_combine_kernel", "kernel_ms": round(k_avg_ms, 5),
+                "peak_source": peaks["source"] + " MEASURED_PEAKS.json hbm_gbs (copy)"}
+    e2e = None
+    if not args.no_e2e:
+        h_o, h_l = w.o_parts.cpu().pin_memory(), w.lse_parts.cpu().pin_memory()
+        h_out, h_lse = torch.empty(out.shape, dtype=out.dtype).pin_memory(), torch.empty(lse.shape).pin_memory()
+        d_o, d_l = torch.empty_like(w.o_parts), torch.empty_like(w.lse_parts)
+
+        def e2e_step():
+            d_o.copy_(h_o, non_blocking=True)
+            d_l.copy_(h_l, non_blocking=True)
+            fp8pa.lse_combine(d_o, d_l, out=out, lse=lse)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(10, args.steps // 10)
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e.record(stream)
+        torch.cuda.synchronize()
+        e_ms = slowest_rank_ms(a.elapsed_time(e), world, dev)
+        e2e = {"value": round(job_rate(work, world, n_e2e, e_ms, False), 3), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h_o.numel() * 2 + h_l.numel() * 4),
+               "d2h_bytes_per_step": int(h_out.numel() * 2 + h_lse.numel() * 4), "steps": n_e2e,
+               "ms_per_step": round(e_ms / n_e2e, 5)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r, cores, desc, _t = combine_oracle_timing(synth.make_combine_config(args.config), args.cpu_budget)
+        cpu = {"value": round(r, 6), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": round(job_rate(work, world, args.steps, ms_total, False), 3), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_total / args.steps, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "parts": P, "total_q": T, "num_heads_q": hq, "head_dim": d,
+                       "bytes_per_step": work, "parallelism": f"replicas x{world}",
+                       "l2": f"inputs larger than L2: {work / 1e6:.0f} MB per step"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+            "clocks": clock_info}))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=synth.CONFIG_NAMES + synth.KV_WRITE_CONFIG_NAMES)
+    ap.add_argument("--config", default=DEFAULT_CONFIG,
+                    choices=synth.CONFIG_NAMES + synth.KV_WRITE_CONFIG_NAMES + synth.COMBINE_CONFIG_NAMES)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
@@ -664,6 +801,8 @@ def main():
         return run_reference(args)
     if args.config in synth.KV_WRITE_CONFIG_NAMES:
         return run_kv_write(args)
+    if args.config in synth.COMBINE_CONFIG_NAMES:
+        return run_combine(args)
     return run_ours(args)
 
 

@@ -411,3 +411,32 @@ def make_kv_write_config(name: str, device="cpu", copies: int = 1, seed: int = 7
     vd = float(np.float32(np.float32(value.float().abs().amax().item()) / np.float32(448.0)))
     return KVWriteWorkload(name=name, key=key.to(device), value=value.to(device), slot_mappings=maps, num_pages=pool,
                            k_descale=kd, v_descale=vd, num_heads_kv=hkv, head_dim=d)
+
+
+# ------------------------------------------------------------------ LSE-combine inputs
+
+@dataclasses.dataclass
+class CombineWorkload:
+    name: str
+    o_parts: torch.Tensor      # bf16 [P, total_q, Hq, D]
+    lse_parts: torch.Tensor    # f32 [P, Hq, total_q]
+
+    def bytes_algorithmic(self) -> int:
+        """The parts read (bf16 O and f32 LSE) and the merged row written (bf16 O, f32 LSE)."""
+        P, T, hq, d = self.o_parts.shape
+        return (P + 1) * T * hq * (2 * d + 4)
+
+
+COMBINE_CONFIG_NAMES = [
+    "lse_combine_mixed_hd512",  # two DCP shards of the hd512 mixed batch's 8128 query rows: Hq 32, D 512
+]
+
+
+def make_combine_config(name: str, device="cpu", seed: int = 11) -> CombineWorkload:
+    """Partial outputs N(0, 1) in bf16 and partial LSEs N(0, 3), two parts."""
+    P, T, hq, d = {"lse_combine_mixed_hd512": (2, 8128, 32, 512)}[name]
+    g = torch.Generator().manual_seed(seed)
+    o = torch.randn((P, T, hq, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    lse = torch.randn((P, hq, T), generator=g, dtype=torch.float32) * 3.0
+    return CombineWorkload(name=name, o_parts=o.to(device), lse_parts=lse.to(device))
+
