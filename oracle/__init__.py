@@ -59,6 +59,7 @@ class _AttnArgs(ctypes.Structure):
         ("softmax_scale", ctypes.c_float),
         ("window_left", ctypes.c_int),
         ("causal", ctypes.c_int),
+        ("sinks", ctypes.c_void_p),
     ]
 
 
@@ -194,7 +195,7 @@ class AttnProblem:
 
     def __init__(self, q, q_is_e4m3, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, num_heads_kv,
                  q_descale, k_descale, v_descale, softmax_scale, window_left=-1, causal=True,
-                 descale_batch_stride=0, descale_head_stride=0):
+                 descale_batch_stride=0, descale_head_stride=0, sinks=None):
         self.q = np.ascontiguousarray(q)
         self.q_is_e4m3 = bool(q_is_e4m3)
         assert self.q.dtype == (np.uint8 if self.q_is_e4m3 else np.uint16)
@@ -212,6 +213,10 @@ class AttnProblem:
         self.causal = bool(causal)
         self.descale_batch_stride = int(descale_batch_stride)
         self.descale_head_stride = int(descale_head_stride)
+        # per query head sink logits (natural-log units), or None
+        self.sinks = None if sinks is None else np.ascontiguousarray(sinks, dtype=np.float32)
+        if self.sinks is not None:
+            assert self.sinks.shape == (self.q.shape[1],)
 
     @property
     def total_q(self):
@@ -253,6 +258,7 @@ class AttnProblem:
         a.softmax_scale = self.softmax_scale
         a.window_left = self.window_left
         a.causal = int(self.causal)
+        a.sinks = None if self.sinks is None else self.sinks.ctypes.data
         return a
 
 

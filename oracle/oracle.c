@@ -37,6 +37,12 @@
  *    is a padding token that writes nothing, and each element is quantized like
  *    Q: E4M3_RNE_sat(fl32(x / descale)) with the per-tensor K or V descale.
  *
+ *  - Attention sinks: listed as a feature of the d512 kernel ("[Kernel]
+ *    Integrate FA4 SM90 FP8 MMA for Gemma-4 full attention", review comment
+ *    on the d512 specialization: "including sinks").  Reading used (the page
+ *    defines no formula): a per-query-head logit sink_h joins the softmax
+ *    denominator and attends to no value, o = sum_j e^{s_j} v_j /
+ *    (sum_j e^{s_j} + e^{sink_h}) and lse = ln(sum_j e^{s_j} + e^{sink_h}).
  *  - Combining attention partials by their LSE: the context call of
  *    decode-context parallelism, in which each rank attends over its shard of
  *    the keys and returns its output and LSE ("[Kernel] Integrate FA4 SM90 FP8
@@ -259,6 +265,7 @@ typedef struct {
   float softmax_scale;
   int window_left; /* < 0: no window */
   int causal;
+  const float* sinks; /* [Hq] sink logits (natural-log units), or NULL */
 } or_attn_args;
 
 /* Visible key range [*lo, *hi] of query i in a sequence with Lq queries and
@@ -330,7 +337,8 @@ static int attend_row(const or_attn_args* a, int t, int h, double* o, double* ls
   if (probs)
     for (j = 0; j < Lk; ++j) probs[j] = 0.0;
   if (!or_visible_range(Lq, Lk, i, a->window_left, a->causal, &lo, &hi)) {
-    *lse = -INFINITY;
+    /* no key: the sink alone (if any) makes up the denominator, o = 0 */
+    *lse = a->sinks ? (double)a->sinks[h] : -INFINITY;
     return 0;
   }
   load_q(a, t, h, qd);
@@ -344,8 +352,11 @@ static int attend_row(const or_attn_args* a, int t, int h, double* o, double* ls
     s[j - lo] = (double)a->softmax_scale * acc;
     if (s[j - lo] > m) m = s[j - lo];
   }
+  /* a sink is one more logit in the denominator that attends to no value */
+  if (a->sinks && (double)a->sinks[h] > m) m = (double)a->sinks[h];
   l = 0.0;
   for (j = lo; j <= hi; ++j) l += exp(s[j - lo] - m);
+  if (a->sinks) l += exp((double)a->sinks[h] - m);
   for (j = lo; j <= hi; ++j) {
     int64_t off = kv_row_offset(a, b, j, hk);
     double w = exp(s[j - lo] - m) / l;

@@ -669,3 +669,55 @@ def test_lse_combine_is_independent_of_part_order():
     p = [2, 0, 3, 1]
     b = oracle.lse_combine(o[p], l[p])
     assert np.allclose(a[0], b[0], rtol=0, atol=1e-12) and np.allclose(a[1], b[1], rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ attention sinks
+
+def _sink_problem(seed, sinks, lq=(3, 1, 4), lk=(70, 1, 130), window_left=-1, causal=True):
+    rng = np.random.default_rng(seed)
+    hkv, G, d = 2, 2, 16
+    kl = [rng.choice(FINITE[FINITE < 0x70], size=(n, hkv, d)) for n in lk]
+    vl = [rng.choice(FINITE[FINITE < 0x70], size=(n, hkv, d)) for n in lk]
+    kc, vc, bt = paged_from_logical(kl, vl, list(lk), np.random.default_rng(seed + 1))
+    q = _to_bf16_bits(rng.normal(size=(sum(lq), hkv * G, d)))
+    return oracle.AttnProblem(q=q, q_is_e4m3=False, k_cache=kc, v_cache=vc, block_table=bt,
+                              cu_seqlens_q=cu_from_lq(list(lq)), seqused_k=np.array(lk, np.int32), num_heads_kv=hkv,
+                              q_descale=1.0, k_descale=0.5, v_descale=0.25, softmax_scale=0.3,
+                              window_left=window_left, causal=causal, sinks=sinks)
+
+
+def test_sinks_at_minus_inf_change_nothing():
+    a = oracle.paged_attention(_sink_problem(41, None))
+    b = oracle.paged_attention(_sink_problem(41, np.full(4, -np.inf, np.float32)))
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_sink_is_an_extra_logit_with_no_value():
+    # o_sink = o * exp(lse - lse_sink), lse_sink = ln(exp(lse) + exp(sink)), row by row
+    sinks = np.array([0.5, -2.0, 3.0, 8.0], np.float32)
+    o, lse = oracle.paged_attention(_sink_problem(42, None))
+    os_, lses = oracle.paged_attention(_sink_problem(42, sinks))
+    want_lse = np.logaddexp(lse, sinks[:, None].astype(np.float64))
+    assert np.allclose(lses, want_lse, rtol=0, atol=1e-12)
+    assert np.allclose(os_, o * np.exp(lse - want_lse).T[:, :, None], rtol=0, atol=1e-12)
+
+
+def test_sink_closed_form_single_key():
+    # one visible key with logit s0 (= the sinkless lse) and value v0 (= the sinkless output):
+    # o = v0 * sigmoid(s0 - c), lse = ln(e^s0 + e^c)
+    sinks = np.array([1.0, -1.0, 0.0, 2.5], np.float32)
+    o, lse = oracle.paged_attention(_sink_problem(43, None, lq=(1,), lk=(1,), causal=False))
+    os_, lses = oracle.paged_attention(_sink_problem(43, sinks, lq=(1,), lk=(1,), causal=False))
+    c = sinks.astype(np.float64)
+    s0 = lse[:, 0]
+    sig = 1.0 / (1.0 + np.exp(c - s0))
+    assert np.allclose(lses[:, 0], np.log(np.exp(s0) + np.exp(c)), rtol=0, atol=1e-12)
+    assert np.allclose(os_[0], o[0] * sig[:, None], rtol=0, atol=1e-12)
+
+
+def test_sink_on_a_row_with_no_visible_key():
+    # window_left = 0 and a query before every key: nothing visible, o = 0 and lse = sink
+    sinks = np.array([0.25, -3.0, 1.5, 0.0], np.float32)
+    prob = _sink_problem(44, sinks, lq=(2,), lk=(1,), causal=True)
+    o, lse = oracle.paged_attention(prob)
+    assert np.all(o[0] == 0) and np.array_equal(lse[:, 0], sinks.astype(np.float64))
