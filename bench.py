@@ -401,12 +401,15 @@ def run_ours(args):
         l2_note = (f"inputs larger than L2: {per_copy / 1e6:.0f} MB of cache, Q and outputs, "
                    f"{w.kv_bytes_algorithmic() / 1e6:.0f} MB of K/V read per step, {l2_bytes / 1e6:.0f} MB L2")
 
+    # attention sinks (one logit per query head), drawn N(0, 1), when asked for
+    sinks = (torch.randn(hq, generator=torch.Generator().manual_seed(3)).to(dev) if args.sinks else None)
+
     def step(q_src, bt, cu, su, o, l, r=0):
         kc, vc = kv_rot[r % n_rot]
         q = fp8pa.quantize_q_fp8(q_src, qd, out=q8) if w.fp8_q else q_src
         fp8pa.fp8_paged_attn_fwd(q, kc, vc, bt, cu, su, w.max_seqlen_q, qd, kd, vd,
                                  w.softmax_scale, w.window_left, w.causal, num_splits=ns_arg, out=o, lse=l,
-                                 workspace=workspace)
+                                 workspace=workspace, sinks=sinks)
 
     def args_dev(i):
         o, l = ol_rot[i % n_rot]
@@ -551,7 +554,7 @@ def run_ours(args):
                        "num_heads_kv": hkv, "head_dim": D, "window_left": w.window_left, "causal": w.causal,
                        "q": "e4m3" if w.fp8_q else "bf16", "kv": "e4m3, 64-token pages", "num_splits": splits,
                        "kv_bytes_per_step": kv_bytes, "parallelism": f"replicas x{world}",
-                       "l2": l2_note},
+                       "l2": l2_note, "sinks": bool(args.sinks)},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -794,6 +797,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ctas-per-sm", type=int, default=0, help="force 1 or 2 attention CTAs per SM (0 = auto)")
     ap.add_argument("--num-splits", type=int, default=0, help="split-KV count (0 = automatic)")
+    ap.add_argument("--sinks", action="store_true", help="attention sinks, one logit per query head")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

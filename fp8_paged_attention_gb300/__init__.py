@@ -82,6 +82,8 @@ def load_library():
             c.c_int, c.c_float, c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_size_t, c.c_void_p, c.c_void_p,
             c.c_void_p,
         ]
+        lib.fp8_paged_attn_fwd_sinks.restype = c.c_int
+        lib.fp8_paged_attn_fwd_sinks.argtypes = lib.fp8_paged_attn_fwd.argtypes[:-1] + [c.c_void_p, c.c_void_p]
         lib.fp8_paged_attn_fwd_noalloc.restype = c.c_int
         lib.fp8_paged_attn_fwd_noalloc.argtypes = [
             c.c_void_p, c.c_int, c.c_void_p, c.c_void_p, c.c_int, c.c_void_p, c.c_int, c.c_void_p, c.c_void_p,
@@ -234,12 +236,13 @@ def kv_cache_write(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor
 def fp8_paged_attn_fwd(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q, q_descale,
                        k_descale, v_descale, softmax_scale, window_left=-1, causal=True, num_splits=0,
                        out=None, lse=None, workspace=None, descale_batch_stride=0, descale_head_stride=0,
-                       stream=None, return_lse=True):
+                       stream=None, return_lse=True, sinks=None):
     """Attention over a paged E4M3 KV cache.
 
     q: [total_q, Hq, D] bf16, or uint8 E4M3 codes (FP8-MMA path);
     k_cache, v_cache: uint8 [num_pages, 64, Hkv, D]; block_table int32 [B, max_pages];
-    cu_seqlens_q int32 [B+1]; seqused_k int32 [B]; descales: f32 device tensors.
+    cu_seqlens_q int32 [B+1]; seqused_k int32 [B]; descales: f32 device tensors;
+    sinks: optional f32 [Hq] device tensor of per-head sink logits (fp8_paged_attn_fwd_sinks).
     Returns (out bf16 [total_q, Hq, D], lse f32 [Hq, total_q] or None).
     """
     lib = load_library()
@@ -265,12 +268,17 @@ def fp8_paged_attn_fwd(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k
                     ("cu_seqlens_q", cu_seqlens_q), ("seqused_k", seqused_k), ("out", out)):
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
-    _check(lib.fp8_paged_attn_fwd(
-        _ptr(q), q_dtype, _ptr(k_cache), _ptr(v_cache), num_pages, _ptr(block_table), max_pages,
-        _ptr(cu_seqlens_q), _ptr(seqused_k), batch, total_q, max_seqlen_q, hq, hkv, d, _ptr(q_descale),
-        _ptr(k_descale), _ptr(v_descale), descale_batch_stride, descale_head_stride, float(softmax_scale),
-        int(window_left), int(bool(causal)), int(num_splits), _ptr(workspace), workspace.numel(), _ptr(out),
-        _ptr(lse), _stream_ptr(stream)))
+    args = (_ptr(q), q_dtype, _ptr(k_cache), _ptr(v_cache), num_pages, _ptr(block_table), max_pages,
+            _ptr(cu_seqlens_q), _ptr(seqused_k), batch, total_q, max_seqlen_q, hq, hkv, d, _ptr(q_descale),
+            _ptr(k_descale), _ptr(v_descale), descale_batch_stride, descale_head_stride, float(softmax_scale),
+            int(window_left), int(bool(causal)), int(num_splits), _ptr(workspace), workspace.numel(), _ptr(out),
+            _ptr(lse))
+    if sinks is None:
+        _check(lib.fp8_paged_attn_fwd(*args, _stream_ptr(stream)))
+    else:
+        if sinks.dtype != torch.float32 or not sinks.is_cuda or sinks.numel() != hq or not sinks.is_contiguous():
+            raise ValueError("sinks must be a contiguous CUDA float32 tensor of num_heads_q entries")
+        _check(lib.fp8_paged_attn_fwd_sinks(*args, _ptr(sinks), _stream_ptr(stream)))
     return out, lse
 
 

@@ -373,13 +373,15 @@ int fp8pa_num_splits(int batch, int total_q, int max_seqlen_q, int num_heads_q, 
   return pl.splits;
 }
 
-int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* v_cache, int num_pages,
-                       const int32_t* block_table, int max_pages_per_seq, const int32_t* cu_seqlens_q,
-                       const int32_t* seqused_k, int batch, int total_q, int max_seqlen_q, int num_heads_q,
-                       int num_heads_kv, int head_dim, const float* q_descale, const float* k_descale,
-                       const float* v_descale, int descale_batch_stride, int descale_head_stride,
-                       float softmax_scale, int window_left, int causal, int num_splits, void* workspace,
-                       size_t workspace_bytes, void* out, float* lse, fp8pa_stream_t stream) {
+namespace {
+
+int fwd_impl(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* v_cache, int num_pages,
+             const int32_t* block_table, int max_pages_per_seq, const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+             int batch, int total_q, int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
+             const float* q_descale, const float* k_descale, const float* v_descale, int descale_batch_stride,
+             int descale_head_stride, float softmax_scale, int window_left, int causal, int num_splits,
+             void* workspace, size_t workspace_bytes, void* out, float* lse, const float* sinks,
+             fp8pa_stream_t stream) {
   const bool fp8_q = q_dtype == FP8PA_E4M3;
   CallPlan pl;
   int rc = make_plan(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_dtype, max_pages_per_seq,
@@ -472,6 +474,7 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
   p.lse = lse;
   p.o_part = reinterpret_cast<float*>(ws + pl.off_opart);
   p.lse_part = reinterpret_cast<float*>(ws + pl.off_lsepart);
+  p.sinks = sinks;
   p.status = status;
   const unsigned wl = g_wait_limit.load();
   p.wait_limit = wl ? wl : kDefaultWaitLimit;
@@ -511,10 +514,42 @@ int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const
     cp.lse_part = p.lse_part;
     cp.out = out;
     cp.lse = lse;
+    cp.sinks = sinks;
     e = launch_combine(cp, st);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   }
   return FP8PA_OK;
+}
+
+}  // namespace
+
+int fp8_paged_attn_fwd(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* v_cache, int num_pages,
+                       const int32_t* block_table, int max_pages_per_seq, const int32_t* cu_seqlens_q,
+                       const int32_t* seqused_k, int batch, int total_q, int max_seqlen_q, int num_heads_q,
+                       int num_heads_kv, int head_dim, const float* q_descale, const float* k_descale,
+                       const float* v_descale, int descale_batch_stride, int descale_head_stride,
+                       float softmax_scale, int window_left, int causal, int num_splits, void* workspace,
+                       size_t workspace_bytes, void* out, float* lse, fp8pa_stream_t stream) {
+  return fwd_impl(q, q_dtype, k_cache, v_cache, num_pages, block_table, max_pages_per_seq, cu_seqlens_q, seqused_k,
+                  batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_descale, k_descale, v_descale,
+                  descale_batch_stride, descale_head_stride, softmax_scale, window_left, causal, num_splits, workspace,
+                  workspace_bytes, out, lse, nullptr, stream);
+}
+
+int fp8_paged_attn_fwd_sinks(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* v_cache,
+                             int num_pages, const int32_t* block_table, int max_pages_per_seq,
+                             const int32_t* cu_seqlens_q, const int32_t* seqused_k, int batch, int total_q,
+                             int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim, const float* q_descale,
+                             const float* k_descale, const float* v_descale, int descale_batch_stride,
+                             int descale_head_stride, float softmax_scale, int window_left, int causal,
+                             int num_splits, void* workspace, size_t workspace_bytes, void* out, float* lse,
+                             const float* sinks, fp8pa_stream_t stream) {
+  if (!sinks && batch > 0 && total_q > 0) return fail(FP8PA_EINVAL, "fp8_paged_attn_fwd_sinks: null sinks");
+  if (sinks && !aligned(sinks, 4)) return fail(FP8PA_EINVAL, "sinks must be 4-byte aligned");
+  return fwd_impl(q, q_dtype, k_cache, v_cache, num_pages, block_table, max_pages_per_seq, cu_seqlens_q, seqused_k,
+                  batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_descale, k_descale, v_descale,
+                  descale_batch_stride, descale_head_stride, softmax_scale, window_left, causal, num_splits, workspace,
+                  workspace_bytes, out, lse, sinks, stream);
 }
 
 int fp8pa_get_device_status(unsigned int* host_status, fp8pa_stream_t stream) {

@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           if (split_out)
             p.lse_part[(size_t)it.split * p.hq * p.total_q + li] = NEG_INF;
           else if (p.lse)
-            p.lse[li] = NEG_INF;
+            p.lse[li] = p.sinks ? p.sinks[row_head(n)] : NEG_INF;  // only the sink is left
         }
         continue;
       }
@@ -917,7 +917,14 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         const long long row = (long long)tok * p.hq + head;
         inv_s[n] = l > 0.f ? vd / l : 0.f;
         ooff_s[n] = (split_out ? (long long)it.split * p.total_q * p.hq + row : row) * D;
-        const float lse = l > 0.f ? (m_s[n] - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+        float lse = l > 0.f ? (m_s[n] - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+        if (p.sinks && !split_out) {
+          // the sink joins the denominator here; split partials get it in the combine
+          float inv, lse2;
+          fold_sink(l, m_s[n] - C::kPShift, p.sinks[head] * 1.4426950408889634f, vd, inv, lse2);
+          inv_s[n] = inv;
+          lse = lse2 * 0.69314718055994531f;
+        }
         const size_t li = (size_t)head * p.total_q + tok;
         if (split_out)
           p.lse_part[(size_t)it.split * p.hq * p.total_q + li] = lse;

@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         if (live) {
           uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * D + dbase);
           for (int i = 0; i < HO / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
-          if (p.lse && it.dhalf == 0 && hw == 0) p.lse[li] = NEG_INF;
+          if (p.lse && it.dhalf == 0 && hw == 0) p.lse[li] = p.sinks ? p.sinks[head] : NEG_INF;
         }
         continue;
       }
@@ -519,7 +519,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       if (pair_fail(eok)) break;
       tc_fence_after();
       const float l = lsum[r] + lsum[128 + r];
-      const float inv = l > 0.f ? vd / l : 0.f;
+      float inv = l > 0.f ? vd / l : 0.f;
+      float lse2 = l > 0.f ? m - C::kPShift + __log2f(l) : NEG_INF;
+      if (p.sinks && live) fold_sink(l, m - C::kPShift, p.sinks[head] * 1.4426950408889634f, vd, inv, lse2);
       // Each 32-column chunk of this warp's 32 rows goes through a 2 KB staging
       // buffer (row-major, 16-byte pieces swizzled by (row >> 1) & 3), then out as
       // 64-byte row segments: lane l stores piece l & 3 of row i * 8 + l / 4.
@@ -562,8 +564,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           __syncwarp();
         }
       }
-      if (live && p.lse && it.dhalf == 0 && hw == 0)
-        p.lse[li] = l > 0.f ? (m - C::kPShift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+      if (live && p.lse && it.dhalf == 0 && hw == 0) p.lse[li] = lse2 * 0.69314718055994531f;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_empty);

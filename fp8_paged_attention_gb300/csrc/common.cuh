@@ -50,6 +50,7 @@ struct AttnParams {
   float* lse;       // [hq][total_q] or null
   float* o_part;    // f32 [splits][total_q][hq][D]
   float* lse_part;  // f32 [splits][hq][total_q]
+  const float* sinks;  // [hq] sink logits (natural log), or null; folded in where a row is finished
   // plan
   ClassInfo cls;
   const int4* work;        // items of this class
@@ -59,6 +60,31 @@ struct AttnParams {
   uint32_t wait_limit;
   int inject_stall;  // test hook: the MMA issuer first waits on a barrier that nothing arrives on
 };
+
+// A finished row's normalization with an attention sink: a per-head logit in
+// the softmax denominator that attends to no value.  l = sum_j 2^(s2_j - m2)
+// over the row's keys (log2 units, s2 = score * log2(e)), sink2 = sink * log2(e).
+// inv = vd / (l + 2^(sink2 - m2)), lse2 = log2 of the whole denominator (log2
+// units); a row with no key gets inv = 0 and lse2 = sink2.  No overflow for any
+// m2 and sink2; a sink at -inf leaves inv = vd / l and lse2 = m2 + log2(l).
+__device__ __forceinline__ void fold_sink(float l, float m2, float sink2, float vd, float& inv, float& lse2) {
+  if (!(l > 0.f)) {
+    inv = 0.f;
+    lse2 = sink2;
+    return;
+  }
+  const float a = sink2 - m2;
+  if (a <= 64.f) {
+    const float lt = l + exp2f(a);
+    inv = vd / lt;
+    lse2 = m2 + __log2f(lt);
+  } else {
+    const float r = exp2f(-a);
+    const float lt = fmaf(l, r, 1.0f);
+    inv = vd * r / lt;
+    lse2 = sink2 + __log2f(lt);
+  }
+}
 
 // Visible key range of query i of a sequence (Lq queries, Lk keys); hi < lo when empty.
 __host__ __device__ __forceinline__ void visible_range(int Lq, int Lk, int i, int window_left, int causal, int& lo,

@@ -27,6 +27,7 @@ struct CombineParams {
   const float* lse_part;
   void* out;
   float* lse;
+  const float* sinks;  // [hq] sink logits (natural log), or null
 };
 
 cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream);

@@ -9,8 +9,9 @@
 // shared prefix the same pages again a few sequences later, while still in L2.
 //
 // combine_kernel merges the per-split partial outputs with their log-sum-exps:
-//   L = log sum_s exp(lse_s),  out = sum_s exp(lse_s - L) * O_s
-// Splits that saw no key carry lse = -inf and weigh nothing.
+//   L = log (sum_s exp(lse_s) + exp(sink)),  out = sum_s exp(lse_s - L) * O_s
+// Splits that saw no key carry lse = -inf and weigh nothing; without a sink its
+// term is absent.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -180,7 +181,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(CombinePara
     const int s = lane + 32 * k;
     lse_s[k] = s < ns ? cp.lse_part[(size_t)s * plane + (size_t)h * cp.total_q + t] : NEG_INF;
   }
-  float mx = fmaxf(lse_s[0], lse_s[1]);
+  // a sink joins the denominator as one more term that carries no value
+  const float sink = cp.sinks ? cp.sinks[h] : NEG_INF;
+  float mx = fmaxf(fmaxf(lse_s[0], lse_s[1]), sink);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
   float sum = 0.f;
@@ -191,6 +194,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(CombinePara
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  if (sink != NEG_INF) sum += expf(sink - mx);
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
   const float L = (mx == NEG_INF) ? NEG_INF : mx + logf(sum);
   const size_t rbase = (size_t)t * cp.hq + h;

@@ -106,6 +106,28 @@ int fp8pa_kv_cache_write(const void* key, const void* value, long long key_token
                          const float* k_descale, const float* v_descale, fp8pa_stream_t stream);
 
 /*
+ * fp8_paged_attn_fwd_sinks — fp8_paged_attn_fwd with attention sinks (a
+ * feature of the d512 kernel in the review of "[Kernel] Integrate FA4 SM90 FP8
+ * MMA for Gemma-4 full attention": "including sinks").  Every argument is that
+ * of fp8_paged_attn_fwd; sinks: f32 [num_heads_q] on the device, natural-log
+ * units, not null.  Query head h's sink is one more logit in its softmax
+ * denominator that attends to no value:
+ *   out = sum_j e^{s_j} v_j / (sum_j e^{s_j} + e^{sinks[h]}),
+ *   lse = ln(sum_j e^{s_j} + e^{sinks[h]});
+ * a row with no visible key gets out = 0 and lse = sinks[h].  A sink of -inf
+ * gives the results of fp8_paged_attn_fwd.  Errors: those of
+ * fp8_paged_attn_fwd, and EINVAL for null or misaligned sinks.
+ */
+int fp8_paged_attn_fwd_sinks(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* v_cache,
+                             int num_pages, const int32_t* block_table, int max_pages_per_seq,
+                             const int32_t* cu_seqlens_q, const int32_t* seqused_k, int batch, int total_q,
+                             int max_seqlen_q, int num_heads_q, int num_heads_kv, int head_dim, const float* q_descale,
+                             const float* k_descale, const float* v_descale, int descale_batch_stride,
+                             int descale_head_stride, float softmax_scale, int window_left, int causal,
+                             int num_splits, void* workspace, size_t workspace_bytes, void* out, float* lse,
+                             const float* sinks, fp8pa_stream_t stream);
+
+/*
  * fp8pa_lse_combine — merge attention partials computed over disjoint key
  * shards, as the context call of decode-context parallelism returns them (the
  * pages' review thread on DCP: each rank runs the non-causal context call over
