@@ -392,8 +392,8 @@ int fwd_impl(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* 
   if (descale_batch_stride < 0 || descale_head_stride < 0) return fail(FP8PA_EINVAL, "descale strides must be >= 0");
   if (batch == 0 || total_q == 0) return FP8PA_OK;
   if (num_pages < 1) return fail(FP8PA_EINVAL, "num_pages must be >= 1 (got %d)", num_pages);
-  if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !seqused_k || !k_descale || !v_descale || !out ||
-      (fp8_q && !q_descale))
+  // null descales are the unit scale (no descale read)
+  if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !seqused_k || !out)
     return fail(FP8PA_EINVAL, "null pointer argument");
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
     return fail(FP8PA_EINVAL, "q, k_cache, v_cache and out must be 16-byte aligned");

@@ -232,8 +232,9 @@ __device__ __forceinline__ int page_id(const AttnParams& p, const Item& it, int 
   return phys;
 }
 
+// A null descale pointer is the unit scale: nothing is read.
 __device__ __forceinline__ float load_descale(const float* d, const AttnParams& p, const Item& it) {
-  return d[(size_t)it.b * p.descale_b + (size_t)it.hk * p.descale_h];
+  return d ? d[(size_t)it.b * p.descale_b + (size_t)it.hk * p.descale_h] : 1.0f;
 }
 
 // Stage position of V tile u (0-based within the item) in the item's stream
@@ -673,7 +674,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       const int n_t = it.t1 - it.t0;
       const float kd = load_descale(p.k_descale, p, it);
       const float vd = load_descale(p.v_descale, p, it);
-      const float scale = p.softmax_scale_log2 * kd * (kQ8 ? *p.q_descale : 1.0f);
+      const float scale = p.softmax_scale_log2 * kd * (kQ8 && p.q_descale ? *p.q_descale : 1.0f);
       if (wt < NR) {
         m_s[r0 + wt] = NEG_INF;
         a_s[r0 + wt] = 1.0f;

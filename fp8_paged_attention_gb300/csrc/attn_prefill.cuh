@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       const int n = it.t1 - it.t0;
       const float kd = load_descale(p.k_descale, p, it);
       const float vd = load_descale(p.v_descale, p, it);
-      const float scale = p.softmax_scale_log2 * kd * *p.q_descale;
+      const float scale = p.softmax_scale_log2 * kd * (p.q_descale ? *p.q_descale : 1.0f);
       // this row's visible keys [lo_r, hi_r]; an empty range for padding rows
       const int pq = it.Lk - it.Lq + (it.row0 + r) / G;
       int lo_r = p.window_left >= 0 ? max(0, pq - p.window_left) : 0;

@@ -231,7 +231,8 @@ int fp8pa_num_splits(int batch, int total_q, int max_seqlen_q, int num_heads_q, 
  *   An empty J gives out = 0 and lse = -inf.
  * q_descale: one f32 (per tensor; read only on the E4M3-Q path).  k_descale,
  * v_descale: f32 read at b * descale_batch_stride + hk * descale_head_stride
- * (0, 0 = per tensor).
+ * (0, 0 = per tensor).  A NULL descale pointer is the unit scale 1.0 and is
+ * never read (the no-descale fast path for caches stored without scaling).
  *
  * Support: head_dim 256 with E4M3 Q; head_dim 512 with BF16 Q (K/V dequantized
  * in-kernel, BF16 MMA) or E4M3 Q (FP8 MMA).  V head dim = head_dim.  num_heads_q

@@ -61,3 +61,20 @@ def test_sinks_at_minus_inf_are_bit_identical_to_no_sinks(name):
     a, la = _run(w, None, ns)
     b, lb = _run(w, torch.full((hq,), -float("inf"), dtype=torch.float32, device="cuda"), ns)
     assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+@pytest.mark.parametrize("name", ["decode_hd256", "decode_hd256_split", "decode_hd512_bf16", "prefill_hd256_fp8",
+                                  "prefill_hd512_fp8", "prefill_hd512_bf16"])
+def test_null_descales_are_the_unit_scale(name):
+    # the no-descale fast path: null q/k/v descales give the bits of descale tensors holding 1.0
+    import fp8_paged_attention_gb300 as fp8pa
+    lq, lk, hq, hkv, d, wl, causal, fp8_q, ns = CASES[name]
+    w = synth.make_workload(name, lq, lk, hq, hkv, d, wl, causal, fp8_q, seed=54, device="cuda")
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    q = fp8pa.quantize_q_fp8(w.q, torch.tensor([w.q_descale], device="cuda")) if fp8_q else w.q
+    scale = w.softmax_scale * 0.05  # codes read at unit scale are large: keep the logits moderate
+    common = (q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q, w.seqused_k, w.max_seqlen_q)
+    a, la = fp8pa.fp8_paged_attn_fwd(*common, one, one, one, scale, w.window_left, w.causal, num_splits=ns)
+    b, lb = fp8pa.fp8_paged_attn_fwd(*common, None, None, None, scale, w.window_left, w.causal, num_splits=ns)
+    assert torch.equal(a, b) and torch.equal(la, lb)
+    assert torch.isfinite(a.float()).all()
