@@ -55,8 +55,11 @@ __global__ void __launch_bounds__(32 * kWarps) kv_cache_write_kernel(
       const uint4* src = reinterpret_cast<const uint4*>(is_v ? value + t * value_stride : key + t * key_stride);
       uint2* dst = reinterpret_cast<uint2*>((is_v ? v_cache : k_cache) + sl * (long long)row_vecs * 8);
       const float d = is_v ? dv : dk, r = is_v ? rv : rk;
-      auto q2 = [&](uint32_t w) { return fast ? quant::fast_pair(w, r, d) : quant::exact_pair(w, d); };
-      auto q8 = [&](uint4 a) { return make_uint2(q2(a.x) | (q2(a.y) << 16), q2(a.z) | (q2(a.w) << 16)); };
+      auto q8 = [&](uint4 a) {
+        if (fast) return quant::fast8(a, r, d);
+        return make_uint2(quant::exact_pair(a.x, d) | (quant::exact_pair(a.y, d) << 16),
+                          quant::exact_pair(a.z, d) | (quant::exact_pair(a.w, d) << 16));
+      };
       for (int c0 = lane; c0 < row_vecs; c0 += 32 * kPerLane) {
         uint4 a[kPerLane];
 #pragma unroll

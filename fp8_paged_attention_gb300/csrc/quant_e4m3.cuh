@@ -51,5 +51,28 @@ __device__ __forceinline__ uint32_t fast_pair(uint32_t w, float r, float d) {
   return exact_pair(w, d);
 }
 
+// Eight bf16 values (one 16-byte vector) -> eight codes, low byte first.  The
+// checks of fast_pair are made once per vector: the two brackets' codes are
+// compared as two packed words, and NaN inputs are found on the bf16 bits
+// (exponent all ones, mantissa not zero).  A vector that is not settled that
+// way takes the exact form for all its elements.
+__device__ __forceinline__ uint2 fast8(uint4 v, float r, float d) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const float dn = 1.0f - 0x1p-21f, up = 1.0f + 0x1p-21f;
+  uint32_t lo[2] = {0, 0}, hi[2] = {0, 0};
+  uint32_t nan = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 q = __fmul2_rn(make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u)),
+                                make_float2(r, r));
+    const float2 a = __fmul2_rn(q, make_float2(dn, dn)), b = __fmul2_rn(q, make_float2(up, up));
+    lo[k >> 1] |= cvt_pair(a.x, a.y) << (16 * (k & 1));
+    hi[k >> 1] |= cvt_pair(b.x, b.y) << (16 * (k & 1));
+    nan |= __vcmpgtu2(w[k] & 0x7FFF7FFFu, 0x7F807F80u);
+  }
+  if (lo[0] == hi[0] && lo[1] == hi[1] && nan == 0) return make_uint2(lo[0], lo[1]);
+  return make_uint2(exact_pair(w[0], d) | (exact_pair(w[1], d) << 16), exact_pair(w[2], d) | (exact_pair(w[3], d) << 16));
+}
+
 }  // namespace quant
 }  // namespace fp8pa

@@ -21,8 +21,11 @@ __global__ void quantize_q_vec8(const uint4* __restrict__ q, uint2* __restrict__
   const bool fast = quant::fast_ok(d);
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
     const uint4 v = q[i];
-    auto q2 = [&](uint32_t w) { return fast ? quant::fast_pair(w, r, d) : quant::exact_pair(w, d); };
-    out[i] = make_uint2(q2(v.x) | (q2(v.y) << 16), q2(v.z) | (q2(v.w) << 16));
+    if (fast)
+      out[i] = quant::fast8(v, r, d);
+    else
+      out[i] = make_uint2(quant::exact_pair(v.x, d) | (quant::exact_pair(v.y, d) << 16),
+                          quant::exact_pair(v.z, d) | (quant::exact_pair(v.w, d) << 16));
   }
   // Let the next kernel (the forward's plan) launch only as this grid drains:
   // launched earlier, the attention grid behind it would take SM room from the
