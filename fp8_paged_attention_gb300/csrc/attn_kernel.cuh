@@ -899,17 +899,13 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       if (aborted) break;
       sbase += (kSplit ? 1 : 2) * n_t * DC;
       // ---------------- epilogue: O / l, lse
-      bool ok = pwait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, lim, abort_flag);
-      ok = __all_sync(0xFFFFFFFFu, ok);
+      // The row sums, scales and lse do not depend on O: they are formed while
+      // the item's last PV completes, and only the O read waits for it.
       {
         const float rs = transpose_sum(lt, lane);  // this warp's sum for row (lane mod NR)
         if (lane < NR) lred[quarter * N + r0 + lane] = rs;
       }
-      if (!ok) flag_timeout(p, abort_flag);
-      if (bar_red_or(bar_a, 128, !ok)) {
-        aborted = true;
-        break;
-      }
+      named_bar_sync(bar_a, 128);
       // row owners: output scale vd / l, output offset and lse, once per row
       if (wt < nr) {
         const int n = r0 + wt;
@@ -932,7 +928,13 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         else if (p.lse)
           p.lse[li] = lse;
       }
-      named_bar_sync(bar_b, 128);
+      bool ok = pwait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, lim, abort_flag);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) flag_timeout(p, abort_flag);
+      if (bar_red_or(bar_b, 128, !ok)) {  // also publishes the row owners' scales and offsets
+        aborted = true;
+        break;
+      }
       tc_fence_after();
       // O^T columns of this warpgroup's rows, 16 (or 32) at a time, scaled and stored
       auto store_rows = [&](const uint32_t* r, int cc, int cnt, int d) {
