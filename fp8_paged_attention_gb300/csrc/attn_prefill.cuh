@@ -22,9 +22,9 @@
 // work item of its own: both compute the full S and P, each accumulates O for
 // its slice against that slice of V.
 //
-// Warps: 0 TMA producer, 1 QK^T issuer (and TMEM owner), 2 PV issuer, 3-10
-// softmax / O correction / epilogue in two warpgroups (a pair of warps per row
-// quarter, each thread half of a row's keys and output dims).  The producer and
+// Warps: 0 TMA producer, 1 QK^T issuer (and TMEM owner), 2 PV issuer, then
+// softmax / O correction / epilogue in kSW warpgroups (kSW warps per row
+// quarter, each thread 1 / kSW of a row's keys and output dims).  The producer and
 // the issuers run warp-uniform loops with one elected lane issuing; they and the
 // softmax warps synchronize only through mbarriers.
 #pragma once
@@ -82,10 +82,17 @@ struct PrefillCfg {
   static constexpr int kVStageBytes = kVC * kStageBytes;  // 128 keys x kDO bytes, chunk c at c * 16 KB
   static constexpr int kKStages = D == 256 ? 3 : 4;
   static constexpr int kVStages = 2;
-  static constexpr int kThreads = 11 * 32;  // producer, 2 issuers, 2 softmax warpgroups
+  static constexpr int kSW = 2;                          // softmax warpgroups: each takes 128 / kSW keys of a row
+  static constexpr int kKT = kTileKeys / kSW;            // keys of a tile per softmax thread
+  static constexpr int kHO = kDO / kSW;                  // output dims per softmax thread
+  static constexpr int kOC = kSW == 2 ? 64 : 32;         // O columns per TMEM load in the correction and epilogue
+  static constexpr bool kVWarp = true;                   // V loaded by a warp of its own (else by the producer)
+  static constexpr int kSm0 = kVWarp ? 4 : 3;            // first softmax warp
+  static constexpr int kThreads = (kSm0 + 4 * kSW) * 32; // producer(s), 2 issuers, kSW softmax warpgroups
   static constexpr int kCtrlBytes = 1024;
-  static constexpr int kXchgBytes = 3 * 1024;       // pair exchange: half maxima [2][2][128], row sums [2][128]
-  static constexpr int kOStageBytes = 8 * 32 * 64;  // epilogue: 32 rows x 64 bytes per softmax warp
+  static constexpr int kXchgBytes = 3 * kSW * 512;       // row-group exchange: maxima [2][kSW][128], sums [kSW][128]
+  static constexpr int kSeg = kSW == 2 ? 64 : 32;        // epilogue row segment (bytes) per staging pass
+  static constexpr int kOStageBytes = 4 * kSW * 32 * kSeg;  // epilogue: 32 rows x kSeg bytes per softmax warp
   static constexpr int kSmemBytes = kQBufs * kQBytes + kKStages * kKStageBytes + kVStages * kVStageBytes +
                                     kOStageBytes + kXchgBytes + kCtrlBytes + 1024;
   static_assert(kSmemBytes <= 232448, "smem");
@@ -122,8 +129,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   uint64_t* q_empty = q_full + QB;
   uint64_t* s_full = q_empty + QB;  // [2] QK^T done: S buffer readable
   uint64_t* s_free = s_full + 2;    // [2] PV done: S/P buffer reusable, O up to date
-  uint64_t* p_full = s_free + 2;    // [2] P written (eight softmax warps)
-  uint64_t* o_empty = p_full + 2;   // epilogue read O (eight softmax warps)
+  uint64_t* p_full = s_free + 2;    // [2] P written (every softmax warp)
+  uint64_t* o_empty = p_full + 2;   // epilogue read O (every softmax warp)
   uint64_t* v_ready = o_empty + 1;  // tail tile: its V stage landed (PV issuer -> softmax)
   uint64_t* drain = v_ready + 1;    // [2] one per issuer
   uint64_t* never = drain + 2;      // nothing arrives on it: the stall-injection hook waits here
@@ -150,15 +157,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 1);
-      mbar_init(&p_full[i], 8);
+      mbar_init(&p_full[i], 4 * C::kSW);
       mbar_init(&drain[i], 1);
     }
-    mbar_init(o_empty, 8);
+    mbar_init(o_empty, 4 * C::kSW);
     mbar_init(v_ready, 1);
     mbar_init(never, 1);
     for (int i = 0; i < kItemSlots; ++i) {
       mbar_init(&item_full[i], 1);
-      mbar_init(&item_empty[i], 2 + 8);  // two issuers, eight softmax warps
+      mbar_init(&item_empty[i], C::kSm0 - 1 + 4 * C::kSW);  // issuers, V loader, every softmax warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   const int n_items = *p.work_count;
   const uint32_t lim = p.wait_limit;
 
-  if (warp <= 2) {
+  if (warp < C::kSm0) {
     // ---------------------------------------------------------------- producer and MMA issuers
     const bool leader = elect_one();
     const int leader_lane = __ffs(__ballot_sync(0xFFFFFFFFu, leader)) - 1;
@@ -218,8 +225,42 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       const int qb = qit % QB;
       const uint32_t qpar = (qit / QB) & 1;
       ++qit;
+      auto load_k = [&](int u) -> bool {
+        const int pg = it.pg_lo + 2 * (it.t0 + u);
+        const int pa = page_id(p, it, pg), pb = page_id(p, it, pg + 1);
+        for (int c = 0; c < DC; ++c) {
+          const uint32_t slot = kq % SK;
+          if (!wait_all(&k_empty[slot], ((kq / SK) & 1) ^ 1)) return false;
+          if (leader) {
+            uint8_t* dst = kring + slot * C::kKStageBytes;
+            mbar_arrive_expect_tx(&k_full[slot], C::kKStageBytes);
+            tma_load_4d(dst, &tm_k, &k_full[slot], c * 128, it.hk, 0, pa);
+            tma_load_4d(dst + C::kKStageBytes / 2, &tm_k, &k_full[slot], c * 128, it.hk, 0, pb);
+          }
+          ++kq;
+        }
+        return true;
+      };
+      auto load_v = [&](int u) -> bool {
+        const int pg = it.pg_lo + 2 * (it.t0 + u);
+        const int pa = page_id(p, it, pg), pb = page_id(p, it, pg + 1);
+        const uint32_t slot = vq % SV;
+        if (!wait_all(&v_empty[slot], ((vq / SV) & 1) ^ 1)) return false;
+        if (leader) {
+          uint8_t* dst = vring + slot * C::kVStageBytes;
+          mbar_arrive_expect_tx(&v_full[slot], C::kVStageBytes);
+          for (int c = 0; c < VC; ++c) {
+            const int cv = (it.dhalf * VC + c) * 128;  // this item's slice of the head dims
+            tma_load_4d(dst + c * kStageBytes, &tm_v, &v_full[slot], cv, it.hk, 0, pa);
+            tma_load_4d(dst + c * kStageBytes + kStageBytes / 2, &tm_v, &v_full[slot], cv, it.hk, 0, pb);
+          }
+        }
+        ++vq;
+        return true;
+      };
       if (warp == 0) {
-        // Q tile, then K(0), [K(1), V(0)], [K(2), V(1)], ..., V(n-1)
+        // Q tile, then K(0), [K(1), V(0)], [K(2), V(1)], ..., V(n-1); or Q and the K tiles
+        // alone when V has a loader warp of its own
         if (!(ok = wait_all(&q_empty[qb], qpar ^ 1))) break;
         if (leader) {
           mbar_arrive_expect_tx(&q_full[qb], C::kQBytes);
@@ -227,44 +268,17 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             tma_load_3d(qbuf + qb * C::kQBytes + c * C::kRows * 128, &tm_q, &q_full[qb], c * 128, it.hk * p.group,
                         it.q0 + it.row0 / p.group);
         }
-        auto load_k = [&](int u) -> bool {
-          const int pg = it.pg_lo + 2 * (it.t0 + u);
-          const int pa = page_id(p, it, pg), pb = page_id(p, it, pg + 1);
-          for (int c = 0; c < DC; ++c) {
-            const uint32_t slot = kq % SK;
-            if (!wait_all(&k_empty[slot], ((kq / SK) & 1) ^ 1)) return false;
-            if (leader) {
-              uint8_t* dst = kring + slot * C::kKStageBytes;
-              mbar_arrive_expect_tx(&k_full[slot], C::kKStageBytes);
-              tma_load_4d(dst, &tm_k, &k_full[slot], c * 128, it.hk, 0, pa);
-              tma_load_4d(dst + C::kKStageBytes / 2, &tm_k, &k_full[slot], c * 128, it.hk, 0, pb);
-            }
-            ++kq;
+        if constexpr (C::kVWarp) {
+          for (int u = 0; u < n && ok; ++u) ok = load_k(u);
+        } else {
+          ok = load_k(0);
+          for (int u = 1; u <= n && ok; ++u) {
+            if (u < n) ok = load_k(u);
+            if (ok) ok = load_v(u - 1);
           }
-          return true;
-        };
-        auto load_v = [&](int u) -> bool {
-          const int pg = it.pg_lo + 2 * (it.t0 + u);
-          const int pa = page_id(p, it, pg), pb = page_id(p, it, pg + 1);
-          const uint32_t slot = vq % SV;
-          if (!wait_all(&v_empty[slot], ((vq / SV) & 1) ^ 1)) return false;
-          if (leader) {
-            uint8_t* dst = vring + slot * C::kVStageBytes;
-            mbar_arrive_expect_tx(&v_full[slot], C::kVStageBytes);
-            for (int c = 0; c < VC; ++c) {
-              const int cv = (it.dhalf * VC + c) * 128;  // this item's slice of the head dims
-              tma_load_4d(dst + c * kStageBytes, &tm_v, &v_full[slot], cv, it.hk, 0, pa);
-              tma_load_4d(dst + c * kStageBytes + kStageBytes / 2, &tm_v, &v_full[slot], cv, it.hk, 0, pb);
-            }
-          }
-          ++vq;
-          return true;
-        };
-        ok = load_k(0);
-        for (int u = 1; u <= n && ok; ++u) {
-          if (u < n) ok = load_k(u);
-          if (ok) ok = load_v(u - 1);
         }
+      } else if (C::kVWarp && warp == 3) {
+        for (int u = 0; u < n && ok; ++u) ok = load_v(u);
       } else if (warp == 1) {
         // S(g) = Q . K^T into S buffer g & 1, once PV(g - 2) has released it
         constexpr uint32_t idesc = make_idesc(kFmtE4M3, kKMajor, kKMajor, 128, 128);
@@ -325,14 +339,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       g += n;
     }
     if (!ok && leader) flag_timeout(p, abort_flag);
-    if (warp == 0) {
-      // every issued copy must land before the CTA may exit
+    if (warp == 0 || (C::kVWarp && warp == 3)) {
+      // every issued copy must land before the CTA may exit (each loader drains its own)
       for (uint32_t j = kq > (uint32_t)SK ? kq - SK : 0; j < kq; ++j)
         mbar_wait(&k_full[j % SK], (j / SK) & 1, kDrainWaitLimit);
       for (uint32_t j = vq > (uint32_t)SV ? vq - SV : 0; j < vq; ++j)
         mbar_wait(&v_full[j % SV], (j / SV) & 1, kDrainWaitLimit);
-      for (uint32_t j = qit > (uint32_t)QB ? qit - QB : 0; j < qit; ++j)
-        mbar_wait(&q_full[j % QB], (j / QB) & 1, kDrainWaitLimit);
+      if (warp == 0)
+        for (uint32_t j = qit > (uint32_t)QB ? qit - QB : 0; j < qit; ++j)
+          mbar_wait(&q_full[j % QB], (j / QB) & 1, kDrainWaitLimit);
     } else {
       uint64_t* my_drain = &drain[warp - 1];
       if (leader) mma_commit(my_drain);
@@ -341,28 +356,28 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- softmax, O correction, epilogue
-    // Two warpgroups.  The warp pair of lane quarter q (one warp per group) owns
-    // rows 32q .. 32q + 31; warpgroup hw takes keys [64 hw, 64 hw + 64) of every
-    // tile and output dims [hw * kDO / 2, (hw + 1) * kDO / 2).  A pair exchanges
-    // its half-tile maxima (and finally its row sums) through shared memory on
-    // named barrier 1 + q, and every early exit is a vote on that barrier, so the
-    // two warps of a pair always leave together.
-    const int hw = (warp - 3) >> 2;
+    // kSW warpgroups.  The kSW warps of lane quarter q (one per group) own rows
+    // 32q .. 32q + 31; warpgroup hw takes keys [KT hw, KT hw + KT) of every tile
+    // and output dims [hw * HO, (hw + 1) * HO).  The warps of a row group
+    // exchange their partial tile maxima (and finally their row sums) through
+    // shared memory on named barrier 1 + q, and every early exit is a vote on
+    // that barrier, so the warps of a group always leave together.
+    constexpr int SW = C::kSW, KT = C::kKT, HO = C::kHO, OC = C::kOC;
+    const int hw = (warp - C::kSm0) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // this thread's row = its TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const uint32_t pair_bar = 1 + quarter;
     const float NEG_INF = __int_as_float(0xFF800000);
-    constexpr int HO = DO / 2;  // output dims per warpgroup
-    float* xmax = reinterpret_cast<float*>(xchg);  // [2][2][128] half-tile maxima, by tile parity
-    float* lsum = xmax + 512;                      // [2][128] half row sums
+    float* xmax = reinterpret_cast<float*>(xchg);  // [2][SW][128] partial tile maxima, by tile parity
+    float* lsum = xmax + 2 * SW * 128;             // [SW][128] partial row sums
     uint32_t g = 0, vq = 0, tails = 0;
     auto wait_w = [&](uint64_t* bar, uint32_t parity) {
       const bool w_ok = __all_sync(0xFFFFFFFFu, pwait(bar, parity, lim, abort_flag));
       if (!w_ok) flag_timeout(p, abort_flag);
       return w_ok;
     };
-    auto pair_fail = [&](bool ok_here) { return bar_red_or(pair_bar, 64, !ok_here); };
+    auto pair_fail = [&](bool ok_here) { return bar_red_or(pair_bar, 32 * SW, !ok_here); };
     bool aborted = false;
     for (uint32_t ik = 0; !aborted; ++ik) {
       const uint32_t is = ik % kItemSlots;
@@ -404,36 +419,42 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       float m = NEG_INF, l0 = 0.f, l1 = 0.f;
       bool sticky = true;  // waits after a tile's vote that failed; reported at the next vote
       for (int u = 0; u < n; ++u, ++g) {
-        const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage + 64 * hw;  // first key of this half
+        const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage + KT * hw;  // first key of this part
         const uint32_t sb = g & 1;
         const bool sok = wait_w(&s_full[sb], (g >> 1) & 1);
-        float x[64];
+        float x[KT];
         if (sok) {
           tc_fence_after();
-          tmem_load64f(tmem + lane_base + sb * 128 + 64 * hw, x);
+          if constexpr (KT == 64)
+            tmem_load64f(tmem + lane_base + sb * 128 + KT * hw, x);
+          else
+            tmem_load32f(tmem + lane_base + sb * 128 + KT * hw, x);
         } else {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) x[i] = NEG_INF;
+          for (int i = 0; i < KT; ++i) x[i] = NEG_INF;
         }
-        if (!(kb >= lo_r && kb + 63 <= hi_r)) {
+        if (!(kb >= lo_r && kb + KT - 1 <= hi_r)) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
+          for (int i = 0; i < KT; ++i)
             if (kb + i < lo_r || kb + i > hi_r) x[i] = NEG_INF;
         }
-        // half-tile maximum (raw scores; scale > 0), then the pair's
-        float t[16];
+        // partial tile maximum (raw scores; scale > 0), then the row group's
+        float t[KT / 4];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) t[i] = fmax3(x[4 * i], x[4 * i + 1], fmaxf(x[4 * i + 2], x[4 * i + 3]));
+        for (int i = 0; i < KT / 4; ++i) t[i] = fmax3(x[4 * i], x[4 * i + 1], fmaxf(x[4 * i + 2], x[4 * i + 3]));
 #pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
+        for (int w = KT / 8; w >= 1; w >>= 1)
 #pragma unroll
           for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
-        xmax[(sb * 2 + hw) * 128 + r] = t[0];
+        xmax[(sb * SW + hw) * 128 + r] = t[0];
         if (pair_fail(sok && sticky)) {
           aborted = true;
           break;
         }
-        const float ts = fmaxf(t[0], xmax[(sb * 2 + (hw ^ 1)) * 128 + r]) * scale;
+        float tmax = xmax[(sb * SW) * 128 + r];
+#pragma unroll
+        for (int j = 1; j < SW; ++j) tmax = fmaxf(tmax, xmax[(sb * SW + j) * 128 + r]);
+        const float ts = tmax * scale;
         float alpha = 1.0f;
         bool resc = false;
         if (ts > m + C::kTau) {
@@ -452,24 +473,30 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           if (u > 0) sticky = wait_w(&s_free[(g - 1) & 1], ((g - 1) >> 1) & 1) && sticky;
           tc_fence_after();
 #pragma unroll 1
-          for (int q = 0; q < HO / 64; ++q) {
-            float o[64];
-            const uint32_t ta = tmem + lane_base + C::kOCol + hw * HO + 64 * q;
-            tmem_load64f(ta, o);
+          for (int q = 0; q < HO / OC; ++q) {
+            float o[OC];
+            const uint32_t ta = tmem + lane_base + C::kOCol + hw * HO + OC * q;
+            if constexpr (OC == 64)
+              tmem_load64f(ta, o);
+            else
+              tmem_load32f(ta, o);
 #pragma unroll
-            for (int i = 0; i < 64; i += 2) {
+            for (int i = 0; i < OC; i += 2) {
               const float2 v = __fmul2_rn(make_float2(o[i], o[i + 1]), make_float2(alpha, alpha));
               o[i] = v.x;
               o[i + 1] = v.y;
             }
-            tmem_store64f(ta, o);
+            if constexpr (OC == 64)
+              tmem_store64f(ta, o);
+            else
+              tmem_store32f(ta, o);
           }
         }
         // P' = 2^(x * scale - m + shift) as an E4M3 pair, 32 keys (8 columns) at a time;
-        // this half's words are columns [16 hw, 16 hw + 16) of the hi and lo terms, which
-        // overwrite the first 64 columns of this S buffer (the pair's scores are in registers)
+        // this part's words are columns [KT/4 hw, KT/4 (hw + 1)) of the hi and lo terms, which
+        // overwrite the first 64 columns of this S buffer (the group's scores are in registers)
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < KT / 32; ++q) {
           uint32_t hi[8], lo[8];
           uint32_t sa = 0, sb2 = 0;  // f16x2 partial row sums of these 32 keys
 #pragma unroll
@@ -490,8 +517,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           const float2 fa = f16x2_to_f32(sa), fb = f16x2_to_f32(sb2);
           l0 += fa.x + fb.x;
           l1 += fa.y + fb.y;
-          tmem_store8(tmem + lane_base + sb * 128 + 16 * hw + 8 * q, hi);
-          tmem_store8(tmem + lane_base + sb * 128 + 32 + 16 * hw + 8 * q, lo);
+          tmem_store8(tmem + lane_base + sb * 128 + (KT / 4) * hw + 8 * q, hi);
+          tmem_store8(tmem + lane_base + sb * 128 + 32 + (KT / 4) * hw + 8 * q, lo);
         }
         tmem_wait_st();
         // rows of the last page past the sequence end may hold anything (even NaN):
@@ -503,7 +530,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           const int zr = max(0, it.Lk - kt);
           uint8_t* st = vring + (vq % SV) * C::kVStageBytes;
           for (int c = 0; c < VC; ++c)
-            for (int x16 = zr * 8 + hw * 128 + r; x16 < kTileKeys * 8; x16 += 256)
+            for (int x16 = zr * 8 + hw * 128 + r; x16 < kTileKeys * 8; x16 += 128 * SW)
               *reinterpret_cast<uint4*>(st + c * kStageBytes + x16 * 16) = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
         }
@@ -518,48 +545,56 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       lsum[hw * 128 + r] = l0 + l1;
       if (pair_fail(eok)) break;
       tc_fence_after();
-      const float l = lsum[r] + lsum[128 + r];
+      float l = lsum[r];
+#pragma unroll
+      for (int j = 1; j < SW; ++j) l += lsum[j * 128 + r];
       float inv = l > 0.f ? vd / l : 0.f;
       float lse2 = l > 0.f ? m - C::kPShift + __log2f(l) : NEG_INF;
       if (p.sinks && live) fold_sink(l, m - C::kPShift, p.sinks[head] * 1.4426950408889634f, vd, inv, lse2);
-      // Each 32-column chunk of this warp's 32 rows goes through a 2 KB staging
-      // buffer (row-major, 16-byte pieces swizzled by (row >> 1) & 3), then out as
-      // 64-byte row segments: lane l stores piece l & 3 of row i * 8 + l / 4.
-      uint8_t* stg = ostage + (warp - 3) * 2048;
-      __nv_bfloat16* dst_row[4];
-      bool dst_live[4];
+      // Each kSeg-byte column segment of this warp's 32 rows goes through a
+      // 32 x kSeg staging buffer (row-major, 16-byte pieces swizzled by row), then
+      // out as kSeg-byte row segments: lane l stores piece l % NP of row
+      // i * (32 / NP) + l / NP, with NP = kSeg / 16 pieces per segment.
+      constexpr int SEG = C::kSeg, NP = SEG / 16, SC = SEG / 2;  // bytes, pieces, columns per segment
+      const int sw_shift = NP == 4 ? 1 : 2;                      // piece swizzle: (row >> sw_shift) & (NP - 1)
+      uint8_t* stg = ostage + (warp - C::kSm0) * 32 * SEG;
+      __nv_bfloat16* dst_row[NP];
+      bool dst_live[NP];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int rr = quarter * 32 + i * 8 + (lane >> 2);
+      for (int i = 0; i < NP; ++i) {
+        const int rr = quarter * 32 + i * (32 / NP) + lane / NP;
         dst_live[i] = rr < it.nrows;
         const size_t row = (size_t)(it.q0 + (it.row0 + rr) / G) * p.hq + it.hk * G + (it.row0 + rr) % G;
-        dst_row[i] = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + dbase + (lane & 3) * 8;
+        dst_row[i] = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + dbase + (lane % NP) * 8;
       }
 #pragma unroll 1
-      for (int q2 = 0; q2 < HO / 64; ++q2) {
-        float o[64];
-        tmem_load64f(tmem + lane_base + C::kOCol + hw * HO + 64 * q2, o);
+      for (int q2 = 0; q2 < HO / OC; ++q2) {
+        float o[OC];
+        if constexpr (OC == 64)
+          tmem_load64f(tmem + lane_base + C::kOCol + hw * HO + OC * q2, o);
+        else
+          tmem_load32f(tmem + lane_base + C::kOCol + hw * HO + OC * q2, o);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int q = 2 * q2 + hh;
+        for (int hh = 0; hh < OC / SC; ++hh) {
+          const int q = (OC / SC) * q2 + hh;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < NP; ++c) {
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               __nv_bfloat162 b2 =
-                  __floats2bfloat162_rn(o[32 * hh + 8 * c + 2 * i] * inv, o[32 * hh + 8 * c + 2 * i + 1] * inv);
+                  __floats2bfloat162_rn(o[SC * hh + 8 * c + 2 * i] * inv, o[SC * hh + 8 * c + 2 * i + 1] * inv);
               w[i] = *reinterpret_cast<uint32_t*>(&b2);
             }
-            *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+            *reinterpret_cast<uint4*>(stg + lane * SEG + ((c ^ ((lane >> sw_shift) & (NP - 1))) << 4)) =
                 make_uint4(w[0], w[1], w[2], w[3]);
           }
           __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int rr = i * 8 + (lane >> 2), c = lane & 3;
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4));
-            if (dst_live[i]) *reinterpret_cast<uint4*>(dst_row[i] + 32 * q) = v;
+          for (int i = 0; i < NP; ++i) {
+            const int rr = i * (32 / NP) + lane / NP, c = lane % NP;
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * SEG + ((c ^ ((rr >> sw_shift) & (NP - 1))) << 4));
+            if (dst_live[i]) *reinterpret_cast<uint4*>(dst_row[i] + SC * q) = v;
           }
           __syncwarp();
         }
