@@ -541,10 +541,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       }
       if (aborted) break;
       // ---------------- epilogue: O / l, lse
-      const bool eok = wait_w(&s_free[(g - 1) & 1], ((g - 1) >> 1) & 1) && sticky;
+      // Row sums, scales and destinations need the last tile's P, not its PV:
+      // they are formed while that PV completes, and O is read after it.
       lsum[hw * 128 + r] = l0 + l1;
-      if (pair_fail(eok)) break;
-      tc_fence_after();
+      if (pair_fail(sticky)) break;
       float l = lsum[r];
 #pragma unroll
       for (int j = 1; j < SW; ++j) l += lsum[j * 128 + r];
@@ -567,6 +567,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         const size_t row = (size_t)(it.q0 + (it.row0 + rr) / G) * p.hq + it.hk * G + (it.row0 + rr) % G;
         dst_row[i] = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + dbase + (lane % NP) * 8;
       }
+      const bool eok = wait_w(&s_free[(g - 1) & 1], ((g - 1) >> 1) & 1);
+      if (pair_fail(eok)) break;
+      tc_fence_after();
 #pragma unroll 1
       for (int q2 = 0; q2 < HO / OC; ++q2) {
         float o[OC];
