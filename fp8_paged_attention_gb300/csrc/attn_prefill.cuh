@@ -22,11 +22,11 @@
 // work item of its own: both compute the full S and P, each accumulates O for
 // its slice against that slice of V.
 //
-// Warps: 0 TMA producer, 1 QK^T issuer (and TMEM owner), 2 PV issuer, then
-// softmax / O correction / epilogue in kSW warpgroups (kSW warps per row
-// quarter, each thread 1 / kSW of a row's keys and output dims).  The producer and
-// the issuers run warp-uniform loops with one elected lane issuing; they and the
-// softmax warps synchronize only through mbarriers.
+// Warps: 0 TMA producer (Q and K), 1 QK^T issuer (and TMEM owner), 2 PV issuer,
+// 3 V loader, then softmax / O correction / epilogue in kSW warpgroups (kSW
+// warps per row quarter, each thread 1 / kSW of a row's keys and output dims).
+// The loaders and the issuers run warp-uniform loops with one elected lane
+// issuing; they and the softmax warps synchronize only through mbarriers.
 #pragma once
 #include "attn_kernel.cuh"
 #include "kernels.h"
