@@ -80,7 +80,13 @@ struct PrefillCfg {
   static constexpr int kQBufs = D == 256 ? 2 : 1;
   static constexpr int kKStageBytes = kStageBytes;        // 128 keys x one 128-byte chunk
   static constexpr int kVStageBytes = kVC * kStageBytes;  // 128 keys x kDO bytes, chunk c at c * 16 KB
-  static constexpr int kKStages = D == 256 ? 3 : 4;
+  // QK^T in two N = 64 halves: keys 64..127 (S columns 64..127) as soon as the
+  // softmax has read the buffer's previous scores, keys 0..63 (the columns P
+  // overwrites) once the PV of that tile has released them.  At head dim 512
+  // the halves read Q twice over four chunks and a one-tile K ring cannot run
+  // ahead, so there S(g) stays one N = 128 MMA per step.
+  static constexpr bool kSplitQK = D == 256;
+  static constexpr int kKStages = (D == 256 && !kSplitQK) ? 3 : 4;
   static constexpr int kVStages = 2;
   static constexpr int kSW = 2;                          // softmax warpgroups: each takes 128 / kSW keys of a row
   static constexpr int kKT = kTileKeys / kSW;            // keys of a tile per softmax thread
@@ -134,7 +140,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   uint64_t* v_ready = o_empty + 1;  // tail tile: its V stage landed (PV issuer -> softmax)
   uint64_t* drain = v_ready + 1;    // [2] one per issuer
   uint64_t* never = drain + 2;      // nothing arrives on it: the stall-injection hook waits here
-  uint64_t* item_full = never + 1;
+  uint64_t* s_read = never + 1;     // [2] S buffer's scores in registers (every softmax warp)
+  uint64_t* item_full = s_read + 2;
   uint64_t* item_empty = item_full + kItemSlots;
   ItemSlot* islot = reinterpret_cast<ItemSlot*>(item_empty + kItemSlots);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(islot + kItemSlots);
@@ -159,6 +166,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       mbar_init(&s_free[i], 1);
       mbar_init(&p_full[i], 4 * C::kSW);
       mbar_init(&drain[i], 1);
+      mbar_init(&s_read[i], 4 * C::kSW);
     }
     mbar_init(o_empty, 4 * C::kSW);
     mbar_init(v_ready, 1);
@@ -280,30 +288,61 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       } else if (C::kVWarp && warp == 3) {
         for (int u = 0; u < n && ok; ++u) ok = load_v(u);
       } else if (warp == 1) {
-        // S(g) = Q . K^T into S buffer g & 1, once PV(g - 2) has released it
-        constexpr uint32_t idesc = make_idesc(kFmtE4M3, kKMajor, kKMajor, 128, 128);
+        // S(g) = Q . K^T into S buffer g & 1, once PV(g - 2) has released it; with
+        // kSplitQK, keys 64..127 already once the softmax has read S(g - 2)
+        constexpr uint32_t idesc = make_idesc(kFmtE4M3, kKMajor, kKMajor, 128, C::kSplitQK ? 64 : 128);
         if (!(ok = wait_all(&q_full[qb], qpar))) break;
         tc_fence_after();
         const uint32_t qaddr = smem_u32(qbuf + qb * C::kQBytes);
-        for (int u = 0; u < n && ok; ++u) {
-          const uint32_t gg = g + u, sb = gg & 1;
-          if (!(ok = wait_all(&s_free[sb], ((gg >> 1) & 1) ^ 1))) break;
-          tc_fence_after();
-          for (int c = 0; c < DC && ok; ++c) {
-            const uint32_t slot = kq % SK;
-            if (!(ok = wait_all(&k_full[slot], (kq / SK) & 1))) break;
-            tc_fence_after();
-            const uint32_t a0 = qaddr + c * C::kRows * 128, b0 = smem_u32(kring + slot * C::kKStageBytes);
+        // one half of S(gg): keys [64 h, 64 h + 64) of the tile's K stages into columns [64 h, 64 h + 64)
+        auto qk_half = [&](uint32_t sb, int h, bool wait_k) -> bool {
+          for (int c = 0; c < DC; ++c) {
+            const uint32_t pos = kq + c, slot = pos % SK;
+            if (wait_k) {
+              if (!wait_all(&k_full[slot], (pos / SK) & 1)) return false;
+              tc_fence_after();
+            }
+            const uint32_t a0 = qaddr + c * C::kRows * 128;
+            const uint32_t b0 = smem_u32(kring + slot * C::kKStageBytes) + h * (C::kKStageBytes / 2);
             if (leader) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_f8f6f4(tmem + sb * 128, make_sdesc(a0 + kk * 32, 16, 1024, kLayoutSW128),
+                mma_f8f6f4(tmem + sb * 128 + 64 * h, make_sdesc(a0 + kk * 32, 16, 1024, kLayoutSW128),
                            make_sdesc(b0 + kk * 32, 16, 1024, kLayoutSW128), idesc, (c | kk) != 0);
-              mma_commit(&k_empty[slot]);
+              if (h == 0) mma_commit(&k_empty[slot]);  // the stage's last MMAs
             }
-            ++kq;
           }
-          if (ok && leader) mma_commit(&s_full[sb]);
+          return true;
+        };
+        for (int u = 0; u < n && ok; ++u) {
+          const uint32_t gg = g + u, sb = gg & 1;
+          if constexpr (C::kSplitQK) {
+            if (!(ok = wait_all(&s_read[sb], ((gg >> 1) & 1) ^ 1))) break;
+            tc_fence_after();
+            if (!(ok = qk_half(sb, 1, true))) break;
+            if (!(ok = wait_all(&s_free[sb], ((gg >> 1) & 1) ^ 1))) break;
+            tc_fence_after();
+            if (!(ok = qk_half(sb, 0, false))) break;
+          } else {
+            if (!(ok = wait_all(&s_free[sb], ((gg >> 1) & 1) ^ 1))) break;
+            tc_fence_after();
+            for (int c = 0; c < DC && ok; ++c) {
+              const uint32_t slot = (kq + c) % SK;
+              if (!(ok = wait_all(&k_full[slot], ((kq + c) / SK) & 1))) break;
+              tc_fence_after();
+              const uint32_t a0 = qaddr + c * C::kRows * 128, b0 = smem_u32(kring + slot * C::kKStageBytes);
+              if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_f8f6f4(tmem + sb * 128, make_sdesc(a0 + kk * 32, 16, 1024, kLayoutSW128),
+                             make_sdesc(b0 + kk * 32, 16, 1024, kLayoutSW128), idesc, (c | kk) != 0);
+                mma_commit(&k_empty[slot]);
+              }
+            }
+            if (!ok) break;
+          }
+          kq += DC;
+          if (leader) mma_commit(&s_full[sb]);
         }
         if (ok && leader) mma_commit(&q_empty[qb]);
       } else {
@@ -432,6 +471,12 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         } else {
 #pragma unroll
           for (int i = 0; i < KT; ++i) x[i] = NEG_INF;
+        }
+        if constexpr (C::kSplitQK) {
+          // the scores are in registers: keys 64..127 of S(g + 2) may go to this buffer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_read[sb]);
         }
         if (!(kb >= lo_r && kb + KT - 1 <= hi_r)) {
 #pragma unroll
