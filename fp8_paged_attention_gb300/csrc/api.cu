@@ -179,16 +179,35 @@ int check_shape(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int h
 }
 
 // Split count for single-row-tile sequences.  Measured on GB300: once every
-// SM has a (sequence, KV head) unit the kernel streams at the HBM roofline and
-// splitting only adds partial writes and the combine, so split only when there
-// are fewer units than SMs, to about two items per SM, each split keeping at
-// least four 128-key tiles.
-int auto_splits(int batch, int hkv, int max_pages, int window_left, int max_lq0, int sms) {
+// SM has a (sequence, KV head) unit, decode tiles of up to 16 rows stream at
+// the HBM roofline and splitting only adds partial writes and the combine, so
+// they split only when there are fewer units than SMs, to about two items per
+// SM, each split keeping at least four 128-key tiles.  Tiles of 32 rows (a few
+// query tokens per sequence, as in speculative verification) do more work per
+// byte, and a part-filled last wave of long units costs them more: between one
+// and four waves of units they take the split count whose item waves leave the
+// least idle tail, with a small cost per extra split (64 sequences x 4 KV
+// heads, 28672 keys: 4 splits, kernel 1.287 -> 1.183 ms).
+int auto_splits(int batch, int hkv, int max_pages, int window_left, int max_lq0, int rows, int sms) {
   const long long units = (long long)hkv * batch;
-  if (units <= 0 || units >= sms) return 1;
+  if (units <= 0) return 1;
   long long pages = max_pages;
   if (window_left >= 0) pages = std::min<long long>(pages, (window_left + max_lq0 - 1) / kPage + 2);
   const long long tiles = (pages + 1) / 2;
+  if (units >= sms) {
+    if (rows <= 16 || units >= 4LL * sms) return 1;
+    int best = 1;
+    double best_cost = 1e30;
+    for (int s = 1; s <= 8 && (s == 1 || tiles / s >= 4); ++s) {
+      const long long waves = (units * s + sms - 1) / sms;
+      const double cost = (double)waves / s * (1.0 + 0.02 * (s - 1));
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = s;
+      }
+    }
+    return best;
+  }
   long long s = (2LL * sms + units - 1) / units;
   s = std::min<long long>(s, std::max<long long>(1, tiles / 4));
   s = std::max<long long>(1, std::min<long long>(s, 64));
@@ -235,7 +254,8 @@ int make_plan(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int hea
   // With a prefill row class in the batch its tiles keep every SM busy: no split.
   pl.splits = num_splits > 0       ? num_splits
               : pl.num_classes > 1 ? 1
-                                   : auto_splits(batch, hkv, max_pages, window_left, lq0_max, device_sms());
+                                   : auto_splits(batch, hkv, max_pages, window_left, lq0_max, pl.cls[0].rows,
+                                                 device_sms());
   pl.cls[0].max_splits = pl.splits;
   pl.cls[1].dhalves = pl.prefill_kernel && head_dim == 512 ? 2 : 1;
   // workspace layout: [counts][class-0 items][class-1 items][o_part][lse_part]

@@ -88,6 +88,12 @@ def test_workspace_and_splits_are_host_functions():
     assert fp8pa.num_splits(8, 8, 1, 32, 4, 512, BF16, 144, -1, 0) > 1
     assert fp8pa.num_splits(8, 8, 1, 32, 4, 512, E4M3, 144, -1, 0) > 1
     assert fp8pa.num_splits(64, 64, 1, 32, 4, 512, E4M3, 144, -1, 0) == 1
+    # 32-row tiles (4 verify tokens x 8 heads) with 1-4 waves of long units: the split count whose
+    # item waves fill the last one best (64 x 4 units on 152 SMs: 4 splits, 6.7 waves)
+    assert fp8pa.num_splits(64, 256, 4, 32, 4, 512, BF16, 448, -1, 0) == 4
+    # 16-row decode tiles with as many units stay whole, and so do 32-row tiles past four waves
+    assert fp8pa.num_splits(64, 64, 1, 32, 4, 512, BF16, 144, -1, 0) == 1
+    assert fp8pa.num_splits(160, 640, 4, 32, 4, 512, BF16, 448, -1, 0) == 1
     # the mixed chunked-prefill batch has plenty of units: no split
     assert fp8pa.num_splits(4033, 8128, 4096, 32, 16, 256, E4M3, 128, 1023, 0) == 1
     # launches: plan + attention (+ combine when split)
