@@ -59,8 +59,23 @@ extern "C" int fp8_paged_attn_fwd_noalloc(const void* q, int q_dtype, const uint
                                           int window_left, int causal, int num_splits, void* out, float* lse,
                                           fp8pa_stream_t stream) {
   // Size check first: the same sizing as the workspace entry point.
-  const size_t need = fp8pa_workspace_size(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_dtype,
-                                           max_pages_per_seq, window_left, num_splits);
+  size_t need = fp8pa_workspace_size(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_dtype,
+                                     max_pages_per_seq, window_left, num_splits);
+  if (num_splits == 0 && need > (size_t)FP8PA_NOALLOC_SCRATCH_BYTES) {
+    // Automatic splits whose partials do not fit: the largest smaller split
+    // count that does (a function of the call's sizes, like the automatic one).
+    const int s_auto = fp8pa_num_splits(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim, q_dtype,
+                                        max_pages_per_seq, window_left, 0);
+    for (int s = s_auto - 1; s >= 1; --s) {
+      const size_t n = fp8pa_workspace_size(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, head_dim,
+                                            q_dtype, max_pages_per_seq, window_left, s);
+      if (n != 0 && n <= (size_t)FP8PA_NOALLOC_SCRATCH_BYTES) {
+        num_splits = s;
+        need = n;
+        break;
+      }
+    }
+  }
   if (need == 0) {
     // rejected shape: let the regular entry point produce its message
     return fp8_paged_attn_fwd(q, q_dtype, k_cache, v_cache, num_pages, block_table, max_pages_per_seq,

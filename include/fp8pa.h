@@ -163,9 +163,14 @@ int fp8pa_lse_combine(const void* o_parts, const float* lse_parts, int num_parts
  * inputs and outputs.
  *
  * Limits and rules:
- *  - A call whose scratch need (fp8pa_workspace_size for the same arguments)
- *    exceeds FP8PA_NOALLOC_SCRATCH_BYTES is rejected with FP8PA_EINVAL and a
- *    message; nothing is launched.  Splits above 1 need the most scratch.
+ *  - With num_splits = 0 (automatic) and an automatic split count whose
+ *    partials do not fit FP8PA_NOALLOC_SCRATCH_BYTES, the call runs the
+ *    largest smaller split count that fits (a function of the sizes alone);
+ *    its results are those of fp8_paged_attn_fwd with that num_splits.
+ *  - Any other call whose scratch need (fp8pa_workspace_size for the same
+ *    arguments) exceeds FP8PA_NOALLOC_SCRATCH_BYTES is rejected with
+ *    FP8PA_EINVAL and a message; nothing is launched.  Splits above 1 need the
+ *    most scratch.
  *  - All calls share the one array on a device: calls whose kernels may
  *    overlap on the GPU (e.g. on different streams without ordering) race and
  *    give undefined results.  Calls ordered on one stream are fine; each call

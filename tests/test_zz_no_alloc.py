@@ -73,6 +73,35 @@ def test_noalloc_matches_workspace_entry_point(case):
     assert torch.equal(results[0][0], results[1][0]) and torch.equal(results[0][1], results[1][1])
 
 
+def test_noalloc_automatic_splits_step_down_to_fit_its_scratch():
+    # 64 sequences x 4 verify tokens, Hq 32 / Hkv 4, D 512: the automatic rule picks 4 splits for these
+    # 32-row tiles, whose partials need more than the scratch holds; the call runs the largest split
+    # count that fits and gives exactly what the workspace entry point gives with that count
+    import fp8_paged_attention_gb300 as fp8pa
+    lk = [2048 + 13 * i for i in range(64)]
+    w = synth.make_workload("verify_steps_down", [4] * 64, lk, 32, 4, 512, -1, True, False, seed=7, device="cuda")
+    mp = w.block_table.shape[1]
+    s_auto = fp8pa.num_splits(w.batch, w.total_q, w.max_seqlen_q, 32, 4, 512, fp8pa.FP8PA_BF16, mp, -1, 0)
+    assert s_auto > 1
+    assert fp8pa.workspace_size(w.batch, w.total_q, w.max_seqlen_q, 32, 4, 512, fp8pa.FP8PA_BF16, mp, -1, 0) > (32 << 20)
+    fits = [s for s in range(1, s_auto) if fp8pa.workspace_size(w.batch, w.total_q, w.max_seqlen_q, 32, 4, 512,
+                                                                 fp8pa.FP8PA_BF16, mp, -1, s) <= (32 << 20)]
+    s_fit = max(fits)
+    qd = torch.ones(1, dtype=torch.float32, device="cuda")
+    kd = torch.tensor([w.k_descale], dtype=torch.float32, device="cuda")
+    vd = torch.tensor([w.v_descale], dtype=torch.float32, device="cuda")
+    ref_out, ref_lse = fp8pa.fp8_paged_attn_fwd(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q, w.seqused_k,
+                                                w.max_seqlen_q, qd, kd, vd, w.softmax_scale, -1, True,
+                                                num_splits=s_fit)
+    out = torch.full_like(ref_out, float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
+    lib = fp8pa.load_library()
+    rc = lib.fp8_paged_attn_fwd_noalloc(*_args(w, w.q, qd, kd, vd, 0, out, lse))
+    assert rc == 0, lib.fp8pa_last_error().decode()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+
+
 def test_noalloc_rejects_calls_beyond_its_scratch():
     import fp8_paged_attention_gb300 as fp8pa
     w = synth.make_workload("big_split", [1] * 64, [4096] * 64, 32, 4, 512, -1, True, False, seed=5, device="cuda")
