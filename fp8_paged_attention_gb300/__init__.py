@@ -1,6 +1,7 @@
 """Paged FP8 (E4M3) KV-cache attention for GB300 (sm_103a).
 
-Thin ctypes binding over the C ABI in ``include/fp8pa.h`` (library
+Thin ctypes binding over the C ABI in ``include/fp8pa.h`` (and the test and
+tuning hooks of ``include/fp8pa_testing.h``) (library
 ``_lib/libfp8pa.so``, built in-tree by ``build()``).  The functions here only
 marshal torch tensors into pointers and sizes; every step of the computation
 runs in the library's CUDA kernels.  There is no CPU fallback: if the library
@@ -148,8 +149,8 @@ def kernel_launches(batch, total_q, max_seqlen_q, num_heads_q, num_heads_kv, hea
 
 
 def set_timing_events(start=None, stop=None):
-    """Profiling hook: record torch.cuda.Event `start`/`stop` around the
-    attention kernels of later calls on this thread (None, None: off)."""
+    """Profiling hook (fp8pa_testing.h): record torch.cuda.Event `start`/`stop`
+    around the attention kernels of later calls on this thread (None, None: off)."""
     lib = load_library()
     if start is None or stop is None:
         lib.fp8pa_set_timing_events(None, None)
@@ -160,13 +161,15 @@ def set_timing_events(start=None, stop=None):
 
 
 def set_ctas_per_sm(ctas: int):
-    """Tuning hook: force 1 or 2 attention CTAs per SM (0 = automatic)."""
+    """Tuning hook (fp8pa_testing.h): force 1 or 2 attention CTAs per SM for
+    later calls on this thread (0 = automatic)."""
     load_library().fp8pa_set_ctas_per_sm(int(ctas))
 
 
 def set_bf16_dequant_v(on: bool):
-    """BF16-Q path: keep V E4M3 with a hi/lo E4M3 P (False, default) or
-    dequantize V to BF16 with a BF16 P (True)."""
+    """Test hook (fp8pa_testing.h), later calls on this thread: the BF16-Q path
+    keeps V E4M3 with a hi/lo E4M3 P (False, default) or dequantizes V to BF16
+    with a BF16 P (True)."""
     load_library().fp8pa_set_bf16_dequant_v(int(bool(on)))
 
 
@@ -297,11 +300,13 @@ def reset_device_status(stream=None):
 
 
 def set_wait_limit(max_iterations: int):
-    """Test hook: cap every bounded pipeline wait (0 restores the default)."""
+    """Test hook (fp8pa_testing.h): cap every bounded pipeline wait of later
+    calls on this thread (0 restores the default)."""
     load_library().fp8pa_set_wait_limit(int(max_iterations))
 
 
 def set_stall_injection(on: bool):
-    """Test hook: make every attention CTA's MMA thread wait on a barrier that
-    nothing arrives on, so that the launch takes its bounded-wait timeout path."""
+    """Test hook (fp8pa_testing.h): in later calls on this thread, every
+    attention CTA's MMA thread waits on a barrier that nothing arrives on, so
+    that the launch takes its bounded-wait timeout path."""
     load_library().fp8pa_set_stall_injection(int(bool(on)))

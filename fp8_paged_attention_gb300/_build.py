@@ -43,7 +43,7 @@ def _nvcc() -> str:
 
 
 def _deps():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "fp8pa.h")]
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     return [f for f in files if os.path.isfile(f)]
 
 

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "fp8pa.h"
+#include "fp8pa_testing.h"
 #include "kernels.h"
 
 namespace fp8pa {
@@ -50,26 +51,28 @@ namespace {
 __device__ unsigned int g_status;
 
 thread_local char g_err[512] = "";
+// Test, tuning and profiling hooks (fp8pa_testing.h): each host thread has its
+// own settings, so one caller's hooks never change another thread's calls.
 thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
-std::atomic<int> g_ctas_override{0};
-std::atomic<int> g_dequant_v{0};
+thread_local int g_ctas_override = 0;
+thread_local int g_dequant_v = 0;
+thread_local unsigned g_wait_limit = 0;
+thread_local int g_inject_stall = 0;
 
 // Kernel path for a Q dtype: E4M3 Q, or BF16 Q with V kept E4M3 (default) or
 // dequantized to BF16 (fp8pa_set_bf16_dequant_v).
-int kernel_path(bool fp8_q) { return fp8_q ? kPathE4M3 : (g_dequant_v.load() ? kPathBf16DqV : kPathBf16); }
+int kernel_path(bool fp8_q) { return fp8_q ? kPathE4M3 : (g_dequant_v ? kPathBf16DqV : kPathBf16); }
 
 // CTAs per SM for a kernel variant: two co-resident CTAs where both fit
 // (16-row tiles of the E4M3-Q path), else one.
 int ctas_per_sm(int head_dim, int path, int rows) {
-  const int forced = g_ctas_override.load();
+  const int forced = g_ctas_override;
   if (forced == 1 || forced == 2) {
     if (attn_smem_bytes(head_dim, path, rows, forced) > 0) return forced;
   }
   if (rows == 16 && attn_smem_bytes(head_dim, path, rows, 2) > 0) return 2;
   return 1;
 }
-std::atomic<unsigned> g_wait_limit{0};
-std::atomic<int> g_inject_stall{0};
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -111,18 +114,16 @@ int device_sms() {
   return v;
 }
 
+// Device address of the status word in the current context.  Looked up on
+// every call (a host-side table lookup, no device work), so it stays right
+// after cudaDeviceReset or a new primary context moves the module.
 unsigned* status_ptr() {
-  static std::atomic<unsigned*> cache[kMaxDevices];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  unsigned* p = cache[dev].load();
-  if (!p) {
-    void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_status) != cudaSuccess) return nullptr;
-    p = static_cast<unsigned*>(addr);
-    cache[dev].store(p);
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_status) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
   }
-  return p;
+  return static_cast<unsigned*>(addr);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -294,13 +295,13 @@ extern "C" {
 
 const char* fp8pa_last_error(void) { return g_err; }
 
-void fp8pa_set_wait_limit(unsigned int max_iterations) { g_wait_limit.store(max_iterations); }
+void fp8pa_set_wait_limit(unsigned int max_iterations) { g_wait_limit = max_iterations; }
 
-void fp8pa_set_stall_injection(int on) { g_inject_stall.store(on ? 1 : 0); }
+void fp8pa_set_stall_injection(int on) { g_inject_stall = on ? 1 : 0; }
 
-void fp8pa_set_ctas_per_sm(int ctas) { g_ctas_override.store(ctas); }
+void fp8pa_set_ctas_per_sm(int ctas) { g_ctas_override = ctas; }
 
-void fp8pa_set_bf16_dequant_v(int on) { g_dequant_v.store(on ? 1 : 0); }
+void fp8pa_set_bf16_dequant_v(int on) { g_dequant_v = on ? 1 : 0; }
 
 void fp8pa_set_timing_events(void* start_event, void* stop_event) {
   g_ev_start = static_cast<cudaEvent_t>(start_event);
@@ -496,9 +497,9 @@ int fwd_impl(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* 
   p.lse_part = reinterpret_cast<float*>(ws + pl.off_lsepart);
   p.sinks = sinks;
   p.status = status;
-  const unsigned wl = g_wait_limit.load();
+  const unsigned wl = g_wait_limit;
   p.wait_limit = wl ? wl : kDefaultWaitLimit;
-  p.inject_stall = g_inject_stall.load();
+  p.inject_stall = g_inject_stall;
   const bool timed = g_ev_start && g_ev_stop;
   if (timed && (e = cudaEventRecord(g_ev_start, st)) != cudaSuccess) return cuda_fail(e, "timing event");
   for (int k = 0; k < pl.num_classes; ++k) {

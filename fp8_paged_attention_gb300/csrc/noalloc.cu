@@ -8,7 +8,6 @@
 // gives kernel libraries no allocator of their own, or a latency-critical
 // path that cannot afford cudaMalloc's implicit device synchronization.  For
 // them this entry point needs nothing beyond the inputs and outputs.
-#include <atomic>
 #include <cstdio>
 
 #include "fp8pa.h"
@@ -19,27 +18,24 @@ namespace {
 // Every device that loads the library holds this array until the process exits.
 __device__ __align__(256) unsigned char g_noalloc_scratch[FP8PA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
-
-// Device address of the scratch array on the current device.  The array's name
-// in host code is only a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// Device address of the scratch array in the current context.  The array's
+// name in host code is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress with the device current.  It is looked up on every call
+// (a host-side table lookup, no device work): a cached address would go stale
+// after cudaDeviceReset or a new primary context reloads the module.
 int scratch_address(void** out, char* msg, size_t msg_len) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  if (e != cudaSuccess || dev < 0) {
     snprintf(msg, msg_len, "no usable current device (%s)", cudaGetErrorString(e));
     return FP8PA_ECUDA;
   }
-  void* p = g_scratch_addr[dev].load();
-  if (!p) {
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p) {
-      snprintf(msg, msg_len, "cudaGetSymbolAddress of the scratch array failed: %s", cudaGetErrorString(e));
-      return FP8PA_ECUDA;
-    }
-    g_scratch_addr[dev].store(p);
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p) {
+    cudaGetLastError();
+    snprintf(msg, msg_len, "cudaGetSymbolAddress of the scratch array failed: %s", cudaGetErrorString(e));
+    return FP8PA_ECUDA;
   }
   *out = p;
   return FP8PA_OK;

@@ -175,9 +175,15 @@ int fp8pa_lse_combine(const void* o_parts, const float* lse_parts, int num_parts
  *    overlap on the GPU (e.g. on different streams without ordering) race and
  *    give undefined results.  Calls ordered on one stream are fine; each call
  *    rewrites all the scratch it reads, so nothing must be cleared between calls.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture on that device.
+ *  - Every call looks up the array's device address in the current context
+ *    (cudaGetSymbolAddress, a host-side lookup), so the address stays right
+ *    after cudaDeviceReset.  The first call on a device may load the library's
+ *    device code into that device's context: make that first call before any
+ *    stream capture on that device.
+ *  - At the speculative-verify size (a few query tokens per sequence, 32 query
+ *    heads at head dim 512, 64 sequences) two splits' partials already exceed
+ *    the array, so automatic splits step down to one split and the call runs
+ *    at the unsplit kernel's speed.
  * This entry point has no counterpart on the source pages: it is a deployment
  * convenience of this library.
  */
@@ -270,31 +276,6 @@ int fp8pa_kernel_launches(int batch, int total_q, int max_seqlen_q, int num_head
                           int head_dim, int q_dtype, int max_pages_per_seq, int window_left, int num_splits);
 
 /*
- * fp8pa_set_timing_events — profiling hook for the calling host thread.  When
- * both are non-NULL (cudaEvent_t handles), later fp8_paged_attn_fwd calls on
- * this thread record `start` on their stream just before the first attention
- * kernel and `stop` just after the last one, so the caller can time the
- * attention kernels alone.  NULL, NULL turns it off.
- */
-void fp8pa_set_timing_events(void* start_event, void* stop_event);
-
-/*
- * fp8pa_set_ctas_per_sm — tuning hook: 1 or 2 forces that many attention CTAs
- * per SM where the kernel variant supports it; 0 restores the automatic choice
- * (two co-resident CTAs for E4M3 Q with 16-row tiles, else one).
- */
-void fp8pa_set_ctas_per_sm(int ctas);
-
-/*
- * fp8pa_set_bf16_dequant_v — selects how the BF16-Q path treats V (K is always
- * dequantized to BF16 in-kernel and multiplied with BF16 Q on BF16 tensor
- * cores).  0 (default): V stays E4M3, exact, in an E4M3 PV MMA with P carried
- * as an E4M3 hi/lo pair (about BF16's 8 significant bits).  1: V is also
- * dequantized to BF16 in shared memory and PV is a BF16 MMA with BF16 P.
- */
-void fp8pa_set_bf16_dequant_v(int on);
-
-/*
  * fp8pa_get_device_status — enqueue on `stream` a copy of the current device's
  * status word (FP8PA_DEV_* bits accumulated by earlier launches) into
  * *host_status, which must be pinned host memory; the value is valid once the
@@ -307,26 +288,6 @@ int fp8pa_reset_device_status(fp8pa_stream_t stream);
 
 /* fp8pa_last_error — message for the last non-OK status returned on this host thread. */
 const char* fp8pa_last_error(void);
-
-/*
- * fp8pa_set_wait_limit — test hook.  Sets the iteration cap of every bounded
- * pipeline wait in later launches (0 restores the default).  A tiny cap makes
- * waits run out, which exercises the timeout path: the kernel sets
- * FP8PA_DEV_TIMEOUT, drains its own copies and MMAs, frees its tensor memory
- * and returns; results of that launch are undefined.
- */
-void fp8pa_set_wait_limit(unsigned int max_iterations);
-
-/*
- * fp8pa_set_stall_injection — test hook (0 = off, the default).  While on, the
- * MMA-issuing thread of every attention CTA of later launches first waits on a
- * barrier that nothing ever arrives on, so that wait always runs out (after the
- * wait limit above or about two seconds, whichever comes first).  The launch then
- * takes the timeout path described above: FP8PA_DEV_TIMEOUT is set, the call
- * itself returns OK, results of that launch are undefined, and the CUDA
- * context stays usable.
- */
-void fp8pa_set_stall_injection(int on);
 
 #ifdef __cplusplus
 }

@@ -6,14 +6,15 @@ import os
 import re
 
 import pytest
+import torch
 
 import fp8_paged_attention_gb300 as fp8pa
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _declared_functions():
-    txt = open(os.path.join(ROOT, "include", "fp8pa.h")).read()
+def _declared_functions(header="fp8pa.h"):
+    txt = open(os.path.join(ROOT, "include", header)).read()
     txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:int|size_t|void|const char\*)\s+(\w+)\s*\(", txt, flags=re.M)))
 
@@ -22,9 +23,16 @@ def test_library_exports_every_declared_symbol():
     lib = fp8pa.load_library()
     names = _declared_functions()
     assert {"fp8_paged_attn_fwd", "quantize_q_fp8", "fp8pa_workspace_size"} <= set(names)
-    for n in names:
+    hooks = _declared_functions("fp8pa_testing.h")
+    assert {"fp8pa_set_wait_limit", "fp8pa_set_bf16_dequant_v"} <= set(hooks)
+    for n in names + hooks:
         assert hasattr(lib, n), n
         assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_product_header_has_no_process_wide_switch():
+    # tuning and test hooks live in fp8pa_testing.h, not in the product interface
+    assert not [n for n in _declared_functions() if n.startswith("fp8pa_set_")]
 
 
 def _fwd(**kw):
@@ -89,8 +97,17 @@ def test_workspace_and_splits_are_host_functions():
     assert fp8pa.num_splits(8, 8, 1, 32, 4, 512, E4M3, 144, -1, 0) > 1
     assert fp8pa.num_splits(64, 64, 1, 32, 4, 512, E4M3, 144, -1, 0) == 1
     # 32-row tiles (4 verify tokens x 8 heads) with 1-4 waves of long units: the split count whose
-    # item waves fill the last one best (64 x 4 units on 152 SMs: 4 splits, 6.7 waves)
-    assert fp8pa.num_splits(64, 256, 4, 32, 4, 512, BF16, 448, -1, 0) == 4
+    # item waves fill the last one best, with a 2 % cost per extra split (64 x 4 units on 152 SMs:
+    # 4 splits, 6.7 waves).  The SM count is the visible device's (152 on GB300, and without a device).
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+    units = 64 * 4
+    if sms <= units < 4 * sms:
+        costs = {s: -(-units * s // sms) / s * (1 + 0.02 * (s - 1)) for s in range(1, 9)}
+        expect = min(costs, key=lambda s: (costs[s], s))
+        assert fp8pa.num_splits(64, 256, 4, 32, 4, 512, BF16, 448, -1, 0) == expect
+        if sms == 152:
+            assert expect == 4
+    assert fp8pa.num_splits(64, 256, 4, 32, 4, 512, BF16, 448, -1, 0) > 1
     # 16-row decode tiles with as many units stay whole, and so do 32-row tiles past four waves
     assert fp8pa.num_splits(64, 64, 1, 32, 4, 512, BF16, 144, -1, 0) == 1
     assert fp8pa.num_splits(160, 640, 4, 32, 4, 512, BF16, 448, -1, 0) == 1
