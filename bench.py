@@ -4,11 +4,19 @@
 One step = one pass of the whole hot path over one batch: Q -> E4M3 (FP8-MMA
 workloads), the device-side plan, the attention kernel(s) and the split-KV
 combine, through the library's C ABI.  Inputs are resident in HBM when the
-timed region starts.  The metric is KV-cache bytes read per second
-(algorithmic bytes: the K and V rows of every (sequence, KV head) visible
-key range, counted once), the decode roofline.  The kv_write_* workloads
-time the paged KV-cache write instead (bf16 K/V read plus E4M3 bytes written,
-per second).
+timed region starts.  Decode, verify and mixed batches are measured in
+KV-cache bytes read per second (algorithmic bytes: the K and V rows of every
+(sequence, KV head) visible key range, counted once), the decode roofline;
+the 4096-token chunk alone (chunk_* workloads) in TFLOP/s of visible QK^T and
+PV work against the dense tensor peak.  The kv_write_* workloads time the
+paged KV-cache write instead (bf16 K/V read plus E4M3 bytes written, per
+second), lse_combine_* the merge of DCP partials.
+
+The default workload is the largest one that fits one GPU: the chunked-prefill
+mixed batch at head dim 512 (4096-token chunk on 4096 cached keys plus 4032
+decode sequences, BF16 Q, 71.9 GB of K/V read per step).  A one-GPU run then
+also measures every other attention workload and reports each in the line's
+per_config block (kernel time, roofline fraction, clocks).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
@@ -39,7 +47,7 @@ if ROOT not in sys.path:
 
 import synth  # noqa: E402
 
-DEFAULT_CONFIG = "swa_decode_hd256"
+DEFAULT_CONFIG = "mixed_hd512_causal"
 METRIC = "paged FP8 attn: prefill TFLOP/s & decode KV GB/s, % of GB300 roofline"
 KERNEL_SOURCES = ["attn_kernel.cuh", "attn_prefill.cuh", "common.cuh", "ptx.cuh", "attn_launch.cuh"]
 KV_WRITE_SOURCES = ["kv_cache_write.cu", "quant_e4m3.cuh"]
@@ -84,16 +92,21 @@ def ncu_traffic(config: str, sources=None):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling around the timed region.  Samples
+    carry nvidia-smi's own timestamp; mark() brackets the timed region on the
+    host clock, and the summary keeps only the samples inside it (all samples
+    when the region was too short to hold one)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 25
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -101,41 +114,57 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", str(self.PERIOD_MS)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+
+    def mark(self, t0: float, t1: float):
+        """Host wall-clock times (time.time()) of the timed region's start and end."""
+        self.t0, self.t1 = t0, t1
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, smax, reasons = [], 0.0, set()
+        import datetime
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         try:
             with open(self.path) as f:
                 for line in f:
                     parts = [p.strip() for p in line.split(",")]
-                    if len(parts) < 9:
+                    if len(parts) < 10:
                         continue
                     try:
-                        sm.append(float(parts[1]))
-                        smax = max(smax, float(parts[2]))
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                        sm, smax = float(parts[2]), float(parts[3])
                     except ValueError:
                         continue
-                    for n, v in zip(names, parts[5:9]):
-                        if v.lower() == "active":
-                            reasons.add(n)
+                    act = {n for n, v in zip(names, parts[6:10]) if v.lower() == "active"}
+                    rows.append((ts, sm, smax, act))
             os.unlink(self.path)
         except Exception:
             return None
-        if not sm:
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+        window = "timed region"
+        if self.t0 is not None:
+            inside = [r for r in rows if self.t0 <= r[0] <= self.t1]
+            if inside:
+                rows_used = inside
+            else:
+                rows_used, window = rows, "whole sampler run (timed region shorter than the sampling period)"
+        else:
+            rows_used, window = rows, "whole sampler run"
+        reasons = set().union(*[r[3] for r in rows_used])
+        return {"sm_mhz": statistics.median(r[1] for r in rows_used), "sm_max_mhz": max(r[2] for r in rows_used),
+                "reasons": sorted(reasons), "samples": len(rows_used), "period_ms": self.PERIOD_MS,
+                "window": window}
 
 
 def unit_bytes_of(w: synth.Workload, units):
@@ -356,16 +385,38 @@ def job_rate(work_per_step: float, world: int, steps: int, ms_total: float, tflo
 
 # ------------------------------------------------------------------ GPU leg
 
-def run_ours(args):
-    rank, local_rank, world = dist_env()
+def unique_kv_bytes(w: synth.Workload) -> int:
+    """K+V bytes of the distinct physical pages that visible keys sit in,
+    counting each page's visible slots once however many sequences share it
+    (the speculative-verify batch's prefix pages are shared by every sequence)."""
+    slots = {}
+    for b in range(w.batch):
+        span = synth._seq_visible_span(int(w.lq[b]), int(w.lk[b]), w.window_left, w.causal)
+        if span is None:
+            continue
+        lo, hi = span
+        for j in range(lo // synth.PAGE, hi // synth.PAGE + 1):
+            a, e = max(lo, j * synth.PAGE), min(hi, j * synth.PAGE + synth.PAGE - 1)
+            phys = int(w.bt[b, j])
+            slots[phys] = max(slots.get(phys, 0), e - a + 1)
+    return sum(slots.values()) * w.num_heads_kv * w.head_dim * 2
+
+
+# The workloads the default run measures after its headline line, each in one
+# entry of the line's per_config block: the decode and verify configurations,
+# the other mixed batches, the 4096-token chunk alone (prefill, tensor-bound)
+# and the tiny prefill.
+PER_CONFIG = ["swa_decode_hd256", "full_decode_hd512_bf16q", "full_decode_hd512_fp8q", "spec_verify_hd512",
+              "mixed_hd256_swa", "mixed_hd512_causal", "mixed_hd512_causal_fp8q", "chunk_hd256_swa",
+              "chunk_hd512_causal", "chunk_hd512_causal_fp8q", "tiny_prefill_hd256"]
+
+
+def time_workload(w: synth.Workload, args, dev, world: int, steps: int, warmup: int, with_e2e: bool):
+    """Times `steps` forward steps of one workload (after `warmup` untimed
+    ones) with inputs resident, the attention kernels alone on CUDA events, and
+    optionally the end-to-end loop through the public call with host buffers.
+    Returns a dict of the measurements."""
     import fp8_paged_attention_gb300 as fp8pa  # the CUDA library; raises if it cannot load
-    torch.cuda.set_device(local_rank)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
-    dev = torch.device("cuda", local_rank)
-    fp8pa.set_ctas_per_sm(args.ctas_per_sm)
-    w = synth.make_config(args.config, device=dev)
     stream = torch.cuda.current_stream()
     qd = torch.tensor([w.q_descale], dtype=torch.float32, device=dev)
     kd = torch.tensor([w.k_descale], dtype=torch.float32, device=dev)
@@ -415,7 +466,7 @@ def run_ours(args):
         o, l = ol_rot[i % n_rot]
         return (q_rot[i % n_rot], w.block_table, w.cu_seqlens_q, w.seqused_k, o, l, i)
 
-    for i in range(args.warmup):
+    for i in range(warmup):
         step(*args_dev(i))
     torch.cuda.synchronize()
 
@@ -424,55 +475,67 @@ def run_ours(args):
             torch.distributed.barrier()
 
     # ---------------- device-resident timed region
-    k_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    k_stop = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    k_start = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    k_stop = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for e in k_start + k_stop:
         e.record(stream)  # torch creates the CUDA event on first record; the library re-records it
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
     barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.2)
+    h0 = time.time()
     t_start.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         fp8pa.set_timing_events(k_start[i], k_stop[i])
-        step(*args_dev(args.warmup + i))
+        step(*args_dev(warmup + i))
     fp8pa.set_timing_events(None, None)
     t_stop.record(stream)
     torch.cuda.synchronize()
+    clocks.mark(h0, time.time())
     barrier()
     clock_info = clocks.stop()
     ms_total = t_start.elapsed_time(t_stop)
     k_ms = [a.elapsed_time(b) for a, b in zip(k_start, k_stop)]
     ms_total = slowest_rank_ms(ms_total, world, dev)
-    ms_step = ms_total / args.steps
     kv_bytes = w.kv_bytes_algorithmic()
     peaks = measured_peaks()
     k_avg_ms = sum(k_ms) / len(k_ms)
     tensor_bound = w.name.startswith("chunk_")
+    # prefill-class row tiles with E4M3 Q run the rows-on-lanes prefill kernel, all others attn_fwd_kernel
+    prefill_tiles = w.max_seqlen_q * (hq // hkv) > 32
+    if w.fp8_q and prefill_tiles:
+        kernel = "attn_prefill_kernel" if w.name.startswith("chunk_") else \
+            "attn_fwd_kernel (decode rows) + attn_prefill_kernel (chunk rows)"
+    else:
+        kernel = "attn_fwd_kernel"
     if tensor_bound:
         # a prefill chunk alone: causal/window-visible QK^T + PV flops against the dense tensor peak
         flops = w.flops_algorithmic()
         unit = "TFLOP/s"
-        value = job_rate(flops, world, args.steps, ms_total, True)
+        value = job_rate(flops, world, steps, ms_total, True)
         achieved = flops / (k_avg_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"] * (2.0 if w.fp8_q else 1.0)
         peak_src = (peaks["source"] + " MEASURED_PEAKS.json bf16_tflops (burst)" +
                     (" x 2, the nominal FP8/BF16 dense ratio" if w.fp8_q else ""))
         roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(w.name),
-                    # prefill tiles with E4M3 Q run the rows-on-lanes kernel
-                    "kernel": "attn_prefill_kernel" if w.fp8_q else "attn_fwd_kernel",
-                    "kernel_ms": round(k_avg_ms, 5), "peak_source": peak_src}
+                    "kernel": kernel, "kernel_ms": round(k_avg_ms, 5), "peak_source": peak_src}
     else:
         unit = "GB/s"
-        value = job_rate(kv_bytes, world, args.steps, ms_total, False)
+        value = job_rate(kv_bytes, world, steps, ms_total, False)
         achieved = kv_bytes / (k_avg_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": unit,
                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(w.name),
-                    "kernel": "attn_fwd_kernel", "kernel_ms": round(k_avg_ms, 5),
+                    "kernel": kernel, "kernel_ms": round(k_avg_ms, 5),
                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}
+        ub = unique_kv_bytes(w)
+        if ub < kv_bytes:
+            # pages shared by several sequences: their bytes can come from L2 after the first read
+            roofline["unique_bytes"] = ub
+            roofline["unique_achieved"] = round(ub / (k_avg_ms * 1e-3) / 1e9, 2)
+            roofline["unique_frac"] = round(ub / (k_avg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
 
     def rate(n_steps, ms):
         work = w.flops_algorithmic() if tensor_bound else kv_bytes
@@ -485,7 +548,7 @@ def run_ours(args):
     # neighbouring steps: two device buffer sets, ordered by events.  The timed
     # region runs from the first upload to the end of the last read-back.
     e2e = None
-    if not args.no_e2e:
+    if with_e2e:
         pin = lambda t: t.cpu().pin_memory()  # noqa: E731
         h_q, h_bt, h_cu, h_su = pin(w.q), pin(w.block_table), pin(w.cu_seqlens_q), pin(w.seqused_k)
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -522,9 +585,9 @@ def run_ours(args):
                     h_lse.copy_(b["lse"], non_blocking=True)
                     b["back"].record(down_stream)
 
-        e2e_run(max(3, args.warmup // 4), True)
+        e2e_run(max(3, warmup // 4), True)
         torch.cuda.synchronize()
-        n_e2e = max(10, args.steps // 4)
+        n_e2e = max(10, steps // 4)
         barrier()
         a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(up_stream)
@@ -538,29 +601,70 @@ def run_ours(args):
                "ms_per_step": round(e_ms / n_e2e, 5),
                "note": "K/V cache is resident state; per step Q, block table and lengths go up and out and lse "
                        "come back, on copy streams overlapping the neighbouring steps' compute"}
+    return dict(value=value, unit=unit, ms_per_step=ms_total / steps, roofline=roofline, e2e=e2e, clocks=clock_info,
+                splits=splits, launches=launches, l2_note=l2_note, kv_bytes=kv_bytes, tensor_bound=tensor_bound)
 
+
+def config_of(w: synth.Workload, r: dict, world: int, sinks: bool) -> dict:
+    return {"workload": w.name, "batch": w.batch, "total_q": w.total_q, "num_heads_q": w.num_heads_q,
+            "num_heads_kv": w.num_heads_kv, "head_dim": w.head_dim, "window_left": w.window_left,
+            "causal": w.causal, "q": "e4m3" if w.fp8_q else "bf16", "kv": "e4m3, 64-token pages",
+            "num_splits": r["splits"], "kv_bytes_per_step": r["kv_bytes"],
+            "flops_per_step": w.flops_algorithmic() if r["tensor_bound"] else None,
+            "parallelism": f"replicas x{world}", "l2": r["l2_note"], "sinks": bool(sinks)}
+
+
+def run_ours(args):
+    import gc
+
+    rank, local_rank, world = dist_env()
+    import fp8_paged_attention_gb300 as fp8pa  # the CUDA library; raises if it cannot load
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+    fp8pa.set_ctas_per_sm(args.ctas_per_sm)
+    w = synth.make_config(args.config, device=dev)
+    r = time_workload(w, args, dev, world, args.steps, args.warmup, with_e2e=not args.no_e2e)
     # ---------------- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r, cores, desc, _t = oracle_timing(w, budget_s=args.cpu_budget, tflops=tensor_bound)
-        cpu = {"value": round(r, 6), "unit": unit, "cores": cores, "kind": "oracle", "sample": desc}
-
+        rr, cores, desc, _t = oracle_timing(w, budget_s=args.cpu_budget, tflops=r["tensor_bound"])
+        cpu = {"value": round(rr, 6), "unit": r["unit"], "cores": cores, "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": round(r["value"], 3), "unit": r["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if w.fp8_q else "bf16", "data": "synthetic",
+        "config": config_of(w, r, world, args.sinks),
+        "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
+        "gpu_launches": r["launches"] * args.steps, "clocks": r["clocks"],
+    }
+    # ---------------- the other workloads of the metric, one GPU only: kernel and step rates,
+    # roofline fraction and clocks of each (no e2e loop, no CPU leg)
+    if not args.no_per_config and world == 1:
+        del w
+        gc.collect()
+        torch.cuda.empty_cache()
+        per = {}
+        steps = args.per_config_steps or args.steps
+        for name in PER_CONFIG:
+            if name == args.config:
+                continue
+            wc = synth.make_config(name, device=dev)
+            rc = time_workload(wc, args, dev, world, steps, args.warmup, with_e2e=False)
+            per[name] = {"value": round(rc["value"], 3), "unit": rc["unit"], "steps": steps,
+                         "ms_per_step": round(rc["ms_per_step"], 5), "roofline": rc["roofline"],
+                         "clocks": rc["clocks"], "gpu_launches": rc["launches"] * steps,
+                         "dtype": "e4m3" if wc.fp8_q else "bf16", "config": config_of(wc, rc, world, args.sinks)}
+            line["gpu_launches"] += rc["launches"] * (steps + args.warmup)
+            del wc
+            gc.collect()
+            torch.cuda.empty_cache()
+        line["per_config"] = per
+        line["per_config_note"] = ("measured after the headline line's timed region; gpu_launches above counts "
+                                   "the headline's timed launches plus every per-config warm-up and timed launch")
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "e4m3" if w.fp8_q else "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "total_q": w.total_q, "num_heads_q": hq,
-                       "num_heads_kv": hkv, "head_dim": D, "window_left": w.window_left, "causal": w.causal,
-                       "q": "e4m3" if w.fp8_q else "bf16", "kv": "e4m3, 64-token pages", "num_splits": splits,
-                       "kv_bytes_per_step": kv_bytes, "parallelism": f"replicas x{world}",
-                       "l2": l2_note, "sinks": bool(args.sinks)},
-            "roofline": roofline,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": launches * args.steps,
-            "clocks": clock_info,
-        }
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -608,7 +712,8 @@ def run_kv_write(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.2)
+    h0 = time.time()
     t_start.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -616,6 +721,7 @@ def run_kv_write(args):
         ev[i][1].record(stream)
     t_stop.record(stream)
     torch.cuda.synchronize()
+    clocks.mark(h0, time.time())
     if world > 1:
         torch.distributed.barrier()
     clock_info = clocks.stop()
@@ -717,7 +823,8 @@ def run_combine(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.2)
+    h0 = time.time()
     t_start.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -725,6 +832,7 @@ def run_combine(args):
         ev[i][1].record(stream)
     t_stop.record(stream)
     torch.cuda.synchronize()
+    clocks.mark(h0, time.time())
     if world > 1:
         torch.distributed.barrier()
     clock_info = clocks.stop()
@@ -787,8 +895,8 @@ def run_combine(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG,
                     choices=synth.CONFIG_NAMES + synth.KV_WRITE_CONFIG_NAMES + synth.COMBINE_CONFIG_NAMES)
@@ -798,6 +906,9 @@ def main():
     ap.add_argument("--ctas-per-sm", type=int, default=0, help="force 1 or 2 attention CTAs per SM (0 = auto)")
     ap.add_argument("--num-splits", type=int, default=0, help="split-KV count (0 = automatic)")
     ap.add_argument("--sinks", action="store_true", help="attention sinks, one logit per query head")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure only --config (by default a one-GPU run also measures the other workloads)")
+    ap.add_argument("--per-config-steps", type=int, default=0, help="timed steps per extra workload (0 = --steps)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

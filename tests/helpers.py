@@ -89,3 +89,19 @@ def lse_error(gpu_lse: np.ndarray, ref_lse: np.ndarray):
     assert np.array_equal(np.isfinite(gpu_lse), fin), "empty rows must give lse = -inf exactly"
     assert np.all(gpu_lse[~fin] == -np.inf)
     return float(np.abs(gpu_lse[fin] - ref_lse[fin]).max()) if fin.any() else 0.0
+
+
+def permute_pages(w: synth.Workload, seed: int) -> synth.Workload:
+    """The same workload with its physical pages moved by a random permutation
+    (cache rows and block-table entries together).  Pages shared by several
+    sequences stay shared; every logical page keeps its contents."""
+    n = w.num_pages
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(seed)).to(w.k_cache.device)
+    kc = torch.empty_like(w.k_cache)
+    vc = torch.empty_like(w.v_cache)
+    kc[perm] = w.k_cache
+    vc[perm] = w.v_cache
+    bt = perm.to(torch.int32)[w.block_table.long()].contiguous()
+    bt_host = bt.cpu().numpy()
+    return synth.Workload(**{**w.__dict__, "k_cache": kc, "v_cache": vc, "block_table": bt, "bt": bt_host,
+                             "poison_page": int(perm[w.poison_page])})

@@ -127,19 +127,35 @@ def test_explicit_splits_agree_and_repeat_bit_identically(fp8):
         assert torch.equal(out, out2) and torch.equal(lse, lse2)
 
 
-def test_page_permutation_is_bit_identical():
-    w = make("perm", [1, 1, 3, 40], [900, 1500, 700, 300], 32, 16, 256, 1023, True, True, seed=11)
-    out1, lse1 = run_gpu(w)
-    n = w.num_pages
-    perm = torch.randperm(n, generator=torch.Generator().manual_seed(5)).to("cuda")
-    kc = torch.empty_like(w.k_cache)
-    vc = torch.empty_like(w.v_cache)
-    kc[perm] = w.k_cache
-    vc[perm] = w.v_cache
-    bt = perm.to(torch.int32)[w.block_table.long()]
-    w2 = synth.Workload(**{**w.__dict__, "k_cache": kc, "v_cache": vc, "block_table": bt.contiguous()})
-    out2, lse2 = run_gpu(w2)
-    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+PERM_CASES = [
+    # name, lq, lk, hq, hkv, d, window_left, causal, fp8, num_splits, shared_prefix_pages
+    ("decode_swa_hd256_e4m3", [1, 1, 3, 40], [900, 1500, 700, 300], 32, 16, 256, 1023, True, True, 0, 0),
+    ("prefill_tiles_hd256_e4m3", [200, 1, 150], [400, 900, 150], 8, 4, 256, 100, True, True, 0, 0),
+    ("decode_hd512_bf16q", [1] * 5, [90, 700, 1300, 2100, 3000], 32, 4, 512, -1, True, False, 0, 0),
+    ("prefill_tiles_hd512_bf16q", [70, 1, 129], [300, 500, 129], 16, 2, 512, -1, True, False, 0, 0),
+    ("prefill_tiles_hd512_e4m3", [70, 1, 129], [300, 500, 129], 16, 2, 512, -1, True, True, 0, 0),
+    ("decode_hd512_e4m3_split3", [1] * 4, [700, 1300, 2100, 3000], 32, 4, 512, -1, True, True, 3, 0),
+    ("decode_hd512_bf16q_split3", [1] * 4, [700, 1300, 2100, 3000], 32, 4, 512, -1, True, False, 3, 0),
+    ("verify_shared_prefix_hd512_bf16q", [4] * 6, [1400 + 64 * i for i in range(6)], 32, 4, 512, -1, True, False,
+     0, 16),
+    ("verify_shared_prefix_hd512_e4m3_split4", [4] * 6, [1400 + 64 * i for i in range(6)], 32, 4, 512, -1, True,
+     True, 4, 16),
+]
+
+
+@pytest.mark.parametrize("case", PERM_CASES, ids=[c[0] for c in PERM_CASES])
+def test_page_permutation_is_bit_identical(case):
+    """Moving the physical pages (cache rows and block table together) changes
+    no output bit on any kernel path: decode, prefill tiles of both kernels,
+    split KV with the combine, and a prefix whose pages every sequence shares."""
+    from tests.helpers import permute_pages
+    name, lq, lk, hq, hkv, d, wl, causal, fp8, ns, shared = case
+    w = make(name, lq, lk, hq, hkv, d, wl, causal, fp8, seed=11, shared_prefix_pages=shared)
+    out1, lse1 = run_gpu(w, num_splits=ns)
+    check(w, out1, lse1)
+    for seed in (5, 6):
+        out2, lse2 = run_gpu(permute_pages(w, seed), num_splits=ns)
+        assert torch.equal(out1, out2) and torch.equal(lse1, lse2), (name, seed)
 
 
 def test_per_batch_head_descales():

@@ -1,7 +1,15 @@
 """Full-size benchmark workloads on the GPU, in the launch configuration the
-benchmark times (automatic split count), checked against the oracle on
-sampled output rows: a seeded sample of sequences with every query row and
-head, plus a sample of the chunked-prefill sequence's rows."""
+benchmark times (automatic split count), checked against the oracle:
+
+* the decode and speculative-verify workloads at full parity: every query row
+  and head of every sequence;
+* the chunked-prefill mixed batches on every row of the 4096-token chunk plus
+  a seeded sample of 256 of the 4032 decode sequences, all heads (the oracle's
+  fp64 pass over all 4032 decode rows would add minutes of host time and no
+  new kernel path: the decode rows of the batch run the same tiles).
+
+The small-cache workloads are also run with their physical pages permuted,
+which must change no output bit."""
 import gc
 
 import numpy as np
@@ -10,64 +18,78 @@ import torch
 
 import oracle
 import synth
-from tests.helpers import LSE_GATE, TOL, lse_error, unit_scale_errors
+from tests.helpers import LSE_GATE, TOL, lse_error, permute_pages, unit_scale_errors
 from tests.test_gpu_attention import run_gpu
 
 pytestmark = pytest.mark.gpu
 
+DECODE_SAMPLE = 256
 
-def sampled_check(w, out, lse, n_seq=12, chunk_tokens=48, seed=0):
-    rng = np.random.default_rng(seed)
-    B = w.batch
-    seqs = sorted(set(rng.choice(B, size=min(n_seq, B), replace=False).tolist()))
-    big = [int(b) for b in np.nonzero(w.lq > 64)[0]]
-    seqs = sorted(set(seqs) - set(big))
-    sub = synth.subproblem_pages(w, seqs + big)
+
+def oracle_rows(w, seqs):
+    """Oracle out [tokens, Hq, D] and lse [Hq, tokens] for every query row and
+    head of sequences `seqs`, with the global token index of each row."""
+    sub = synth.subproblem_pages(w, seqs)
     q = sub["q"]
     if w.fp8_q:
         q = oracle.quantize_q(q, w.q_descale)
     prob = oracle.AttnProblem(q, w.fp8_q, sub["k"], sub["v"], sub["block_table"], sub["cu_seqlens_q"],
                               sub["seqused_k"], w.num_heads_kv, w.q_descale, w.k_descale, w.v_descale,
                               w.softmax_scale, w.window_left, w.causal)
-    # rows: every row of the small sequences, a sample of the big ones' tokens
-    rows_local, tok_global = [], []
-    cu = sub["cu_seqlens_q"]
-    toks = sub["tokens"]
-    for i, b in enumerate(seqs + big):
-        lt = list(range(cu[i], cu[i + 1]))
-        if b in big:
-            lt = sorted(set(rng.choice(lt, size=min(chunk_tokens, len(lt)), replace=False).tolist())
-                        | {lt[0], lt[-1]})
-        for t in lt:
-            for h in range(w.num_heads_q):
-                rows_local.append((t, h))
-                tok_global.append((int(toks[t]), h))
-    rows_local = np.array(rows_local, dtype=np.int32)
-    tok_global = np.array(tok_global, dtype=np.int64)
-    ro, rl = oracle.paged_attention(prob, rows=rows_local)
-    g = out[torch.from_numpy(tok_global[:, 0]).cuda(), torch.from_numpy(tok_global[:, 1]).cuda()].float().cpu().numpy()
-    gl = lse[torch.from_numpy(tok_global[:, 1]).cuda(), torch.from_numpy(tok_global[:, 0]).cuda()].cpu().numpy()
-    e = unit_scale_errors(g, ro, w, heads=tok_global[:, 1])
+    ro, rl = oracle.paged_attention(prob)
+    return ro, rl, sub["tokens"]
+
+
+def compare(w, out, lse, seqs):
+    ro, rl, toks = oracle_rows(w, seqs)
+    idx = torch.from_numpy(toks).to(out.device)
+    g = out.index_select(0, idx).float().cpu().numpy()
+    gl = lse.index_select(1, idx).cpu().numpy()
+    e = unit_scale_errors(g, ro, w)
     le = lse_error(gl, rl)
-    return e, le, len(rows_local)
+    return e, le, g.shape[0] * g.shape[1]
 
 
-@pytest.mark.parametrize("name", ["swa_decode_hd256", "full_decode_hd512_bf16q", "full_decode_hd512_fp8q",
-                                  "spec_verify_hd512", "mixed_hd256_swa", "mixed_hd512_causal",
-                                  "mixed_hd512_causal_fp8q"])
-def test_full_size_config_sampled(name):
+def check_full_size(name, seqs_of):
     w = synth.make_config(name, device="cuda")
     out, lse = run_gpu(w)
     assert torch.isfinite(out.float()).all()
-    e, le, n = sampled_check(w, out, lse)
-    print(f"{name}: rows={n} unit-scale max={e['max']:.3e} mean={e['mean']:.3e} raw_max={e['raw_max']:.3e} "
-          f"lse_max={le:.3e}")
+    seqs = seqs_of(w)
+    e, le, n = compare(w, out, lse, seqs)
+    print(f"{name}: sequences={len(seqs)} rows={n} unit-scale max={e['max']:.3e} mean={e['mean']:.3e} "
+          f"raw_max={e['raw_max']:.3e} lse_max={le:.3e}")
     tmax, tmean = TOL[w.fp8_q]
     assert e["max"] <= tmax and e["mean"] <= tmean, (name, e, le)
     assert le <= LSE_GATE
     # the same call again gives the same bits
     out2, lse2 = run_gpu(w)
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
-    del w, out, lse, out2, lse2
+    return w, out, lse
+
+
+@pytest.mark.parametrize("name", ["swa_decode_hd256", "full_decode_hd512_bf16q", "full_decode_hd512_fp8q",
+                                  "spec_verify_hd512"])
+def test_full_size_config_full_parity(name):
+    w, out, lse = check_full_size(name, lambda w: list(range(w.batch)))
+    # pages permuted (the verify batch's shared prefix stays shared): not one bit changes
+    out_p, lse_p = run_gpu(permute_pages(w, seed=23))
+    assert torch.equal(out, out_p) and torch.equal(lse, lse_p)
+    del w, out, lse, out_p, lse_p
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _chunk_and_sample(w):
+    rng = np.random.default_rng(0)
+    big = [int(b) for b in np.nonzero(w.lq > 64)[0]]
+    dec = [b for b in range(w.batch) if b not in big]
+    sample = sorted(rng.choice(dec, size=min(DECODE_SAMPLE, len(dec)), replace=False).tolist())
+    return sorted(big + sample)
+
+
+@pytest.mark.parametrize("name", ["mixed_hd256_swa", "mixed_hd512_causal", "mixed_hd512_causal_fp8q"])
+def test_mixed_batch_chunk_rows_and_decode_sample(name):
+    w, out, lse = check_full_size(name, _chunk_and_sample)
+    del w, out, lse
     gc.collect()
     torch.cuda.empty_cache()
