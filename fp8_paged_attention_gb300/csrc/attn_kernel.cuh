@@ -32,9 +32,18 @@
 //
 // Paths (template parameter kPath):
 //  kPathE4M3    E4M3 Q: QK^T and PV are kind::f8f6f4 MMAs.
-//  kPathBf16    BF16 Q: K dequantized to BF16, QK^T a kind::f16 MMA with BF16 Q;
-//               V stays E4M3 (exact) in a kind::f8f6f4 PV MMA.
-//  kPathBf16DqV BF16 Q: K and V dequantized to BF16, both MMAs kind::f16, P in BF16.
+//  kPathBf16    BF16 Q: K dequantized to F16 (one conversion per pair of codes,
+//               exact), QK^T a kind::f16 MMA on F16 operands; V stays E4M3
+//               (exact) in a kind::f8f6f4 PV MMA.
+//  kPathBf16DqV BF16 Q: K dequantized as above, V dequantized to BF16, PV a
+//               kind::f16 MMA with BF16 P.
+// On both BF16-Q paths the dequant warps first convert each item's BF16 Q tile
+// in place to F16 scaled by a per-row power of two 2^k_r that puts the row's
+// largest magnitude in [2^14, 2^15): every BF16 value down to 2^-28 of the
+// row's largest is then exact in F16 (8 significant bits fit F16's 11), smaller
+// ones keep an absolute error below 2^-39 of it, far under the f32
+// accumulation's own rounding.  The softmax multiplies row r's scores by
+// 2^-k_r, folded into its per-row score scale.
 // Where the PV MMA is E4M3, P is requantized to E4M3 after a 2^4 pre-scale
 // (P' = 2^(x - m + 4), at most 256 under the lazy rescale below, keeping small
 // weights out of E4M3's subnormal range) as a pair on one scale:
@@ -85,7 +94,8 @@ struct AttnCfg {
   static constexpr int kSmemLimit = kCtas == 1 ? 232448 : 115712;
   // barriers and the item ring (< 1 KB), then per-row state: ooff[N] (8 bytes),
   // red[2][4][N], lred[4][N] and 4 x [N] floats
-  static constexpr int kCtrlBytes = 1536 + 72 * N + 80;
+  // (+ on the BF16-Q paths: per-row score scales of the two Q buffers, 8 * N bytes)
+  static constexpr int kCtrlBytes = 1536 + 72 * N + 80 + (kDq ? 8 * N : 0);
   // Two CTAs per SM: one Q buffer, and the room goes to the stage ring (the next
   // item's Q loads while this item's last tiles and epilogue run).
   static constexpr int kQBufs =
@@ -109,7 +119,12 @@ struct AttnCfg {
   static constexpr int kSmemBytes = kFixed + kStages * kStageBytes;
   // TMEM columns: S (2 buffers of N), O (kDC chunks of N), BF16 K (2 slots of 64 columns = 128 dims)
   static constexpr int kKCol = 2 * N + kDC * N;
-  static constexpr int kTmemUsed = kKCol + (kDq ? 128 : 0);
+  // F16 K chunks in TMEM (64 columns each): as many slots as fit, up to four, so
+  // that the dequant warps can run ahead of the QK^T MMAs
+  static constexpr int kKSlotsFit = (512 / kCtas - kKCol) / 64;
+  static constexpr int kKSlots = kDq ? (kKSlotsFit > 4 ? 4 : kKSlotsFit) : 0;
+  static_assert(!kDq || kKSlots >= 2, "TMEM for the F16 K slots");
+  static constexpr int kTmemUsed = kKCol + 64 * kKSlots;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
                                         : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512 && kCtas * kTmemCols <= 512, "TMEM");
@@ -243,6 +258,23 @@ __device__ __forceinline__ uint32_t v_stage_offset(int u, int n, int dc) {
   return (u < n - 1) ? (uint32_t)(2 * (u + 1) * dc) : (uint32_t)((2 * n - 1) * dc);
 }
 
+// Two E4M3 codes (low byte first) -> F16x2, exact.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint16_t v) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+  return h;
+}
+
+// BF16x2 (low half first) times f, rounded to F16x2.  f is a power of two, so
+// the product is exact in f32; the rounding to F16 is exact for every value in
+// F16's normal range.
+__device__ __forceinline__ uint32_t bf16x2_scaled_to_f16x2(uint32_t w, float f) {
+  const float lo = __uint_as_float(w << 16) * f, hi = __uint_as_float(w & 0xFFFF0000u) * f;
+  uint32_t h;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+  return h;
+}
+
 __device__ __forceinline__ uint32_t cvt_e4m3x2_bf16x2(uint16_t v) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
   float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
@@ -298,9 +330,11 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
   uint64_t* never = drain + 2;    // nothing arrives on it: the stall-injection test hook waits here
   uint64_t* item_full = never + 1;
   uint64_t* item_empty = item_full + kItemSlots;
-  uint64_t* kt_full = item_empty + kItemSlots;  // BF16 K slot in TMEM written (dequant -> MMA)
-  uint64_t* kt_empty = kt_full + 2;             // BF16 K slot consumed (MMA commit -> dequant)
-  ItemSlot* islot = reinterpret_cast<ItemSlot*>(kt_empty + 2);
+  uint64_t* kt_full = item_empty + kItemSlots;  // F16 K slot in TMEM written (dequant -> MMA)
+  uint64_t* kt_empty = kt_full + 4;             // F16 K slot consumed (MMA commit -> dequant)
+  uint64_t* q_conv = kt_empty + 4;              // [QB] Q tile converted to scaled F16 (dequant -> MMA, softmax)
+  uint64_t* srow_empty = q_conv + 2;            // [2] an item's row scales read (softmax -> dequant)
+  ItemSlot* islot = reinterpret_cast<ItemSlot*>(srow_empty + 2);
   // [N] element offset of each row's output (in out, or in o_part for a split)
   long long* ooff_s = reinterpret_cast<long long*>((reinterpret_cast<uintptr_t>(islot + kItemSlots) + 15) & ~(uintptr_t)15);
   float* red = reinterpret_cast<float*>(ooff_s + N);  // [2][4][N] per-warp tile maxima
@@ -309,7 +343,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
   float* a_s = m_s + N;                               // [N] rescale factor of this tile
   float* nmsub_s = a_s + N;                           // [N] exponent offset: P' = 2^(x + nmsub)
   float* inv_s = nmsub_s + N;                         // [N] output scale v_descale / l
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(inv_s + N);
+  float* srow_s = inv_s + N;                          // BF16-Q paths: [2][N] score scale of each row
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(srow_s + (kDq ? 2 * N : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -317,15 +352,20 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&ring_full[i], 1);
-      mbar_init(&ring_empty[i], 1);  // one MMA commit or one arrive for the four dequant warps
+      // one MMA commit, or one arrive of each of the four dequant warps for the stages they consume
+      mbar_init(&ring_empty[i], (kDq && (!kSplit || i < SK)) ? 4 : 1);
     }
     for (int i = 0; i < SB; ++i) {
-      mbar_init(&bf_full[i], 1);
+      mbar_init(&bf_full[i], 4);
       mbar_init(&bf_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&kt_full[i], 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&kt_full[i], 4);
       mbar_init(&kt_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_conv[i], 4);
+      mbar_init(&srow_empty[i], 4 * C::kNW);
     }
     for (int i = 0; i < QB; ++i) {
       mbar_init(&q_full[i], 1);
@@ -458,7 +498,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       };
       const bool do_qk = !C::kTwoIssuers || warp == 1;
       const bool do_pv = !C::kTwoIssuers || warp == 2;
-      constexpr uint32_t idesc_qk = make_idesc(kQ8 ? kFmtE4M3 : kFmtBF16, kKMajor, kKMajor, 128, N);
+      constexpr uint32_t idesc_qk = make_idesc(kQ8 ? kFmtE4M3 : kFmtF16, kKMajor, kKMajor, 128, N);
       constexpr uint32_t idesc_pv = make_idesc(kP8 ? kFmtE4M3 : kFmtBF16, kMNMajor, kMNMajor, 128, N);
       // E4M3 stages: idx = stage-stream position (one ring), or kq / vq = K and V
       // ring positions (split rings); kidx: BF16 K chunks in TMEM; bidx: BF16 V
@@ -482,7 +522,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         if (p.inject_stall && !(ok = wait_all(never, 0))) break;
         if (it.t1 <= it.t0) continue;
         const int qb = qit % QB;
-        if (do_qk && !(ok = wait_all(&q_full[qb], (qit / QB) & 1))) break;
+        // E4M3 Q straight from the TMA; BF16 Q once the dequant warps have converted it
+        if (do_qk && !(ok = wait_all(kDq ? &q_conv[qb] : &q_full[qb], (qit / QB) & 1))) break;
         tc_fence_after();
         const uint32_t qaddr = smem_u32(qbuf + qb * C::kQBytes);
         // S^T(gg) = K . Q^T into S buffer gg & 1
@@ -506,9 +547,10 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
               }
               ++kpos;
             } else {
-              // BF16 K chunk (128 dims = 64 columns) in TMEM slot kidx & 1, written by the dequant warps
-              const uint32_t ks = kidx & 1;
-              if (!wait_all(&kt_full[ks], (kidx >> 1) & 1)) return false;
+              // F16 K chunk (128 dims = 64 columns) in TMEM slot kidx % kKSlots, written by the dequant warps
+              constexpr uint32_t KS = C::kKSlots > 0 ? C::kKSlots : 1;
+              const uint32_t ks = kidx % KS;
+              if (!wait_all(&kt_full[ks], (kidx / KS) & 1)) return false;
               tc_fence_after();
               const uint32_t a_t = tmem + C::kKCol + ks * 64;
               if (leader) {
@@ -624,6 +666,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
     // sends the tile down the exact-maximum path.
     constexpr float kNoKeyOffset = 1e30f;
     uint32_t g = 0, sbase = 0, tails = 0;  // sbase: first stage of the item (stream, or V ring)
+    uint32_t qi = 0;                        // non-empty items so far (Q buffer and row-scale ring position)
     bool aborted = false;
     for (uint32_t ik = 0; !aborted; ++ik) {
       const uint32_t is = ik % kItemSlots;
@@ -675,6 +718,21 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       const float kd = load_descale(p.k_descale, p, it);
       const float vd = load_descale(p.v_descale, p, it);
       const float scale = p.softmax_scale_log2 * kd * (kQ8 && p.q_descale ? *p.q_descale : 1.0f);
+      // BF16-Q paths: row r's scores carry the Q tile's 2^k_r; its score scale
+      // srow[r] = scale * 2^-k_r comes from the dequant warps with the converted Q
+      const uint32_t qb = qi % QB, sr = qi & 1;  // Q buffer, row-scale ring slot
+      const float* srow = srow_s + sr * N;
+      if (kDq) {
+        bool qok = pwait(&q_conv[qb], (qi / QB) & 1, lim, abort_flag);
+        qok = __all_sync(0xFFFFFFFFu, qok);
+        if (!qok) flag_timeout(p, abort_flag);
+        if (bar_red_or(bar_a, 128, !qok)) {
+          aborted = true;
+          break;
+        }
+      }
+      ++qi;
+      auto rscale = [&](int n) { return kDq ? srow[r0 + n] : scale; };
       if (wt < NR) {
         m_s[r0 + wt] = NEG_INF;
         a_s[r0 + wt] = 1.0f;
@@ -736,7 +794,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
             float pm = 0.f;
 #pragma unroll
             for (int n = 0; n < NR; n += 2) {
-              const float2 t = __ffma2_rn(make_float2(x[n], x[n + 1]), make_float2(scale, scale),
+              const float2 t = __ffma2_rn(make_float2(x[n], x[n + 1]), make_float2(rscale(n), rscale(n + 1)),
                                           make_float2(nmsub_s[r0 + n], nmsub_s[r0 + n + 1]));
               x[n] = ex2(t.x);
               x[n + 1] = ex2(t.y);
@@ -757,7 +815,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           if (u > 0) load_scores();
 #pragma unroll
           for (int n = 0; n < NR; n += 2) {
-            const float2 t = __fmul2_rn(make_float2(x[n], x[n + 1]), make_float2(scale, scale));
+            const float2 t = __fmul2_rn(make_float2(x[n], x[n + 1]), make_float2(rscale(n), rscale(n + 1)));
             x[n] = t.x;
             x[n + 1] = t.y;
           }
@@ -897,6 +955,10 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         }
       }
       if (aborted) break;
+      if (kDq) {  // this item's row scales are no longer read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&srow_empty[sr]);
+      }
       sbase += (kSplit ? 1 : 2) * n_t * DC;
       // ---------------- epilogue: O / l, lse
       // The row sums, scales and lse do not depend on O: they are formed while
@@ -966,30 +1028,35 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       if (lane == 0) mbar_arrive(o_empty);
     }
   } else {
-    // ------------------------------------------------------------------ E4M3 -> BF16 dequant (BF16-Q paths)
+    // ------------------------------------------------------------------ dequant warps (BF16-Q paths)
+    // Each of the four warps works on its own quarter of the rows and keys (its
+    // TMEM lane quarter) and meets the other roles only through mbarriers: per
+    // item it converts its rows of the BF16 Q tile in place to F16 scaled by
+    // 2^k_r and publishes their score scales; per K chunk it writes its 32 key
+    // rows as F16 into a TMEM slot (the A operand of QK^T); on the literal path
+    // it also writes its part of each V tile as BF16 into shared memory.
     if (kDq) {
-      const int dt = threadIdx.x - 32 * C::kDqWarp0;  // 0..127
-      constexpr uint32_t kDqBar = 1 + 2 * C::kNW;       // named barrier of the four dequant warps
       const int quarter = warp & 3;
+      const int wq = warp - C::kDqWarp0;  // 0..3
       const int row = quarter * 32 + lane;  // this thread's key row = its TMEM lane
       const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-      // idx: stage stream position (literal path, one ring) or K ring position (split rings)
-      uint32_t idx = 0, kidx = 0, bidx = 0;
+      constexpr uint32_t KS = C::kKSlots > 0 ? C::kKSlots : 1;
       constexpr uint32_t KR = kSplit ? SK : S;
+      // Q conversion: warp wq owns rows [wq * N / 4, (wq + 1) * N / 4); QP lanes per row,
+      // each taking every QP-th 128-byte chunk of its row
+      constexpr int QP = 128 / N;
+      constexpr int kQCh = C::kQChunks;
+      static_assert(!kDq || kQCh % QP == 0, "Q chunks per lane");
+      const int qrow = wq * (N / 4) + lane / QP, qpart = lane % QP;
+      // idx: stage stream position (literal path, one ring) or K ring position (split rings)
+      uint32_t idx = 0, kidx = 0, bidx = 0, qi = 0;
       bool ok = true;
-      // the four dequant warps hand a stage back with a single arrive
-      auto release = [&](uint64_t* a, uint64_t* b) {
-        named_bar_sync(kDqBar, 128);
-        if (dt == 0) {
-          mbar_arrive(a);
-          mbar_arrive(b);
-        }
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xFFFFFFFFu, pwait(bar, parity, lim, abort_flag));
       };
       for (uint32_t ik = 0; ok; ++ik) {
         const uint32_t is = ik % kItemSlots;
-        // every wait decision is a vote of all four dequant warps: they share named barrier kDqBar
-        ok = !bar_red_or(kDqBar, 128, !pwait(&item_full[is], (ik / kItemSlots) & 1, lim, abort_flag));
-        if (!ok) break;
+        if (!(ok = wait_all(&item_full[is], (ik / kItemSlots) & 1))) break;
         const Item it = islot[is].it;
         const bool valid = islot[is].valid != 0;
         __syncwarp();
@@ -997,13 +1064,57 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         if (!valid) break;
         if (it.t1 <= it.t0) continue;
         const int n = it.t1 - it.t0;
-        // K tile u: each chunk (128 dims) -> BF16 in TMEM slot kidx & 1, one key row per thread
+        // ---- this warp's rows of the Q tile: BF16 -> F16 x 2^k_r in place, score scales out
+        {
+          const uint32_t qb = qi % QB, sr = qi & 1;  // Q buffer, row-scale ring slot (two slots)
+          ok = wait_all(&q_full[qb], (qi / QB) & 1) && wait_all(&srow_empty[sr], ((qi >> 1) & 1) ^ 1);
+          if (!ok) break;
+          uint8_t* qrow_base = qbuf + qb * C::kQBytes + qrow * 128;
+          uint32_t mx = 0;  // largest |q| of the row's bits (positive BF16 bit patterns order like their values)
+#pragma unroll 1
+          for (int c = qpart; c < kQCh; c += QP) {
+            const uint4* src = reinterpret_cast<const uint4*>(qrow_base + c * N * 128);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint4 v = src[j];
+              mx = __vmaxu2(mx, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                         __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
+            }
+          }
+          mx = max(mx & 0xFFFFu, mx >> 16);
+#pragma unroll
+          for (int o = 1; o < QP; o <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+          // 2^k_r puts the row's largest magnitude in [2^14, 2^15); an all-zero row keeps k = 0
+          const int e = (int)(mx >> 7);
+          const int k = mx == 0 ? 0 : min(120, 141 - e);
+          const float f = __int_as_float((k + 127) << 23);
+#pragma unroll 1
+          for (int c = qpart; c < kQCh; c += QP) {
+            uint4* src = reinterpret_cast<uint4*>(qrow_base + c * N * 128);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint4 v = src[j];
+              uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) w[i] = bf16x2_scaled_to_f16x2(w[i], f);
+              src[j] = v;
+            }
+          }
+          if (qpart == 0) {
+            const float scale = p.softmax_scale_log2 * load_descale(p.k_descale, p, it) * 1.0f;
+            srow_s[sr * N + qrow] = scale * __int_as_float((127 - k) << 23);
+          }
+          fence_proxy_async_smem();  // the MMA reads the converted tile through the async proxy
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&q_conv[qb]);
+          ++qi;
+        }
+        // K tile u: each chunk (128 dims) -> F16 in TMEM slot kidx % KS, one key row per thread
         auto convert_k = [&](int u) -> bool {
           for (int c = 0; c < DC; ++c) {
-            const uint32_t slot = idx % KR, ks = kidx & 1;
-            const bool w_ok = pwait(&ring_full[slot], (idx / KR) & 1, lim, abort_flag) &&
-                              pwait(&kt_empty[ks], ((kidx >> 1) & 1) ^ 1, lim, abort_flag);
-            if (bar_red_or(kDqBar, 128, !w_ok)) return false;
+            const uint32_t slot = idx % KR, ks = kidx % KS;
+            if (!wait_all(&ring_full[slot], (idx / KR) & 1) || !wait_all(&kt_empty[ks], ((kidx / KS) & 1) ^ 1))
+              return false;
             tc_fence_after();
             const uint8_t* src = ring + slot * kStageBytes + row * 128;
             uint4 vin[8];
@@ -1019,29 +1130,34 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
                 const uint32_t in[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                  o[jj * 8 + 2 * i] = cvt_e4m3x2_bf16x2((uint16_t)(in[i] & 0xFFFF));
-                  o[jj * 8 + 2 * i + 1] = cvt_e4m3x2_bf16x2((uint16_t)(in[i] >> 16));
+                  o[jj * 8 + 2 * i] = cvt_e4m3x2_f16x2((uint16_t)(in[i] & 0xFFFF));
+                  o[jj * 8 + 2 * i + 1] = cvt_e4m3x2_f16x2((uint16_t)(in[i] >> 16));
                 }
               }
-              tmem_store16(ta + h * 16, o);  // dims 32h .. 32h+31 -> columns 16h .. 16h+15
+              tmem_store16_nowait(ta + h * 16, o);  // dims 32h .. 32h+31 -> columns 16h .. 16h+15
             }
+            __syncwarp();  // every lane's stage bytes have been read and converted
+            if (lane == 0) mbar_arrive(&ring_empty[slot]);
+            tmem_wait_st();
             tc_fence_before();
-            release(&ring_empty[slot], &kt_full[ks]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&kt_full[ks]);
             ++idx;
             ++kidx;
           }
           return true;
         };
-        // V tile u, literal path: -> BF16 in shared memory; rows past Lk become zeros
+        // V tile u, literal path: -> BF16 in shared memory; rows past Lk become zeros.
+        // Warp wq converts the 16-byte pieces wq * 32 + lane + 128 j of each stage.
         auto convert_v = [&](int u) -> bool {
           if (!kDqV) return true;  // the PV MMA reads these stages as E4M3, from the V ring
           const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
           const int zero_from = (kb + kTileKeys > it.Lk) ? max(0, it.Lk - kb) : kTileKeys;
+          const int dt = wq * 32 + lane;
           for (int c = 0; c < DC; ++c) {
             const uint32_t slot = idx % S, bslot = bidx % SBm;
-            const bool w_ok = pwait(&ring_full[slot], (idx / S) & 1, lim, abort_flag) &&
-                              pwait(&bf_empty[bslot], ((bidx / SBm) & 1) ^ 1, lim, abort_flag);
-            if (bar_red_or(kDqBar, 128, !w_ok)) return false;
+            if (!wait_all(&ring_full[slot], (idx / S) & 1) || !wait_all(&bf_empty[bslot], ((bidx / SBm) & 1) ^ 1))
+              return false;
             const uint8_t* src = ring + slot * kStageBytes;
             uint8_t* dst = bfbuf + bslot * C::kBfSlotBytes;
             uint4 vin[8];
@@ -1069,7 +1185,11 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
               *reinterpret_cast<uint4*>(drow + (((k0 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
             }
             fence_proxy_async_smem();
-            release(&ring_empty[slot], &bf_full[bslot]);
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(&ring_empty[slot]);
+              mbar_arrive(&bf_full[bslot]);
+            }
             ++idx;
             ++bidx;
           }

@@ -245,6 +245,16 @@ __device__ __forceinline__ void tmem_store64f(uint32_t taddr, const float* x) {
       FP8PA_FI8(56)
       : "memory");
 }
+// Store without waiting: the caller issues tcgen05.wait::st (tmem_wait_st) before
+// the data may be read by another thread's tcgen05 op.
+__device__ __forceinline__ void tmem_store16_nowait(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+      ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_store16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
@@ -257,7 +267,8 @@ __device__ __forceinline__ void tmem_store16(uint32_t taddr, const uint32_t (&r)
 // ---------------------------------------------------------------- descriptors
 // Operand major-ness and element kinds for the instruction descriptor.
 enum : uint32_t { kKMajor = 0, kMNMajor = 1 };
-enum : uint32_t { kFmtE4M3 = 0, kFmtBF16 = 1 };
+// kind::f8f6f4: 0 = E4M3; kind::f16: 0 = F16, 1 = BF16.
+enum : uint32_t { kFmtE4M3 = 0, kFmtF16 = 0, kFmtBF16 = 1 };
 
 // Instruction descriptor for kind::f16 / kind::f8f6f4 with an f32 accumulator:
 // bits 4-5 accumulator format (1 = f32), 7-9 A format, 10-12 B format,

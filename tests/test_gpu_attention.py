@@ -269,3 +269,49 @@ def test_bad_page_id_sets_status_and_reads_zeros():
     assert e["max"] <= TOL[True][0]
     fp8pa.reset_device_status()
     assert fp8pa.get_device_status() == 0
+
+
+@pytest.mark.parametrize("lq,literal_v", [(16, False), (1, False), (16, True)],
+                         ids=["prefill_tiles", "decode_tile", "prefill_tiles_literal_v"])
+def test_bf16_q_path_dequantizes_every_k_code_exactly(lq, literal_v):
+    """BF16-Q path: a single visible key whose 512 channels hold every finite
+    E4M3 code, and one-hot query rows of several magnitudes (1, 2^-30, 2^20, 3).
+    With one key the lse is the score itself, softmax_scale * q * dec(code), so
+    a code decoded wrongly (a flushed subnormal, a wrong exponent) or a Q row
+    scaled wrongly shows at f32 precision."""
+    import fp8_paged_attention_gb300 as fp8pa
+    hq, d = 16, 512
+    codes = np.arange(d) % 256
+    codes[codes == 0x7F] = 0x00
+    codes[codes == 0xFF] = 0x80
+    kc = torch.zeros((2, 64, 1, d), dtype=torch.uint8)
+    vc = torch.zeros((2, 64, 1, d), dtype=torch.uint8)
+    kc[0, 0, 0] = torch.from_numpy(codes.astype(np.uint8))
+    vc[0, 0, 0] = 0x38  # 1.0
+    qvals = [1.0, 2.0 ** -30, 2.0 ** 20, 3.0]
+    rows = lq * hq
+    q = torch.zeros((lq, hq, d), dtype=torch.float32)
+    want = np.zeros((hq, lq))
+    dec = oracle.e4m3_decode(codes)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    for r in range(rows):
+        t, h = divmod(r, hq)
+        ch = (r * 37) % 256 if rows < 256 else r % 256
+        qv = qvals[r % len(qvals)]
+        q[t, h, ch] = qv
+        want[h, t] = scale * qv * dec[ch]
+    q = q.to(torch.bfloat16).cuda()
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    fp8pa.set_bf16_dequant_v(literal_v)
+    try:
+        out, lse = fp8pa.fp8_paged_attn_fwd(q, kc.cuda(), vc.cuda(), torch.zeros((1, 1), dtype=torch.int32, device="cuda"),
+                                            torch.tensor([0, lq], dtype=torch.int32, device="cuda"),
+                                            torch.tensor([1], dtype=torch.int32, device="cuda"), lq, one, one, one,
+                                            scale, -1, False)
+        torch.cuda.synchronize()
+    finally:
+        fp8pa.set_bf16_dequant_v(False)
+    got = lse.cpu().numpy().astype(np.float64)
+    err = np.abs(got - want)
+    assert np.all(err <= 2e-6 + 1e-5 * np.abs(want)), (err.max(), np.unravel_index(err.argmax(), err.shape))
+    assert torch.equal(out.float().cpu(), torch.ones((lq, hq, d)))  # the one V row, all 1.0
