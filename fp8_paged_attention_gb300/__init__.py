@@ -107,6 +107,12 @@ def load_library():
         lib.fp8pa_set_bf16_dequant_v.argtypes = [c.c_int]
         lib.fp8pa_set_ctas_per_sm.restype = None
         lib.fp8pa_set_ctas_per_sm.argtypes = [c.c_int]
+        lib.fp8pa_set_grid_sms.restype = None
+        lib.fp8pa_set_grid_sms.argtypes = [c.c_int]
+        lib.fp8pa_set_sm_split.restype = None
+        lib.fp8pa_set_sm_split.argtypes = [c.c_int]
+        lib.fp8pa_set_prefill_rows.restype = None
+        lib.fp8pa_set_prefill_rows.argtypes = [c.c_int]
         lib.fp8pa_set_timing_events.restype = None
         lib.fp8pa_set_timing_events.argtypes = [c.c_void_p, c.c_void_p]
         _lib = lib
@@ -164,6 +170,24 @@ def set_ctas_per_sm(ctas: int):
     """Tuning hook (fp8pa_testing.h): force 1 or 2 attention CTAs per SM for
     later calls on this thread (0 = automatic)."""
     load_library().fp8pa_set_ctas_per_sm(int(ctas))
+
+
+def set_grid_sms(sms: int):
+    """Tuning hook (fp8pa_testing.h): attention grids of later calls on this
+    thread use at most `sms` SMs (0 = all)."""
+    load_library().fp8pa_set_grid_sms(int(sms))
+
+
+def set_sm_split(sms: int):
+    """Tuning hook (fp8pa_testing.h): SMs of the prefill row class when the two
+    classes run side by side, for later calls on this thread (0 = estimate)."""
+    load_library().fp8pa_set_sm_split(int(sms))
+
+
+def set_prefill_rows(rows: int):
+    """Tuning hook (fp8pa_testing.h): rows per prefill-class tile with BF16 Q
+    (32 or 64; 0 = default) for later calls on this thread."""
+    load_library().fp8pa_set_prefill_rows(int(rows))
 
 
 def set_bf16_dequant_v(on: bool):

@@ -58,6 +58,9 @@ thread_local int g_ctas_override = 0;
 thread_local int g_dequant_v = 0;
 thread_local unsigned g_wait_limit = 0;
 thread_local int g_inject_stall = 0;
+thread_local int g_grid_sms = 0;
+thread_local int g_prefill_rows = 0;
+thread_local int g_sm_split = 0;
 
 // Kernel path for a Q dtype: E4M3 Q, or BF16 Q with V kept E4M3 (default) or
 // dequantized to BF16 (fp8pa_set_bf16_dequant_v).
@@ -216,6 +219,35 @@ int auto_splits(int batch, int hkv, int max_pages, int window_left, int max_lq0,
   return (int)(s == 2 ? 3 : s);
 }
 
+// Cost model of the side-by-side split of the SMs between the decode and the
+// prefill row classes (plan kernel), per kernel path, from measurements on
+// GB300 at 2.07 GHz.  pf_ns_flop: a prefill-class tile's ns x SMs per visible
+// flop, from the 4096-token chunk alone on 152 SMs (head dim 512 BF16 Q 2.32 ms,
+// E4M3 Q 1.18 ms, head dim 256 E4M3 0.132 ms); the E4M3 head-dim-512 figure is
+// raised 1.5x because beside the streaming decode rows that kernel measured that
+// much slower (its K/V re-reads no longer stay in L2).  dec_gbs_sm, dec_gbs: the
+// decode class's per-SM and whole-GPU stream rates (4032 decode rows of the mixed
+// batch on 72..152 SMs: BF16 Q levels off at 7.0 TB/s from ~125 SMs, E4M3 Q at
+// 7.2 TB/s from ~90; head dim 256 about 50 GB/s per SM).  Splits swept on the
+// mixed batches: head dim 512 BF16 Q best at 36 prefill SMs (12.0 ms), E4M3 Q at
+// 28..48 (10.1..10.3 ms), head dim 256 flat within 1 % from 4 to 24.
+struct SplitCost {
+  float pf_ns_flop, dec_gbs_sm, dec_gbs;
+};
+SplitCost split_cost(int head_dim, bool fp8_q) {
+  if (!fp8_q) return {2.14e-4f, 60.f, 7000.f};
+  return head_dim == 512 ? SplitCost{1.64e-4f, 75.f, 7200.f} : SplitCost{1.46e-4f, 50.f, 7000.f};
+}
+
+// Whether row class k is launched: it can hold a sequence (with one sequence,
+// only the class of its total_q queries can).
+bool class_launched(const CallPlan& pl, int k, int batch, int total_q) {
+  const ClassInfo& c = pl.cls[k];
+  if (c.lq_max < c.lq_min) return false;
+  if (batch == 1) return total_q >= c.lq_min && total_q <= c.lq_max;
+  return true;
+}
+
 int make_plan(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int head_dim, int q_dtype, int max_pages,
               int window_left, int num_splits, CallPlan& pl) {
   int rc = check_shape(batch, total_q, max_seqlen_q, hq, hkv, head_dim, max_pages, window_left, num_splits);
@@ -230,7 +262,7 @@ int make_plan(int batch, int total_q, int max_seqlen_q, int hq, int hkv, int hea
   // prefill-class tiles with E4M3 Q run the rows-on-lanes kernel with 128 rows (at head
   // dim 512 as two work items per row tile, one per 256-wide slice of the output dims)
   pl.prefill_kernel = pl.fp8_q;
-  const int prefill_rows = pl.prefill_kernel ? 128 : 64;
+  const int prefill_rows = pl.prefill_kernel ? 128 : (g_prefill_rows == 32 ? 32 : 64);
   const int g = hq / hkv;
   pl.group = g;
   const long long rmax = (long long)max_seqlen_q * g;
@@ -303,6 +335,12 @@ void fp8pa_set_ctas_per_sm(int ctas) { g_ctas_override = ctas; }
 
 void fp8pa_set_bf16_dequant_v(int on) { g_dequant_v = on ? 1 : 0; }
 
+void fp8pa_set_grid_sms(int sms) { g_grid_sms = sms > 0 ? sms : 0; }
+
+void fp8pa_set_prefill_rows(int rows) { g_prefill_rows = rows; }
+
+void fp8pa_set_sm_split(int sms) { g_sm_split = sms > 0 ? sms : 0; }
+
 void fp8pa_set_timing_events(void* start_event, void* stop_event) {
   g_ev_start = static_cast<cudaEvent_t>(start_event);
   g_ev_stop = static_cast<cudaEvent_t>(stop_event);
@@ -317,7 +355,7 @@ int fp8pa_kernel_launches(int batch, int total_q, int max_seqlen_q, int num_head
   if (batch == 0 || total_q == 0) return 0;
   int n = 1;  // plan
   for (int k = 0; k < pl.num_classes; ++k)
-    if (pl.cls[k].lq_max >= pl.cls[k].lq_min) ++n;
+    if (class_launched(pl, k, batch, total_q)) ++n;
   if (pl.splits > 1) ++n;
   return n;
 }
@@ -425,7 +463,7 @@ int fwd_impl(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* 
   cudaStream_t st = (cudaStream_t)stream;
   unsigned* status = status_ptr();
   if (!status) return fail(FP8PA_ECUDA, "cannot resolve the device status word");
-  const int sms = device_sms();
+  const int sms = g_grid_sms > 0 ? std::min(g_grid_sms, device_sms()) : device_sms();
   const int g = pl.group;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* counts = reinterpret_cast<int*>(ws);
@@ -468,6 +506,14 @@ int fwd_impl(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* 
   }
   pp.counts = counts;
   pp.status = status;
+  const SplitCost sc = split_cost(head_dim, fp8_q);
+  pp.hq = num_heads_q;
+  pp.head_dim = head_dim;
+  pp.sms = sms;
+  pp.pf_ns_flop = sc.pf_ns_flop;
+  pp.dec_gbs_sm = sc.dec_gbs_sm;
+  pp.dec_gbs = sc.dec_gbs;
+  pp.forced_split = g_sm_split;
   cudaError_t e = launch_plan(pp, st);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
 
@@ -502,8 +548,16 @@ int fwd_impl(const void* q, int q_dtype, const uint8_t* k_cache, const uint8_t* 
   p.inject_stall = g_inject_stall;
   const bool timed = g_ev_start && g_ev_stop;
   if (timed && (e = cudaEventRecord(g_ev_start, st)) != cudaSuccess) return cuda_fail(e, "timing event");
-  for (int k = 0; k < pl.num_classes; ++k) {
-    if (pl.cls[k].lq_max < pl.cls[k].lq_min) continue;
+  // With both row classes launched they run side by side: the prefill class
+  // first, on the SMs the plan kernel gave it, then the decode class on the rest.
+  const bool both = pl.num_classes > 1 && class_launched(pl, 0, batch, total_q) &&
+                    class_launched(pl, 1, batch, total_q);
+  p.sm_split = counts + 4;
+  p.grid_sms = sms;
+  for (int kk = 0; kk < pl.num_classes; ++kk) {
+    const int k = both ? 1 - kk : kk;
+    if (!class_launched(pl, k, batch, total_q)) continue;
+    p.conc_role = both ? (k == 1 ? 1 : 2) : 0;
     p.cls = pl.cls[k];
     p.work = reinterpret_cast<const int4*>(ws + pl.off_work[k]);
     p.work_count = counts + k;

@@ -349,6 +349,13 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  if (p.conc_role == 2 && (int)blockIdx.x >= active_ctas(p, kCtas)) {
+    // second launch of a side-by-side pair, with no share of the SMs: nothing to
+    // do, but the launch must not end before the first one (CTA 0 waits for it)
+    if (blockIdx.x == 0) griddep_wait();
+    return;
+  }
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&ring_full[i], 1);
@@ -399,7 +406,15 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  griddep_wait();  // the work list, Q and the K/V cache are written by earlier kernels
+  // The work list, Q and the K/V cache are written by earlier kernels.  The
+  // second launch of a side-by-side pair starts only once the first launch has
+  // seen them complete, and waits for that first launch before it exits.
+  if (p.conc_role != 2) griddep_wait();
+  bool idle = false;
+  if (p.conc_role == 1) {
+    idle = (int)blockIdx.x >= active_ctas(p, kCtas);
+    griddep_launch_dependents();  // this CTA is resident: the second launch may take the free SMs
+  }
   const uint32_t tmem = *tmem_slot;
   const int n_items = *p.work_count;
   const uint32_t lim = p.wait_limit;
@@ -418,8 +433,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       uint32_t idx = 0, kq = 0, vq = 0, qit = 0;
       bool ok = true;
       for (uint32_t ik = 0; ok; ++ik) {
-        int w = 0;
-        if (leader) w = atomicAdd(p.work_next, 1);
+        int w = n_items;  // an idle CTA takes no item
+        if (leader && !idle) w = atomicAdd(p.work_next, 1);
         w = __shfl_sync(0xFFFFFFFFu, w, leader_lane);
         const bool valid = w < n_items;
         const uint32_t is = ik % kItemSlots;
@@ -1211,6 +1226,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (p.conc_role == 2) griddep_wait();  // the pair ends when the first launch has ended too
 }
 
 }  // namespace fp8pa

@@ -189,6 +189,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   griddep_wait();  // the work list, Q and the K/V cache are written by earlier kernels
+  bool idle = false;
+  if (p.conc_role == 1) {  // first launch of a side-by-side pair (never the second)
+    idle = (int)blockIdx.x >= active_ctas(p, 1);
+    griddep_launch_dependents();  // this CTA is resident: the second launch may take the free SMs
+  }
   const uint32_t tmem = *tmem_slot;
   const int n_items = *p.work_count;
   const uint32_t lim = p.wait_limit;
@@ -207,8 +212,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       Item it{};
       bool valid;
       if (warp == 0) {
-        int w = 0;
-        if (leader) w = atomicAdd(p.work_next, 1);
+        int w = n_items;  // an idle CTA takes no item
+        if (leader && !idle) w = atomicAdd(p.work_next, 1);
         w = __shfl_sync(0xFFFFFFFFu, w, leader_lane);
         valid = w < n_items;
         if (!(ok = wait_all(&item_empty[is], ((ik / kItemSlots) & 1) ^ 1))) break;

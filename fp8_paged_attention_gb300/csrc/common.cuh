@@ -59,7 +59,22 @@ struct AttnParams {
   unsigned* status;
   uint32_t wait_limit;
   int inject_stall;  // test hook: the MMA issuer first waits on a barrier that nothing arrives on
+  // Two row classes run side by side on disjoint SMs: the prefill class is
+  // launched first (conc_role 1) and keeps *sm_split SMs; the decode class is
+  // launched second (conc_role 2), as soon as every CTA of the first is
+  // resident, and keeps the other grid_sms - *sm_split.  conc_role 0: the
+  // launch has every SM.
+  int conc_role;
+  const int* sm_split;
+  int grid_sms;
 };
+
+// CTAs of this launch that take work; the others leave at once.
+__device__ __forceinline__ int active_ctas(const AttnParams& p, int ctas_per_sm) {
+  if (p.conc_role == 0) return (int)gridDim.x;
+  const int split = *p.sm_split;
+  return (p.conc_role == 1 ? split : p.grid_sms - split) * ctas_per_sm;
+}
 
 // A finished row's normalization with an attention sink: a per-head logit in
 // the softmax denominator that attends to no value.  l = sum_j 2^(s2_j - m2)

@@ -14,8 +14,16 @@ struct PlanParams {
   int num_classes;
   ClassInfo cls[2];
   int4* work[2];
-  int* counts;  // [4]: item counts of the two classes, then their dynamic counters
+  int* counts;  // [5]: item counts of the two classes, their dynamic counters, SMs of the prefill class
   unsigned* status;
+  // Side-by-side split of the SMs between the two classes (counts[4]), from the
+  // classes' work: prefill-class time = visible flops * pf_ns_flop / SMs, decode-
+  // class time = visible K/V bytes / min(SMs * dec_gbs_sm, dec_gbs).
+  int hq, head_dim, sms;
+  float pf_ns_flop;  // ns x SMs per visible flop of a prefill-class tile
+  float dec_gbs_sm;  // decode-class bytes per ns one SM streams
+  float dec_gbs;     // decode-class bytes per ns the whole GPU streams
+  int forced_split;  // > 0: SMs of the prefill class (tuning hook), instead of the estimate
 };
 
 struct CombineParams {

@@ -31,6 +31,44 @@ __device__ __forceinline__ int clamp_lk(int lk, int max_pages) {
 
 __device__ __forceinline__ bool in_class(int Lq, const ClassInfo& c) { return Lq >= c.lq_min && Lq <= c.lq_max; }
 
+// Number of visible (query, key) pairs of a sequence, the sum over its queries
+// of |[lo, hi]| (visible_range), in closed form over the query positions
+// p = Lk - Lq + i: a sum of arithmetic series.
+__device__ long long visible_pairs(int Lq, int Lk, int wl, int causal) {
+  if (Lq <= 0 || Lk <= 0) return 0;
+  const long long P0 = (long long)Lk - Lq, P1 = (long long)Lk - 1;
+  long long total = 0;
+  if (causal) {
+    // p < 0 sees nothing; p + 1 keys up to p = wl (or always without a window); wl + 1 after
+    const long long a = P0 > 0 ? P0 : 0;
+    if (a > P1) return 0;
+    const long long m = wl < 0 ? P1 : (P1 < wl ? P1 : (long long)wl);
+    if (a <= m) total += (m - a + 1) * (a + m + 2) / 2;
+    if (wl >= 0) {
+      const long long a2 = a > (long long)wl + 1 ? a : (long long)wl + 1;
+      if (a2 <= P1) total += (P1 - a2 + 1) * ((long long)wl + 1);
+    }
+  } else {
+    // every key up to p = wl (or always without a window); Lk + wl - p keys after
+    const long long m = wl < 0 ? P1 : (P1 < wl ? P1 : (long long)wl);
+    if (P0 <= m) total += (m - P0 + 1) * Lk;
+    if (wl >= 0) {
+      const long long a2 = P0 > (long long)wl + 1 ? P0 : (long long)wl + 1;
+      if (a2 <= P1) total += (P1 - a2 + 1) * ((long long)Lk + wl) - (a2 + P1) * (P1 - a2 + 1) / 2;
+    }
+  }
+  return total;
+}
+
+// Keys in the union of a sequence's visible ranges (its K/V rows read once per KV head).
+__device__ __forceinline__ long long visible_span(int Lq, int Lk, int wl, int causal) {
+  if (Lq <= 0 || Lk <= 0) return 0;
+  int lo0, hi0, lo1, hi1;
+  visible_range(Lq, Lk, 0, wl, causal, lo0, hi0);
+  visible_range(Lq, Lk, Lq - 1, wl, causal, lo1, hi1);
+  return hi1 >= lo0 ? (long long)hi1 - lo0 + 1 : 0;
+}
+
 // Query count of sequence b, or 0 (and a status flag) when cu_seqlens_q is not a
 // nondecreasing run inside [0, total_q]: such a sequence gets no work.
 __device__ __forceinline__ int seq_lq(const PlanParams& pp, int b) {
@@ -47,18 +85,62 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
   ptx::griddep_launch_dependents();  // the attention grid may start its prologue
   ptx::griddep_wait();               // inputs and the workspace belong to earlier kernels until they finish
   __shared__ int wsum[2][32];
+  __shared__ long long wwork[2][32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int per = (pp.batch + kPlanThreads - 1) / kPlanThreads;
   const int b0 = min(pp.batch, tid * per), b1 = min(pp.batch, b0 + per);
   int cnt[2] = {0, 0};
+  long long work[2] = {0, 0};  // decode class: visible span keys; prefill class: visible pairs
   for (int b = b0; b < b1; ++b) {
     const int Lq = seq_lq(pp, b);
     const int Lk = clamp_lk(pp.seqused_k[b], pp.max_pages);
     for (int k = 0; k < pp.num_classes; ++k) {
       const ClassInfo& c = pp.cls[k];
-      if (Lq > 0 && in_class(Lq, c))
+      if (Lq > 0 && in_class(Lq, c)) {
         cnt[k] += seq_row_tiles(Lq, pp.group, c.rows) *
                   unit_items(seq_splits(Lq, Lk, pp.group, pp.window_left, pp.causal, c), c);
+        work[k] += k == 0 ? visible_span(Lq, Lk, pp.window_left, pp.causal)
+                          : visible_pairs(Lq, Lk, pp.window_left, pp.causal);
+      }
+    }
+  }
+  if (pp.num_classes > 1) {
+    // SMs for the prefill class when both classes run side by side
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) work[k] += __shfl_xor_sync(0xFFFFFFFFu, work[k], off);
+      if (lane == 0) wwork[k][wid] = work[k];
+    }
+    __syncthreads();
+    if (tid == 0) {
+      long long w0 = 0, w1 = 0;
+      for (int i = 0; i < 32; ++i) {
+        w0 += wwork[0][i];
+        w1 += wwork[1][i];
+      }
+      const double bytes0 = (double)w0 * pp.hkv * pp.head_dim * 2.0;
+      const double t1 = (double)w1 * pp.hq * pp.head_dim * 4.0 * pp.pf_ns_flop;  // ns x SMs
+      int best = w1 > 0 ? pp.sms : 0;
+      if (w1 > 0 && w0 > 0) {
+        // the split with the smallest estimated time; where a range of splits is within
+        // 1 % of it (the decode class at its stream cap, the prefill class done sooner),
+        // the middle of that range, away from both of its edges
+        auto est = [&](int k) {
+          const double bw = fmin((double)(pp.sms - k) * pp.dec_gbs_sm, (double)pp.dec_gbs);
+          return fmax(t1 / k, bytes0 / bw);
+        };
+        double best_t = 1e300;
+        for (int k = 1; k < pp.sms; ++k) best_t = fmin(best_t, est(k));
+        int lo = -1, hi = -1;
+        for (int k = 1; k < pp.sms; ++k)
+          if (est(k) <= best_t * 1.01) {
+            if (lo < 0) lo = k;
+            hi = k;
+          }
+        best = (lo + hi) / 2;
+      }
+      pp.counts[4] = pp.forced_split > 0 ? min(pp.forced_split, pp.sms) : best;
     }
   }
   // exclusive prefix sums of the per-thread counts: within each warp, then over the warp totals

@@ -46,6 +46,27 @@ void fp8pa_set_ctas_per_sm(int ctas);
 void fp8pa_set_bf16_dequant_v(int on);
 
 /*
+ * fp8pa_set_grid_sms — tuning hook: the attention kernels' persistent grids use
+ * at most this many SMs (0 = all).  Results do not depend on it; it measures
+ * how a workload's throughput scales with the SMs it gets.
+ */
+void fp8pa_set_grid_sms(int sms);
+
+/*
+ * fp8pa_set_prefill_rows — tuning hook: packed query rows per tile of
+ * prefill-class row tiles with BF16 Q, 32 or 64 (0 = the default, 64).  Results
+ * agree within rounding; it measures the tile size's cost.
+ */
+void fp8pa_set_prefill_rows(int rows);
+
+/*
+ * fp8pa_set_sm_split — tuning hook: when a call runs its decode and prefill row
+ * classes side by side, the prefill class gets this many SMs instead of the
+ * plan kernel's estimate (0 = the estimate).  Results do not depend on it.
+ */
+void fp8pa_set_sm_split(int sms);
+
+/*
  * fp8pa_set_wait_limit — test hook.  Sets the iteration cap of every bounded
  * pipeline wait in later launches (0 restores the default).  A tiny cap makes
  * waits run out, which exercises the timeout path: the kernel sets
