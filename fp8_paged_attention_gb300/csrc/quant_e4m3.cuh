@@ -74,5 +74,29 @@ __device__ __forceinline__ uint2 fast8(uint4 v, float r, float d) {
   return make_uint2(exact_pair(w[0], d) | (exact_pair(w[1], d) << 16), exact_pair(w[2], d) | (exact_pair(w[3], d) << 16));
 }
 
+// Eight bf16 values -> eight codes by the fast form, settled pair by pair:
+// returns a 4-bit mask of the pairs the fast form could not settle (bracket
+// codes differ, or a NaN code, which only a NaN input gives); those pairs'
+// codes in `out` are not final and the caller takes the exact form for them.
+__device__ __forceinline__ uint32_t fast8_masked(uint4 v, float r, uint2& out) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const float dn = 1.0f - 0x1p-21f, up = 1.0f + 0x1p-21f;
+  uint32_t ca[4], cb[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 q = __fmul2_rn(make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u)),
+                                make_float2(r, r));
+    const float2 a = __fmul2_rn(q, make_float2(dn, dn)), b = __fmul2_rn(q, make_float2(up, up));
+    ca[k] = cvt_pair(a.x, a.y);
+    cb[k] = cvt_pair(b.x, b.y);
+  }
+  const uint32_t lo0 = __byte_perm(ca[0], ca[1], 0x5410), lo1 = __byte_perm(ca[2], ca[3], 0x5410);
+  const uint32_t hi0 = __byte_perm(cb[0], cb[1], 0x5410), hi1 = __byte_perm(cb[2], cb[3], 0x5410);
+  const uint32_t n0 = __vcmpne2((lo0 ^ hi0) | __vcmpeq4(lo0 & 0x7F7F7F7Fu, 0x7F7F7F7Fu), 0);
+  const uint32_t n1 = __vcmpne2((lo1 ^ hi1) | __vcmpeq4(lo1 & 0x7F7F7F7Fu, 0x7F7F7F7Fu), 0);
+  out = make_uint2(lo0, lo1);
+  return (n0 & 1u) | ((n0 >> 15) & 2u) | ((n1 & 1u) << 2) | ((n1 >> 13) & 8u);
+}
+
 }  // namespace quant
 }  // namespace fp8pa

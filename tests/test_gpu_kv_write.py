@@ -120,3 +120,22 @@ def test_kv_write_then_attention_reads_what_was_written():
     o = out.float().cpu().numpy()
     err = np.abs(o - want) / np.maximum(1.0, np.abs(want))
     assert err.max() <= TOL[False][0] and err.mean() <= TOL[False][1], (err.max(), err.mean())
+
+
+@pytest.mark.parametrize("kd,vd", [(5 / 64, 3 / 64), (0.75, 5.0), (35 / 448, 1.0)],
+                         ids=["short_mantissa_5_64_3_64", "short_mantissa_0.75_5", "short_35_448_and_unit"])
+def test_kv_write_every_bf16_pattern_with_short_mantissa_descales(kd, vd):
+    """Every bf16 bit pattern as a key and a value, under descales whose short
+    mantissas put many quotients exactly on E4M3 rounding boundaries: most
+    vectors then hold pairs the fast form cannot settle, which the warps hand
+    to the exact form together.  The cache matches the oracle bit for bit."""
+    T, hkv, d, pool = 128, 2, 256, 3
+    pat = np.arange(65536, dtype=np.uint16)
+    rng = np.random.default_rng(31)
+    k = torch.from_numpy(rng.permutation(pat).astype(np.int16).reshape(T, hkv, d)).view(torch.bfloat16)
+    v = torch.from_numpy(rng.permutation(pat).astype(np.int16).reshape(T, hkv, d)).view(torch.bfloat16)
+    slots = rng.permutation(pool * 64)[:T].astype(np.int64)
+    kc, vc, okc, ovc, bad = _run_both(k, v, slots, kd, vd, pool)
+    assert bad == 0
+    assert np.array_equal(kc, okc), np.argwhere(kc != okc)[:5]
+    assert np.array_equal(vc, ovc), np.argwhere(vc != ovc)[:5]
