@@ -105,41 +105,49 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
     }
   }
   if (pp.num_classes > 1) {
-    // SMs for the prefill class when both classes run side by side
+    // SMs for the prefill class when both classes run side by side.  Thread k
+    // (1 <= k < SMs) estimates the time with k SMs for the prefill class; the
+    // block takes the smallest estimate and, where a range of splits is within
+    // 1 % of it (the decode class at its stream cap, the prefill class done
+    // sooner), the middle of that range, away from both of its edges.
+    __shared__ float tmin[32];
+    __shared__ int klo, khi;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) work[k] += __shfl_xor_sync(0xFFFFFFFFu, work[k], off);
       if (lane == 0) wwork[k][wid] = work[k];
     }
+    if (tid == 0) {
+      klo = 1 << 30;
+      khi = -1;
+    }
+    __syncthreads();
+    long long w0 = 0, w1 = 0;
+    for (int i = 0; i < 32; ++i) {
+      w0 += wwork[0][i];
+      w1 += wwork[1][i];
+    }
+    const float bytes0 = (float)w0 * pp.hkv * pp.head_dim * 2.0f;
+    const float t1 = (float)w1 * pp.hq * pp.head_dim * 4.0f * pp.pf_ns_flop;  // ns x SMs
+    const int k = tid;
+    float est = __int_as_float(0x7F800000);
+    if (k >= 1 && k < pp.sms)
+      est = fmaxf(t1 / k, bytes0 / fminf((float)(pp.sms - k) * pp.dec_gbs_sm, pp.dec_gbs));
+    float m = est;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fminf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    if (lane == 0) tmin[wid] = m;
+    __syncthreads();
+    float best_t = tmin[0];
+    for (int i = 1; i < 32; ++i) best_t = fminf(best_t, tmin[i]);
+    if (k >= 1 && k < pp.sms && est <= best_t * 1.01f) {
+      atomicMin(&klo, k);
+      atomicMax(&khi, k);
+    }
     __syncthreads();
     if (tid == 0) {
-      long long w0 = 0, w1 = 0;
-      for (int i = 0; i < 32; ++i) {
-        w0 += wwork[0][i];
-        w1 += wwork[1][i];
-      }
-      const double bytes0 = (double)w0 * pp.hkv * pp.head_dim * 2.0;
-      const double t1 = (double)w1 * pp.hq * pp.head_dim * 4.0 * pp.pf_ns_flop;  // ns x SMs
-      int best = w1 > 0 ? pp.sms : 0;
-      if (w1 > 0 && w0 > 0) {
-        // the split with the smallest estimated time; where a range of splits is within
-        // 1 % of it (the decode class at its stream cap, the prefill class done sooner),
-        // the middle of that range, away from both of its edges
-        auto est = [&](int k) {
-          const double bw = fmin((double)(pp.sms - k) * pp.dec_gbs_sm, (double)pp.dec_gbs);
-          return fmax(t1 / k, bytes0 / bw);
-        };
-        double best_t = 1e300;
-        for (int k = 1; k < pp.sms; ++k) best_t = fmin(best_t, est(k));
-        int lo = -1, hi = -1;
-        for (int k = 1; k < pp.sms; ++k)
-          if (est(k) <= best_t * 1.01) {
-            if (lo < 0) lo = k;
-            hi = k;
-          }
-        best = (lo + hi) / 2;
-      }
+      const int best = (w1 > 0 && w0 > 0) ? (klo + khi) / 2 : (w1 > 0 ? pp.sms : 0);
       pp.counts[4] = pp.forced_split > 0 ? min(pp.forced_split, pp.sms) : best;
     }
   }
