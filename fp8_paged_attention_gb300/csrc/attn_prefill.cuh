@@ -336,18 +336,18 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
               if (!(ok = wait_all(&k_full[slot], ((kq + c) / SK) & 1))) break;
               tc_fence_after();
               const uint32_t a0 = qaddr + c * C::kRows * 128, b0 = smem_u32(kring + slot * C::kKStageBytes);
-              if (leader) {
+              // issued by the converged warp, predicated on the elected lane: at four
+              // chunks per tile the issuing thread's cost per MMA otherwise shows
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  mma_f8f6f4(tmem + sb * 128, make_sdesc(a0 + kk * 32, 16, 1024, kLayoutSW128),
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8f6f4_p(leader, tmem + sb * 128, make_sdesc(a0 + kk * 32, 16, 1024, kLayoutSW128),
                              make_sdesc(b0 + kk * 32, 16, 1024, kLayoutSW128), idesc, (c | kk) != 0);
-                mma_commit(&k_empty[slot]);
-              }
+              mma_commit_p(leader, &k_empty[slot]);
             }
             if (!ok) break;
           }
           kq += DC;
-          if (leader) mma_commit(&s_full[sb]);
+          mma_commit_p(leader, &s_full[sb]);
         }
         if (ok && leader) mma_commit(&q_empty[qb]);
       } else {
@@ -367,15 +367,26 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           if (!(ok = wait_all(&v_full[slot], vpar))) break;
           tc_fence_after();
           const uint32_t v0 = smem_u32(vring + slot * C::kVStageBytes);
-          if (leader) {
+          if constexpr (C::kSplitQK) {
+            if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t vb = make_sdesc(v0 + kk * 4096, kStageBytes, 1024, kLayoutSW128);
+                mma_f8f6f4_tmem_a(tmem + C::kOCol, tmem + sb * 128 + kk * 8, vb, idesc, !(u == 0 && kk == 0));
+                mma_f8f6f4_tmem_a(tmem + C::kOCol, tmem + sb * 128 + 32 + kk * 8, vb, idesc, 1);
+              }
+              mma_commit(&v_empty[slot]);
+              mma_commit(&s_free[sb]);
+            }
+          } else {  // head dim 512: from the converged warp, as QK^T
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t vb = make_sdesc(v0 + kk * 4096, kStageBytes, 1024, kLayoutSW128);
-              mma_f8f6f4_tmem_a(tmem + C::kOCol, tmem + sb * 128 + kk * 8, vb, idesc, !(u == 0 && kk == 0));
-              mma_f8f6f4_tmem_a(tmem + C::kOCol, tmem + sb * 128 + 32 + kk * 8, vb, idesc, 1);
+              mma_f8f6f4_tmem_a_p(leader, tmem + C::kOCol, tmem + sb * 128 + kk * 8, vb, idesc, !(u == 0 && kk == 0));
+              mma_f8f6f4_tmem_a_p(leader, tmem + C::kOCol, tmem + sb * 128 + 32 + kk * 8, vb, idesc, 1);
             }
-            mma_commit(&v_empty[slot]);
-            mma_commit(&s_free[sb]);
+            mma_commit_p(leader, &v_empty[slot]);
+            mma_commit_p(leader, &s_free[sb]);
           }
           ++vq;
         }
