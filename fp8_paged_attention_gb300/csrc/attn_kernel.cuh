@@ -19,10 +19,10 @@
 // consume them); warp 1 allocates tensor memory and issues the MMAs from one
 // thread; the next one or two warpgroups run the softmax, the O rescale and the
 // epilogue (with two, each owns half the rows of every tile).  On the BF16-Q
-// paths the last four warps dequantize each E4M3 K stage into BF16 straight into
-// tensor memory, where it is the A operand of the QK^T MMA (exact: every E4M3
-// value is a BF16 value); on the literal path they also dequantize V into BF16
-// shared-memory tiles.
+// paths the last four warps convert each item's BF16 Q tile in place; on the
+// literal path they also dequantize each E4M3 K stage to F16 straight into
+// tensor memory (the A operand of the QK^T MMA; exact, every E4M3 value is an
+// F16 value) and V into BF16 shared-memory tiles.
 //
 // Softmax per tile: with the running offsets of the previous tiles, P' is
 // computed directly; only when some P' exceeds the lazy bound (a row maximum
@@ -32,18 +32,21 @@
 //
 // Paths (template parameter kPath):
 //  kPathE4M3    E4M3 Q: QK^T and PV are kind::f8f6f4 MMAs.
-//  kPathBf16    BF16 Q: K dequantized to F16 (one conversion per pair of codes,
-//               exact), QK^T a kind::f16 MMA on F16 operands; V stays E4M3
-//               (exact) in a kind::f8f6f4 PV MMA.
-//  kPathBf16DqV BF16 Q: K dequantized as above, V dequantized to BF16, PV a
-//               kind::f16 MMA with BF16 P.
-// On both BF16-Q paths the dequant warps first convert each item's BF16 Q tile
-// in place to F16 scaled by a per-row power of two 2^k_r that puts the row's
-// largest magnitude in [2^14, 2^15): every BF16 value down to 2^-28 of the
-// row's largest is then exact in F16 (8 significant bits fit F16's 11), smaller
-// ones keep an absolute error below 2^-39 of it, far under the f32
-// accumulation's own rounding.  The softmax multiplies row r's scores by
-// 2^-k_r, folded into its per-row score scale.
+//  kPathBf16    BF16 Q as an exact pair of E4M3 terms: per item the Q tile is
+//               scaled per row by a power of two 2^k_r (the row's largest
+//               magnitude in [2^7, 2^8)) and split into hi = e4m3(x) and
+//               lo = e4m3(x - hi).  BF16's 8 significant bits fit the two
+//               terms' 4 + 4, so hi + lo = x for every value down to 2^-10 of
+//               the row's largest (below it within 2^-10 absolute, scaled).
+//               QK^T is two kind::f8f6f4 MMAs per K step on the E4M3 K stage,
+//               both into the same S; V stays E4M3 (exact) in the PV MMA.
+//  kPathBf16DqV BF16 Q, the literal form: Q converted in place to F16 scaled
+//               by 2^k_r (largest magnitude in [2^14, 2^15): every BF16 value
+//               down to 2^-28 of it exact), K dequantized to F16 (exact), QK^T a
+//               kind::f16 MMA; V dequantized to BF16, PV a kind::f16 MMA with
+//               BF16 P.
+// On both BF16-Q paths the softmax multiplies row r's scores by 2^-k_r, folded
+// into its per-row score scale.
 // Where the PV MMA is E4M3, P is requantized to E4M3 after a 2^4 pre-scale
 // (P' = 2^(x - m + 4), at most 256 under the lazy rescale below, keeping small
 // weights out of E4M3's subnormal range) as a pair on one scale:
@@ -72,8 +75,10 @@ struct AttnCfg {
   static_assert(kCtas == 1 || kCtas == 2, "CTAs per SM");
   static_assert(kPath >= 0 && kPath <= 2, "path");
   static constexpr bool kQ8 = kPath == kPathE4M3;     // Q and K enter QK^T as E4M3
+  static constexpr bool kQSplit = kPath == kPathBf16;  // BF16 Q enters QK^T as an exact E4M3 pair, K as E4M3
   static constexpr bool kP8 = kPath != kPathBf16DqV;  // P (hi/lo) and V enter PV as E4M3
-  static constexpr bool kDq = kPath != kPathE4M3;     // dequant warps: K -> BF16 in TMEM
+  static constexpr bool kDq = kPath != kPathE4M3;     // dequant warps: the BF16 Q tile, per item
+  static constexpr bool kKDq = kPath == kPathBf16DqV; // ... K -> F16 in TMEM, per tile
   static constexpr bool kDqV = kPath == kPathBf16DqV; // ... and V -> BF16 in shared memory
   static constexpr int kDC = D / 128;                    // 128-byte chunks of an E4M3 row
   static constexpr int kQChunkElems = kQ8 ? 128 : 64;    // Q elements per 128-byte chunk
@@ -122,8 +127,8 @@ struct AttnCfg {
   // F16 K chunks in TMEM (64 columns each): as many slots as fit, up to four, so
   // that the dequant warps can run ahead of the QK^T MMAs
   static constexpr int kKSlotsFit = (512 / kCtas - kKCol) / 64;
-  static constexpr int kKSlots = kDq ? (kKSlotsFit > 4 ? 4 : kKSlotsFit) : 0;
-  static_assert(!kDq || kKSlots >= 2, "TMEM for the F16 K slots");
+  static constexpr int kKSlots = kKDq ? (kKSlotsFit > 4 ? 4 : kKSlotsFit) : 0;
+  static_assert(!kKDq || kKSlots >= 2, "TMEM for the F16 K slots");
   static constexpr int kTmemUsed = kKCol + 64 * kKSlots;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
                                         : kTmemUsed <= 256 ? 256 : 512;
@@ -275,6 +280,16 @@ __device__ __forceinline__ uint32_t bf16x2_scaled_to_f16x2(uint32_t w, float f) 
   return h;
 }
 
+// Two f32 values -> two E4M3 codes (lo first, in the low byte), round to nearest
+// even, saturating.
+__device__ __forceinline__ uint16_t e4m3x2_of(float lo, float hi) {
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(hi), "f"(lo));
+  return c;
+}
+
+__device__ __forceinline__ __half2 u32_as_half2(uint32_t h) { return *reinterpret_cast<__half2*>(&h); }
+
 __device__ __forceinline__ uint32_t cvt_e4m3x2_bf16x2(uint16_t v) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
   float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
@@ -296,7 +311,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
     attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using C = AttnCfg<D, kPath, N, kCtas>;
-  constexpr bool kQ8 = C::kQ8, kP8 = C::kP8, kDq = C::kDq, kDqV = C::kDqV;
+  constexpr bool kQ8 = C::kQ8, kP8 = C::kP8, kDq = C::kDq, kDqV = C::kDqV, kQS = C::kQSplit, kKDq = C::kKDq;
   using namespace ptx;
   using namespace detail;
   constexpr int S = C::kStages;
@@ -360,7 +375,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
     for (int i = 0; i < S; ++i) {
       mbar_init(&ring_full[i], 1);
       // one MMA commit, or one arrive of each of the four dequant warps for the stages they consume
-      mbar_init(&ring_empty[i], (kDq && (!kSplit || i < SK)) ? 4 : 1);
+      mbar_init(&ring_empty[i], (kKDq && (!kSplit || i < SK)) ? 4 : 1);
     }
     for (int i = 0; i < SB; ++i) {
       mbar_init(&bf_full[i], 4);
@@ -513,7 +528,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       };
       const bool do_qk = !C::kTwoIssuers || warp == 1;
       const bool do_pv = !C::kTwoIssuers || warp == 2;
-      constexpr uint32_t idesc_qk = make_idesc(kQ8 ? kFmtE4M3 : kFmtF16, kKMajor, kKMajor, 128, N);
+      constexpr uint32_t idesc_qk = make_idesc(kKDq ? kFmtF16 : kFmtE4M3, kKMajor, kKMajor, 128, N);
       constexpr uint32_t idesc_pv = make_idesc(kP8 ? kFmtE4M3 : kFmtBF16, kMNMajor, kMNMajor, 128, N);
       // E4M3 stages: idx = stage-stream position (one ring), or kq / vq = K and V
       // ring positions (split rings); kidx: BF16 K chunks in TMEM; bidx: BF16 V
@@ -548,16 +563,22 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           tc_fence_after();
           const uint32_t d_tmem = tmem + sb * N;
           for (int c = 0; c < DC; ++c) {
-            if (kQ8) {
+            if (kQ8 || kQS) {
               const uint32_t slot = kslot(kpos);
               if (!wait_all(&ring_full[slot], kpar(kpos))) return false;
               tc_fence_after();
-              const uint32_t a0 = smem_u32(ring + slot * kStageBytes), b0 = qaddr + c * N * 128;
+              // E4M3 Q: chunk c of the tile; split BF16 Q: the hi term of dims 128c.. in
+              // chunk 2c of the converted tile, its lo term in chunk 2c + 1
+              const uint32_t a0 = smem_u32(ring + slot * kStageBytes), b0 = qaddr + (kQS ? 2 * c : c) * N * 128;
               if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
+                for (int kk = 0; kk < 4; ++kk) {
                   mma_f8f6f4(d_tmem, make_sdesc(a0 + kk * 32, 16, 1024, kLayoutSW128),
                              make_sdesc(b0 + kk * 32, 16, 1024, kLayoutSW128), idesc_qk, (c | kk) != 0);
+                  if (kQS)
+                    mma_f8f6f4(d_tmem, make_sdesc(a0 + kk * 32, 16, 1024, kLayoutSW128),
+                               make_sdesc(b0 + N * 128 + kk * 32, 16, 1024, kLayoutSW128), idesc_qk, 1);
+                }
                 mma_commit(&ring_empty[slot]);
               }
               ++kpos;
@@ -1139,20 +1160,70 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           mx = max(mx & 0xFFFFu, mx >> 16);
 #pragma unroll
           for (int o = 1; o < QP; o <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-          // 2^k_r puts the row's largest magnitude in [2^14, 2^15); an all-zero row keeps k = 0
-          const int e = (int)(mx >> 7);
-          const int k = mx == 0 ? 0 : min(120, 141 - e);
-          const float f = __int_as_float((k + 127) << 23);
+          int k;
+          if constexpr (kQS) {
+            // 2^k_r puts the row's largest magnitude in [2^7, 2^8) (an all-zero row keeps
+            // k = 0).  Dims 128j .. 128j + 127 of the row (BF16 chunks 2j and 2j + 1) become
+            // hi = e4m3(x), lo = e4m3(x - hi) with x = q 2^k_r, hi in chunk 2j and lo in
+            // chunk 2j + 1 as E4M3 rows (128 bytes, 16-byte pieces swizzled by row).  x has
+            // BF16's 8 significant bits and hi keeps the top 4 (rounded), so x - hi is exact
+            // and has at most 4 more; lo holds it exactly whenever |x| >= 2^-2, i.e. for every
+            // value down to 2^-10 of the row's largest, and within 2^-10 below that.
+            const int e = (int)(mx >> 7);
+            k = mx == 0 ? 0 : min(120, 134 - e);
+            const float f = __int_as_float((k + 127) << 23);
+            const int sw = qrow & 7;
 #pragma unroll 1
-          for (int c = qpart; c < kQCh; c += QP) {
-            uint4* src = reinterpret_cast<uint4*>(qrow_base + c * N * 128);
+            for (int j = qpart; j < kQCh / 2; j += QP) {
+              uint8_t* c0 = qrow_base + 2 * j * N * 128;  // the row in chunk 2j
+              uint8_t* c1 = c0 + N * 128;                 // and in chunk 2j + 1
+              uint4 v[16];                                // BF16 pieces in dim order (8 dims each)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              uint4 v = src[j];
-              uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+              for (int t = 0; t < 8; ++t) {
+                v[t] = *reinterpret_cast<const uint4*>(c0 + ((t ^ sw) << 4));
+                v[8 + t] = *reinterpret_cast<const uint4*>(c1 + ((t ^ sw) << 4));
+              }
 #pragma unroll
-              for (int i = 0; i < 4; ++i) w[i] = bf16x2_scaled_to_f16x2(w[i], f);
-              src[j] = v;
+              for (int t = 0; t < 8; ++t) {  // E4M3 piece t: dims 16t .. 16t + 15 of the 128
+                const uint32_t w[8] = {v[2 * t].x,     v[2 * t].y,     v[2 * t].z,     v[2 * t].w,
+                                       v[2 * t + 1].x, v[2 * t + 1].y, v[2 * t + 1].z, v[2 * t + 1].w};
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  uint32_t hq[2], lq[2];
+#pragma unroll
+                  for (int b = 0; b < 2; ++b) {
+                    const uint32_t x2 = w[2 * q + b];
+                    const float2 x = __fmul2_rn(make_float2(__uint_as_float(x2 << 16), __uint_as_float(x2 & 0xFFFF0000u)),
+                                                make_float2(f, f));
+                    const uint16_t hc = e4m3x2_of(x.x, x.y);
+                    const float2 hv = __half22float2(u32_as_half2(cvt_e4m3x2_f16x2(hc)));
+                    hq[b] = hc;
+                    lq[b] = e4m3x2_of(x.x - hv.x, x.y - hv.y);
+                  }
+                  h[q] = hq[0] | (hq[1] << 16);
+                  l[q] = lq[0] | (lq[1] << 16);
+                }
+                *reinterpret_cast<uint4*>(c0 + ((t ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(c1 + ((t ^ sw) << 4)) = make_uint4(l[0], l[1], l[2], l[3]);
+              }
+            }
+          } else {
+            // 2^k_r puts the row's largest magnitude in [2^14, 2^15); an all-zero row keeps k = 0
+            const int e = (int)(mx >> 7);
+            k = mx == 0 ? 0 : min(120, 141 - e);
+            const float f = __int_as_float((k + 127) << 23);
+#pragma unroll 1
+            for (int c = qpart; c < kQCh; c += QP) {
+              uint4* src = reinterpret_cast<uint4*>(qrow_base + c * N * 128);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint4 v = src[j];
+                uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) w[i] = bf16x2_scaled_to_f16x2(w[i], f);
+                src[j] = v;
+              }
             }
           }
           if (qpart == 0) {
@@ -1164,8 +1235,10 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
           if (lane == 0) mbar_arrive(&q_conv[qb]);
           ++qi;
         }
+        if constexpr (kQS) continue;  // K and V reach the MMAs as E4M3: nothing to convert per tile
         // K tile u: each chunk (128 dims) -> F16 in TMEM slot kidx % KS, one key row per thread
         auto convert_k = [&](int u) -> bool {
+          if (!kKDq) return true;
           for (int c = 0; c < DC; ++c) {
             const uint32_t slot = idx % KR, ks = kidx % KS;
             if (!wait_all(&ring_full[slot], (idx / KR) & 1) || !wait_all(&kt_empty[ks], ((kidx / KS) & 1) ^ 1))
