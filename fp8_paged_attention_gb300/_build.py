@@ -66,7 +66,13 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None, e
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
-        r = subprocess.run(cmd, capture_output=True, text=True)
+        # A compiler process that dies on a signal (seen as an occasional segmentation
+        # fault under a parallel build) is run again; a diagnosed error is not.
+        for attempt in range(3):
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            crashed = r.returncode < 0 or r.returncode >= 128 or "Segmentation fault" in r.stderr
+            if r.returncode == 0 or not crashed:
+                break
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
         if verbose and (r.stdout or r.stderr):
