@@ -192,8 +192,9 @@ def set_prefill_rows(rows: int):
 
 def set_bf16_dequant_v(on: bool):
     """Test hook (fp8pa_testing.h), later calls on this thread: the BF16-Q path
-    keeps V E4M3 with a hi/lo E4M3 P (False, default) or dequantizes V to BF16
-    with a BF16 P (True)."""
+    runs FP8 MMAs with Q split into an exact E4M3 pair, V E4M3 and a hi/lo E4M3
+    P (False, default), or the literal form with K dequantized to F16 and V to
+    BF16 with a BF16 P (True)."""
     load_library().fp8pa_set_bf16_dequant_v(int(bool(on)))
 
 

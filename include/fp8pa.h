@@ -245,8 +245,11 @@ int fp8pa_num_splits(int batch, int total_q, int max_seqlen_q, int num_heads_q, 
  * (0, 0 = per tensor).  A NULL descale pointer is the unit scale 1.0 and is
  * never read (the no-descale fast path for caches stored without scaling).
  *
- * Support: head_dim 256 with E4M3 Q; head_dim 512 with BF16 Q (K/V dequantized
- * in-kernel, BF16 MMA) or E4M3 Q (FP8 MMA).  V head dim = head_dim.  num_heads_q
+ * Support: head_dim 256 with E4M3 Q; head_dim 512 with BF16 Q or E4M3 Q.  With
+ * BF16 Q each row of Q is split in-kernel into an exact pair of E4M3 terms under
+ * a power-of-two row scale (every value down to 2^-10 of the row's largest is
+ * carried exactly) and QK^T runs as FP8 MMAs on the E4M3 K; the result is that
+ * of a 16-bit MMA on the dequantized K.  V head dim = head_dim.  num_heads_q
  * a multiple of num_heads_kv with a group size in {1, 2, 4, 8, 16}.
  * window_left >= -1.  num_splits: 0 = automatic, else (1..64) the maximum number
  * of key splits per (sequence, KV head); splits are combined by log-sum-exp.

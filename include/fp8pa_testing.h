@@ -36,12 +36,13 @@ void fp8pa_set_timing_events(void* start_event, void* stop_event);
 void fp8pa_set_ctas_per_sm(int ctas);
 
 /*
- * fp8pa_set_bf16_dequant_v — selects how the BF16-Q path treats V (K is always
- * dequantized to BF16 in-kernel and multiplied with BF16 Q on BF16 tensor
- * cores).  0 (default): V stays E4M3, exact, in an E4M3 PV MMA with P carried
- * as an E4M3 hi/lo pair (about BF16's 8 significant bits).  1: V is also
- * dequantized to BF16 in shared memory and PV is a BF16 MMA with BF16 P (the
- * literal form of the dequant path, kept to check the default against).
+ * fp8pa_set_bf16_dequant_v — selects the form of the BF16-Q path.  0 (default):
+ * Q is split per row into an exact E4M3 pair and QK^T runs as FP8 MMAs on the
+ * E4M3 K; V stays E4M3, exact, in an E4M3 PV MMA with P carried as an E4M3
+ * hi/lo pair (about BF16's 8 significant bits).  1: the literal dequant form,
+ * kept to check the default against: Q in F16, K dequantized to F16 in tensor
+ * memory for a 16-bit QK^T, V dequantized to BF16 in shared memory and PV a BF16
+ * MMA with BF16 P.
  */
 void fp8pa_set_bf16_dequant_v(int on);
 
