@@ -36,7 +36,7 @@
 //               scaled per row by a power of two 2^k_r (the row's largest
 //               magnitude in [2^7, 2^8)) and split into hi = e4m3(x) and
 //               lo = e4m3(x - hi).  BF16's 8 significant bits fit the two
-//               terms' 4 + 4, so hi + lo = x for every value down to 2^-10 of
+//               terms' 4 + 4, so hi + lo = x for every value down to 2^-9 of
 //               the row's largest (below it within 2^-10 absolute, scaled).
 //               QK^T is two kind::f8f6f4 MMAs per K step on the E4M3 K stage,
 //               both into the same S; V stays E4M3 (exact) in the PV MMA.
@@ -1168,7 +1168,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
             // chunk 2j + 1 as E4M3 rows (128 bytes, 16-byte pieces swizzled by row).  x has
             // BF16's 8 significant bits and hi keeps the top 4 (rounded), so x - hi is exact
             // and has at most 4 more; lo holds it exactly whenever |x| >= 2^-2, i.e. for every
-            // value down to 2^-10 of the row's largest, and within 2^-10 below that.
+            // value down to 2^-9 of the row's largest, and within 2^-10 below that.
             const int e = (int)(mx >> 7);
             k = mx == 0 ? 0 : min(120, 134 - e);
             const float f = __int_as_float((k + 127) << 23);

@@ -247,7 +247,7 @@ int fp8pa_num_splits(int batch, int total_q, int max_seqlen_q, int num_heads_q, 
  *
  * Support: head_dim 256 with E4M3 Q; head_dim 512 with BF16 Q or E4M3 Q.  With
  * BF16 Q each row of Q is split in-kernel into an exact pair of E4M3 terms under
- * a power-of-two row scale (every value down to 2^-10 of the row's largest is
+ * a power-of-two row scale (every value down to 2^-9 of the row's largest is
  * carried exactly) and QK^T runs as FP8 MMAs on the E4M3 K; the result is that
  * of a 16-bit MMA on the dequantized K.  V head dim = head_dim.  num_heads_q
  * a multiple of num_heads_kv with a group size in {1, 2, 4, 8, 16}.

@@ -315,3 +315,54 @@ def test_bf16_q_path_dequantizes_every_k_code_exactly(lq, literal_v):
     err = np.abs(got - want)
     assert np.all(err <= 2e-6 + 1e-5 * np.abs(want)), (err.max(), np.unravel_index(err.argmax(), err.shape))
     assert torch.equal(out.float().cpu(), torch.ones((lq, hq, d)))  # the one V row, all 1.0
+
+
+@pytest.mark.parametrize("lq", [16, 1])
+def test_bf16_q_split_carries_full_mantissa_rows(lq):
+    """BF16-Q path: with one visible key the lse is the score itself, so it shows
+    how exactly the kernel carries Q.  Rows of full-mantissa BF16 values: N(0, 1)
+    rows, rows whose values all lie within [2^-9, 1] of the row's largest, and
+    rows spanning 2^-30 .. 2^20 in magnitude.  The kernel's E4M3 pair holds every
+    value down to 2^-9 of the row's largest exactly, so those terms must agree
+    with fp64 to f32 accumulation accuracy; a smaller value is off by at most
+    its own magnitude, which the bound allows for."""
+    import fp8_paged_attention_gb300 as fp8pa
+    hq, d = 16, 512
+    rng = np.random.default_rng(77)
+    codes = rng.integers(0, 256, size=d)
+    codes[(codes & 0x7F) == 0x7F] = 0x38
+    kc = torch.zeros((2, 64, 1, d), dtype=torch.uint8)
+    vc = torch.zeros((2, 64, 1, d), dtype=torch.uint8)
+    kc[0, 0, 0] = torch.from_numpy(codes.astype(np.uint8))
+    vc[0, 0, 0] = 0x38  # 1.0
+    dec = oracle.e4m3_decode(codes).astype(np.float64)
+    q = np.zeros((lq, hq, d), dtype=np.float32)
+    for t in range(lq):
+        for h in range(hq):
+            kind = (t * hq + h) % 3
+            if kind == 0:
+                row = rng.standard_normal(d)
+            elif kind == 1:
+                row = rng.choice([-1.0, 1.0], d) * np.exp2(rng.uniform(-9.0, 0.0, d))
+            else:
+                row = rng.choice([-1.0, 1.0], d) * np.exp2(rng.uniform(-30.0, 20.0, d))
+            q[t, h] = row
+    qb = torch.from_numpy(q).to(torch.bfloat16)
+    qv = qb.float().numpy().astype(np.float64)  # the BF16 values the kernel sees
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    want = scale * np.einsum("thd,d->ht", qv, dec)
+    bound = scale * np.einsum("thd,d->ht", np.abs(qv), np.abs(dec))
+    small = np.abs(qv) < np.exp2(-9.0) * np.abs(qv).max(axis=2, keepdims=True)
+    slack = scale * np.einsum("thd,d->ht", np.abs(qv) * small, np.abs(dec))
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    out, lse = fp8pa.fp8_paged_attn_fwd(qb.cuda(), kc.cuda(), vc.cuda(), torch.zeros((1, 1), dtype=torch.int32, device="cuda"),
+                                        torch.tensor([0, lq], dtype=torch.int32, device="cuda"),
+                                        torch.tensor([1], dtype=torch.int32, device="cuda"), lq, one, one, one,
+                                        scale, -1, False)
+    torch.cuda.synchronize()
+    got = lse.cpu().numpy().astype(np.float64)
+    err = np.abs(got - want)
+    assert np.all(err <= 2e-6 * bound + slack + 1e-30), (float((err / np.maximum(bound, 1e-30)).max()),)
+    exact_rows = ~small.any(axis=2).T  # rows with no value below 2^-9 of their largest
+    assert exact_rows.any() and np.all(err[exact_rows] <= 2e-6 * bound[exact_rows])
+    assert torch.equal(out.float().cpu(), torch.ones((lq, hq, d)))
