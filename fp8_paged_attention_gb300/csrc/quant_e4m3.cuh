@@ -1,17 +1,27 @@
-// bf16 -> E4M3 codes by the rule E4M3_RNE_sat(fl32(x / d)), two elements at a time.
+// bf16 -> E4M3 codes by the rule E4M3_RNE_sat(fl32(x / d)), eight elements at a time.
 //
 // Exact form: an IEEE fp32 division, then the hardware round-to-nearest-even
 // saturating conversion; a NaN quotient gives 0x7F with the input's sign bit.
 //
-// Fast form, bit-identical: q = x * r with r = fl32(1 / d) is within 3 units of
-// 2^-24 (relative) of x / d, and so is fl32(x / d).  Rounding to E4M3 is
-// monotone, so when q * (1 - 2^-21) and q * (1 + 2^-21) round to the same code,
-// the correctly rounded quotient, which lies between them, rounds to that code
-// too.  Otherwise (a quotient within a few ulps of an E4M3 rounding boundary, or
-// a NaN) the exact form decides.  Tiny quotients (below fp32's normal range) all
-// round to a zero code either way; q overflowing to infinity only where x / d
-// exceeds 448 saturates to the same code.  The fast form needs r to carry the
-// relative error bound, hence the normal-range test on d.
+// Fast form, bit-identical: the correctly rounded quotient fl32(x / d) without a
+// division, by Markstein's correction (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1),
+// 1990; also Muller et al., Handbook of Floating-Point Arithmetic, the section
+// on division with a fused multiply-add).  With y = RN(1 / d) and q a faithful
+// rounding of x / d, the residual r = x - d * q is exact in fp32 and
+// RN(q + r * y) = RN(x / d).  The start q0 = RN(x * y) lies within 2^-23
+// (relative) of x / d; one correction step from it forms q0 + r0 * y within
+// 2^-46 of x / d before its one rounding, so its result is faithful, and the
+// second step is Markstein's.  Each residual and each correction is one fused
+// multiply-add (one rounding).
+//
+// Range: 2^-64 <= d <= 2^64.  A quotient below 2^-11 gives a zero code whatever
+// the steps do to it (the smallest E4M3 rounding boundary is 2^-10, and they move
+// it by far less than that); for a larger quotient every residual the steps need
+// has its last bit at or above 2^-121, so none is lost to underflow.  The code's
+// sign is the input's (d > 0), which keeps -0 right.  An infinite input, or a
+// product x * y that overflows, makes the steps give NaN: those codes, and NaN
+// inputs, show as the NaN code 0x7F and are flagged for the exact form.
 #pragma once
 #include <cuda_fp8.h>
 #include <stdint.h>
@@ -30,8 +40,8 @@ __device__ __forceinline__ uint32_t exact_pair(uint32_t w, float d) {
   return exact_one((uint16_t)w, d) | (exact_one((uint16_t)(w >> 16), d) << 8);
 }
 
-// d in a range where fl32(1 / d) is a normal number with its usual error bound
-__device__ __forceinline__ bool fast_ok(float d) { return fabsf(d) > 1e-30f && fabsf(d) < 1e30f; }
+// d in the range where the fast form is exact
+__device__ __forceinline__ bool fast_ok(float d) { return d >= 0x1p-64f && d <= 0x1p64f; }
 
 __device__ __forceinline__ uint32_t cvt_pair(float lo, float hi) {
   uint16_t c;
@@ -39,63 +49,35 @@ __device__ __forceinline__ uint32_t cvt_pair(float lo, float hi) {
   return c;
 }
 
-__device__ __forceinline__ uint32_t fast_pair(uint32_t w, float r, float d) {
-  const float2 q = __fmul2_rn(make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)),
-                              make_float2(r, r));
-  const float dn = 1.0f - 0x1p-21f, up = 1.0f + 0x1p-21f;
-  const float2 a = __fmul2_rn(q, make_float2(dn, dn)), b = __fmul2_rn(q, make_float2(up, up));
-  const uint32_t ca = cvt_pair(a.x, a.y), cb = cvt_pair(b.x, b.y);
-  // E4M3 NaN codes come only from NaN inputs (the conversion saturates): exact form
-  const bool nan_code = (ca & 0x7F) == 0x7F || (ca & 0x7F00) == 0x7F00;
-  if (ca == cb && !nan_code) return ca;
-  return exact_pair(w, d);
-}
-
-// Eight bf16 values (one 16-byte vector) -> eight codes, low byte first.  The
-// checks of fast_pair are made once per vector: the two brackets' codes are
-// compared as two packed words, and NaN inputs are found on the bf16 bits
-// (exponent all ones, mantissa not zero).  A vector that is not settled that
-// way takes the exact form for all its elements.
-__device__ __forceinline__ uint2 fast8(uint4 v, float r, float d) {
+// Eight bf16 values (one 16-byte vector) -> eight codes by the fast form, low
+// byte first; y = RN(1 / d), nd = -d, d in the fast_ok range.  `flags` gets
+// 0x80 in each byte whose code is the NaN code: the caller takes the exact form
+// for those (they come only from NaN or infinite inputs or an overflowing x * y).
+__device__ __forceinline__ uint2 fast8(uint4 v, float y, float nd, uint2& flags) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  const float dn = 1.0f - 0x1p-21f, up = 1.0f + 0x1p-21f;
-  uint32_t lo[2] = {0, 0}, hi[2] = {0, 0};
-  uint32_t nan = 0;
+  const float2 y2 = make_float2(y, y), nd2 = make_float2(nd, nd);
+  uint32_t c[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float2 q = __fmul2_rn(make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u)),
-                                make_float2(r, r));
-    const float2 a = __fmul2_rn(q, make_float2(dn, dn)), b = __fmul2_rn(q, make_float2(up, up));
-    lo[k >> 1] |= cvt_pair(a.x, a.y) << (16 * (k & 1));
-    hi[k >> 1] |= cvt_pair(b.x, b.y) << (16 * (k & 1));
-    nan |= __vcmpgtu2(w[k] & 0x7FFF7FFFu, 0x7F807F80u);
+    const float2 x = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+    float2 q = __fmul2_rn(x, y2);
+#pragma unroll
+    for (int s = 0; s < 2; ++s) q = __ffma2_rn(__ffma2_rn(q, nd2, x), y2, q);  // q += (x - d q) y
+    c[k] = cvt_pair(q.x, q.y);
   }
-  if (lo[0] == hi[0] && lo[1] == hi[1] && nan == 0) return make_uint2(lo[0], lo[1]);
-  return make_uint2(exact_pair(w[0], d) | (exact_pair(w[1], d) << 16), exact_pair(w[2], d) | (exact_pair(w[3], d) << 16));
+  const uint32_t mag = 0x7F7F7F7Fu;
+  const uint32_t c0 = __byte_perm(c[0], c[1], 0x5410) & mag, c1 = __byte_perm(c[2], c[3], 0x5410) & mag;
+  // (b & 0x7F) + 1 sets bit 7 of a byte exactly when its code is 0x7F / 0xFF
+  flags = make_uint2((c0 + 0x01010101u) & ~mag, (c1 + 0x01010101u) & ~mag);
+  // sign bits of the eight inputs: bit 15 and bit 31 of each word
+  const uint32_t s0 = __byte_perm(w[0], w[1], 0x7531), s1 = __byte_perm(w[2], w[3], 0x7531);
+  return make_uint2(c0 | (s0 & ~mag), c1 | (s1 & ~mag));
 }
 
-// Eight bf16 values -> eight codes by the fast form, settled pair by pair:
-// returns a 4-bit mask of the pairs the fast form could not settle (bracket
-// codes differ, or a NaN code, which only a NaN input gives); those pairs'
-// codes in `out` are not final and the caller takes the exact form for them.
-__device__ __forceinline__ uint32_t fast8_masked(uint4 v, float r, uint2& out) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  const float dn = 1.0f - 0x1p-21f, up = 1.0f + 0x1p-21f;
-  uint32_t ca[4], cb[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 q = __fmul2_rn(make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u)),
-                                make_float2(r, r));
-    const float2 a = __fmul2_rn(q, make_float2(dn, dn)), b = __fmul2_rn(q, make_float2(up, up));
-    ca[k] = cvt_pair(a.x, a.y);
-    cb[k] = cvt_pair(b.x, b.y);
-  }
-  const uint32_t lo0 = __byte_perm(ca[0], ca[1], 0x5410), lo1 = __byte_perm(ca[2], ca[3], 0x5410);
-  const uint32_t hi0 = __byte_perm(cb[0], cb[1], 0x5410), hi1 = __byte_perm(cb[2], cb[3], 0x5410);
-  const uint32_t n0 = __vcmpne2((lo0 ^ hi0) | __vcmpeq4(lo0 & 0x7F7F7F7Fu, 0x7F7F7F7Fu), 0);
-  const uint32_t n1 = __vcmpne2((lo1 ^ hi1) | __vcmpeq4(lo1 & 0x7F7F7F7Fu, 0x7F7F7F7Fu), 0);
-  out = make_uint2(lo0, lo1);
-  return (n0 & 1u) | ((n0 >> 15) & 2u) | ((n1 & 1u) << 2) | ((n1 >> 13) & 8u);
+// The pairs (input words) of a vector whose codes `fast8` flagged: bit j for word j.
+__device__ __forceinline__ uint32_t flagged_pairs(uint2 f) {
+  return (uint32_t)((f.x & 0x8080u) != 0) | ((uint32_t)((f.x >> 16) != 0) << 1) |
+         ((uint32_t)((f.y & 0x8080u) != 0) << 2) | ((uint32_t)((f.y >> 16) != 0) << 3);
 }
 
 }  // namespace quant

@@ -1,7 +1,8 @@
 // Q -> E4M3 quantization (the sliding-window layers quantize Q to FP8, vLLM
 // PR 63139, Overview).  q8 = RNE_saturate_e4m3(fl32(q / q_descale)), computed
-// bit-identically without a division per element in all but rare cases (see
-// quant_e4m3.cuh); a NaN quotient gives 0x7F with the input's sign bit.
+// bit-identically without a division (Markstein's correction, quant_e4m3.cuh)
+// but for vectors holding NaN or infinite inputs or overflowing quotients; a NaN
+// quotient gives 0x7F with the input's sign bit.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -17,15 +18,17 @@ namespace {
 __global__ void quantize_q_vec8(const uint4* __restrict__ q, uint2* __restrict__ out, const float* __restrict__ qd,
                                 long long n8) {
   ptx::griddep_wait();
-  const float d = *qd, r = __frcp_rn(d);
+  const float d = *qd, y = __frcp_rn(d);
   const bool fast = quant::fast_ok(d);
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
     const uint4 v = q[i];
-    if (fast)
-      out[i] = quant::fast8(v, r, d);
-    else
-      out[i] = make_uint2(quant::exact_pair(v.x, d) | (quant::exact_pair(v.y, d) << 16),
-                          quant::exact_pair(v.z, d) | (quant::exact_pair(v.w, d) << 16));
+    uint2 c, f = make_uint2(1, 0);
+    if (fast) c = quant::fast8(v, y, -d, f);
+    // a vector with a flagged code (NaN / infinite inputs, overflow) takes the exact form
+    if (f.x | f.y)
+      c = make_uint2(quant::exact_pair(v.x, d) | (quant::exact_pair(v.y, d) << 16),
+                     quant::exact_pair(v.z, d) | (quant::exact_pair(v.w, d) << 16));
+    out[i] = c;
   }
   // Let the next kernel (the forward's plan) launch only as this grid drains:
   // launched earlier, the attention grid behind it would take SM room from the

@@ -43,7 +43,8 @@ def _run_both(k, v, slots, kd, vd, pool_pages, key_view=None, value_view=None):
     return kc.cpu().numpy(), vc.cpu().numpy(), okc, ovc, bad
 
 
-@pytest.mark.parametrize("hkv,d,T", [(16, 256, 517), (4, 512, 333), (16, 256, 1), (2, 64, 70)])
+@pytest.mark.parametrize("hkv,d,T", [(16, 256, 517), (4, 512, 333), (16, 256, 1), (2, 64, 70), (3, 512, 97),
+                                     (5, 200, 45), (6, 512, 1000)])
 def test_kv_write_bit_exact_against_oracle(hkv, d, T):
     pool = (T + 63) // 64 * 2 + 1
     k, v, slots, kd, vd = _case(T * 7 + d, T, hkv, d, pool)
@@ -139,3 +140,38 @@ def test_kv_write_every_bf16_pattern_with_short_mantissa_descales(kd, vd):
     assert bad == 0
     assert np.array_equal(kc, okc), np.argwhere(kc != okc)[:5]
     assert np.array_equal(vc, ovc), np.argwhere(vc != ovc)[:5]
+
+
+def _fast_range_descales():
+    """fp32 descales across the division-free quantizer's range [2^-64, 2^64],
+    its two edges and the values just outside them (those take the division),
+    mantissas of all ones, and mantissas 2^20 a +- s, which put quotients of
+    bf16 inputs very close to fp32 rounding midpoints next to E4M3 boundaries."""
+    rng = np.random.default_rng(2024)
+    ds = [2.0 ** -64, 2.0 ** 64, float(np.nextafter(np.float32(2.0 ** -64), np.float32(0))),
+          float(np.nextafter(np.float32(2.0 ** 64), np.float32(np.inf)))]
+    ds += list(2.0 ** rng.uniform(-64, 64, 12)) + list(10.0 ** rng.uniform(-4, 2, 8))
+    ds += [np.ldexp(1 - 2.0 ** -24, e) for e in (-40, -3, 0, 9, 50)]
+    ds += [np.ldexp(float((a << 20) + s), e - 23) for a, s, e in
+           [(8, 1, 0), (9, -3, -4), (11, 5, 3), (13, -7, -10), (15, 9, 0), (12, -1, 6)]]
+    return [float(np.float32(x)) for x in ds]
+
+
+def test_kv_write_every_bf16_pattern_across_the_fast_range():
+    """Every bf16 bit pattern as a key and a value under descales spread over
+    the whole range of the division-free form and just outside it: the cache
+    matches the oracle bit for bit (-0, subnormals, infinities, NaNs, quotients
+    that overflow fp32 included)."""
+    T, hkv, d, pool = 128, 2, 256, 3
+    pat = np.arange(65536, dtype=np.uint16)
+    rng = np.random.default_rng(37)
+    k = torch.from_numpy(rng.permutation(pat).astype(np.int16).reshape(T, hkv, d)).view(torch.bfloat16)
+    v = torch.from_numpy(rng.permutation(pat).astype(np.int16).reshape(T, hkv, d)).view(torch.bfloat16)
+    slots = rng.permutation(pool * 64)[:T].astype(np.int64)
+    ds = _fast_range_descales()
+    for i, kd in enumerate(ds):
+        vd = ds[(i + 7) % len(ds)]
+        kc, vc, okc, ovc, bad = _run_both(k, v, slots, kd, vd, pool)
+        assert bad == 0
+        assert np.array_equal(kc, okc), (kd, np.argwhere(kc != okc)[:5])
+        assert np.array_equal(vc, ovc), (vd, np.argwhere(vc != ovc)[:5])

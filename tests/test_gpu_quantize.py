@@ -11,7 +11,9 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("descale", [1.0, 3.7 / 448, 2.0 ** -10, 1000.0, 0.0123456, 1.0 / 3.0,
-                                     35.0 / 448, 5.0, 3.0 / 64, 0.75])
+                                     35.0 / 448, 5.0, 3.0 / 64, 0.75, 2.0 ** -64, 2.0 ** 64, 2.0 ** -65, 2.0 ** 65,
+                                     1e-30, 3.1e18, (1 - 2.0 ** -24) * 4, (9 * 2 ** 20 - 3) * 2.0 ** -27,
+                                     (13 * 2 ** 20 + 7) * 2.0 ** -23])
 def test_quantize_all_bf16_patterns_bit_exact(descale):
     import fp8_paged_attention_gb300 as fp8pa
     bits = np.arange(65536, dtype=np.uint16)
