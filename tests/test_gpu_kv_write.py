@@ -127,9 +127,9 @@ def test_kv_write_then_attention_reads_what_was_written():
                          ids=["short_mantissa_5_64_3_64", "short_mantissa_0.75_5", "short_35_448_and_unit"])
 def test_kv_write_every_bf16_pattern_with_short_mantissa_descales(kd, vd):
     """Every bf16 bit pattern as a key and a value, under descales whose short
-    mantissas put many quotients exactly on E4M3 rounding boundaries: most
-    vectors then hold pairs the fast form cannot settle, which the warps hand
-    to the exact form together.  The cache matches the oracle bit for bit."""
+    mantissas put many quotients exactly on E4M3 rounding boundaries, where the
+    division-free quotient must round exactly as the IEEE division does.  The
+    cache matches the oracle bit for bit."""
     T, hkv, d, pool = 128, 2, 256, 3
     pat = np.arange(65536, dtype=np.uint16)
     rng = np.random.default_rng(31)
