@@ -312,6 +312,11 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using C = AttnCfg<D, kPath, N, kCtas>;
   constexpr bool kQ8 = C::kQ8, kP8 = C::kP8, kDq = C::kDq, kDqV = C::kDqV, kQS = C::kQSplit, kKDq = C::kKDq;
+  // Decode-shaped tiles with E4M3 V: the key union's edge pages are read trimmed
+  // to their visible slots (page_slot0).  The literal path's V conversion keeps
+  // whole pages, and so do 64-row tiles, whose unions are long enough that the
+  // edge pages weigh little against the per-tile work the trim adds.
+  constexpr bool kTrim = kP8 && N <= 32;
   using namespace ptx;
   using namespace detail;
   constexpr int S = C::kStages;
@@ -476,8 +481,9 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         const int n = it.t1 - it.t0;
         auto load_tile = [&](int u, bool is_v) -> bool {
           const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
-          const int pg = it.pg_lo + 2 * (it.t0 + u);
+          const int pg = it.pg_lo() + 2 * (it.t0 + u);
           const int pa = page_id(p, it, pg), pb = page_id(p, it, pg + 1);
+          const int sa = kTrim ? page_slot0(it, pg) : 0, sb = kTrim ? page_slot0(it, pg + 1) : 0;
           for (int c = 0; c < DC; ++c) {
             uint32_t& pos = !kSplit ? idx : is_v ? vq : kq;
             const uint32_t len = !kSplit ? S : is_v ? SV : SK;
@@ -486,8 +492,8 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
             if (leader) {
               mbar_arrive_expect_tx(&ring_full[slot], kStageBytes);
               uint8_t* dst = ring + slot * kStageBytes;
-              tma_load_4d(dst, tm, &ring_full[slot], c * 128, it.hk, 0, pa);
-              tma_load_4d(dst + kStageBytes / 2, tm, &ring_full[slot], c * 128, it.hk, 0, pb);
+              tma_load_4d(dst, tm, &ring_full[slot], c * 128, it.hk, sa, pa);
+              tma_load_4d(dst + kStageBytes / 2, tm, &ring_full[slot], c * 128, it.hk, sb, pb);
             }
             ++pos;
           }
@@ -657,7 +663,9 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         };
         ++qit;  // pv() reads qit - 1 as this item's ordinal
         const int n = it.t1 - it.t0;
-        auto is_tail = [&](int u) { return (it.pg_lo + 2 * (it.t0 + u)) * kPage + kTileKeys > it.Lk; };
+        auto is_tail = [&](int u) {
+          return (it.pg_lo() + 2 * (it.t0 + u)) * kPage + kTileKeys > it.Lk && !(kTrim && edges_trimmed(it));
+        };
         if (C::kTwoIssuers) {
           if (do_qk) {
             for (int u = 0; u < n && ok; ++u) ok = qk(g + u);
@@ -779,11 +787,16 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
       for (int n = 0; n < NR; ++n) lt[n] = 0.f;
 
       for (int u = 0; u < n_t; ++u, ++g) {
-        const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
-        const int j = kb + kl;
+        const int kb = (it.pg_lo() + 2 * (it.t0 + u)) * kPage;
+        const bool trimmed = kTrim && edges_trimmed(it);
+        int j = kb + kl;  // this lane's key; -1 for a box row outside its page (zero fill)
+        if (trimmed) {
+          const int r = (kl & (kPage - 1)) + page_slot0(it, kb / kPage + kl / kPage);
+          j = (r >= 0 && r < kPage) ? kb + (kl & kPage) + r : -1;
+        }
         const uint32_t sb = g & 1, pb = g & 1;
         const bool interior = kb >= it.lo_max && kb + kTileKeys - 1 <= it.hi_min;
-        const bool tail = kP8 && kb + kTileKeys > it.Lk;
+        const bool tail = kP8 && kb + kTileKeys > it.Lk && !trimmed;
         bool ok = pwait(&s_full[sb], (g >> 1) & 1, lim, abort_flag);
         if (ok && g >= 2) ok = pwait(&pv_done[pb], ((g >> 1) - 1) & 1, lim, abort_flag);  // P buffer free
         ok = __all_sync(0xFFFFFFFFu, ok);
@@ -1279,7 +1292,7 @@ __global__ void __launch_bounds__(AttnCfg<D, kPath, N, kCtas>::kThreads, kCtas)
         // Warp wq converts the 16-byte pieces wq * 32 + lane + 128 j of each stage.
         auto convert_v = [&](int u) -> bool {
           if (!kDqV) return true;  // the PV MMA reads these stages as E4M3, from the V ring
-          const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
+          const int kb = (it.pg_lo() + 2 * (it.t0 + u)) * kPage;
           const int zero_from = (kb + kTileKeys > it.Lk) ? max(0, it.Lk - kb) : kTileKeys;
           const int dt = wq * 32 + lane;
           for (int c = 0; c < DC; ++c) {

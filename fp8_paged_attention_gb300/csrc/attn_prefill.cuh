@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       const uint32_t qpar = (qit / QB) & 1;
       ++qit;
       auto load_k = [&](int u) -> bool {
-        const int pg = it.pg_lo + 2 * (it.t0 + u);
+        const int pg = it.pg_lo() + 2 * (it.t0 + u);
         const int pa = page_id(p, it, pg), pb = page_id(p, it, pg + 1);
         for (int c = 0; c < DC; ++c) {
           const uint32_t slot = kq % SK;
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         return true;
       };
       auto load_v = [&](int u) -> bool {
-        const int pg = it.pg_lo + 2 * (it.t0 + u);
+        const int pg = it.pg_lo() + 2 * (it.t0 + u);
         const int pa = page_id(p, it, pg), pb = page_id(p, it, pg + 1);
         const uint32_t slot = vq % SV;
         if (!wait_all(&v_empty[slot], ((vq / SV) & 1) ^ 1)) return false;
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         for (int u = 0; u < n && ok; ++u) {
           const uint32_t gg = g + u, sb = gg & 1;
           const uint32_t slot = vq % SV, vpar = (vq / SV) & 1;
-          const bool tail = (it.pg_lo + 2 * (it.t0 + u)) * kPage + kTileKeys > it.Lk;
+          const bool tail = (it.pg_lo() + 2 * (it.t0 + u)) * kPage + kTileKeys > it.Lk;
           if (tail) {
             // the softmax zeroes this tile's V rows past Lk once the stage has landed
             if (!(ok = wait_all(&v_full[slot], vpar))) break;
@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       float m = NEG_INF, l0 = 0.f, l1 = 0.f;
       bool sticky = true;  // waits after a tile's vote that failed; reported at the next vote
       for (int u = 0; u < n; ++u, ++g) {
-        const int kb = (it.pg_lo + 2 * (it.t0 + u)) * kPage + KT * hw;  // first key of this part
+        const int kb = (it.pg_lo() + 2 * (it.t0 + u)) * kPage + KT * hw;  // first key of this part
         const uint32_t sb = g & 1;
         const bool sok = wait_w(&s_full[sb], (g >> 1) & 1);
         float x[KT];
@@ -584,7 +584,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         tmem_wait_st();
         // rows of the last page past the sequence end may hold anything (even NaN):
         // zero those V rows so that 0 * V stays 0 in the PV MMA
-        const int kt = (it.pg_lo + 2 * (it.t0 + u)) * kPage;
+        const int kt = (it.pg_lo() + 2 * (it.t0 + u)) * kPage;
         if (kt + kTileKeys > it.Lk) {
           sticky = wait_w(v_ready, tails & 1) && sticky;
           ++tails;

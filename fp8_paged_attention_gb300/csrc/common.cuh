@@ -132,11 +132,12 @@ struct Item {
   int b, rt, hk, split, nsplit;
   int q0, Lq, Lk;
   int row0, nrows;       // first packed row of the tile, valid rows (<= N)
-  int pg_lo;             // first logical page of the tile's key union
-  int t0, t1;            // 128-key tiles [t0, t1) of this split; tile t starts at key (pg_lo + 2t) * 64
+  int lo_min;            // first key visible to any row
+  int t0, t1;            // 128-key tiles [t0, t1) of this split; tile t starts at key (pg_lo() + 2t) * 64
   int lo_max, hi_min;    // keys in [lo_max, hi_min] are visible to every valid row
   int hi_max;            // last key visible to any row (for tail sanitation)
   int dhalf;             // slice of the output dims this item computes (classes with dhalves > 1)
+  __device__ __forceinline__ int pg_lo() const { return lo_min / kPage; }  // first logical page of the key union
 };
 
 // Work item encoding: {b, row_tile, hk | split << 16, nsplit}.
@@ -174,16 +175,35 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int4 w) {
   it.hi_min = hi_f;
   it.hi_max = hi_l;
   if (it.Lk <= 0 || hi_l < lo_f || hi_l < 0) {
-    it.pg_lo = 0;
+    it.lo_min = 0;
     it.t0 = it.t1 = 0;
     return it;
   }
-  it.pg_lo = lo_f / kPage;
-  int pages = hi_l / kPage - it.pg_lo + 1;
+  it.lo_min = lo_f;
+  int pages = hi_l / kPage - it.pg_lo() + 1;
   int tiles = (pages + 1) / 2;
   it.t0 = (int)((long long)it.split * tiles / it.nsplit);
   it.t1 = (int)((long long)(it.split + 1) * tiles / it.nsplit);
   return it;
 }
+
+// First slot of the page box read for logical page pg of the item's key union
+// (decode-shaped tiles with E4M3 V).  The union's first page starts at its first
+// visible slot, and its last page ends at its last visible slot (a negative
+// start: the box rows before slot 0 lie outside the page), so neither edge page
+// reads slots that no row can see, nor slots past the sequence end; box rows
+// outside the page arrive as zeros.  0 for the other pages, and for every page
+// when the union lies within one page.  Box row r of page pg then holds key
+// pg * 64 + r + page_slot0(it, pg).
+__device__ __forceinline__ int page_slot0(const Item& it, int pg) {
+  const int first = it.pg_lo(), last = it.hi_max / kPage;
+  if (first == last) return 0;
+  if (pg == first) return it.lo_min - first * kPage;
+  if (pg == last) return it.hi_max - last * kPage + 1 - kPage;
+  return 0;
+}
+// True when page_slot0 trims the item's edge pages: then no tile holds rows
+// past the sequence end.
+__device__ __forceinline__ bool edges_trimmed(const Item& it) { return it.pg_lo() != it.hi_max / kPage; }
 
 }  // namespace fp8pa
