@@ -76,6 +76,34 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("d,hkv,fp8", [(256, 16, True), (512, 4, True), (512, 4, False)],
+                         ids=["hd256_fp8", "hd512_fp8", "hd512_bf16q"])
+def test_decode_tiles_never_read_slots_before_the_window(d, hkv, fp8):
+    """Decode-shaped tiles read a key union's first page from its first visible
+    slot, so the slots before the window may hold anything: here the E4M3 NaN
+    code in K and V, which would reach the output through 0 * NaN if they were
+    read.  Window starts fall at many offsets within a page; one sequence's
+    union lies within one page (that item reads whole pages, so its page is
+    left clean).  Auto split and three explicit splits."""
+    wl = 700
+    lks = [40] + [wl + 2 + 73 * i for i in range(12)]
+    w = make(f"trim_{d}_{int(fp8)}", [1] * len(lks), lks, 32, hkv, d, wl, True, fp8, seed=41)
+    poisoned = 0
+    for b, lk in enumerate(lks):
+        lo = max(0, lk - 1 - wl)
+        if lo // 64 == (lk - 1) // 64 or lo % 64 == 0:
+            continue
+        phys = int(w.bt[b, lo // 64])
+        w.k_cache[phys, : lo % 64] = 0x7F
+        w.v_cache[phys, : lo % 64] = 0x7F
+        poisoned += 1
+    assert poisoned >= 10
+    ref = oracle.paged_attention(oracle_problem(w))
+    for splits in (0, 3):
+        out, lse = run_gpu(w, num_splits=splits)
+        check(w, out, lse, ref=ref)
+
+
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_attention_cases(case):
     name, lq, lk, hq, hkv, d, wl, causal, fp8 = case
