@@ -7,6 +7,10 @@
 // KV head, row tile and split: CTAs that run side by side read every KV head
 // of the same pages (the heads of one slot are adjacent in memory), and with a
 // shared prefix the same pages again a few sequences later, while still in L2.
+// A prefill-like sequence with many items lists its row tiles last to first,
+// so that a causal chunk's longest units start first and the grid ends on
+// short ones: across all KV heads when its class runs alone, one KV head at a
+// time when it runs beside the other class.
 //
 // combine_kernel merges the per-split partial outputs with their log-sum-exps:
 //   L = log (sum_s exp(lse_s) + exp(sink)),  out = sum_s exp(lse_s - L) * O_s
@@ -192,7 +196,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
     }
   // Items of a sequence: (KV head, row tile, split), split fastest.  A thread
   // writes its own sequences' short lists; a long list (a prefill sequence)
-  // is written by the whole warp, 32 items per round.
+  // is written by the whole warp, 32 items per round, in the order below.
+  const bool beside = total[0] > 0 && total[1] > 0;  // both classes run, side by side
   constexpr int kLongList = 64;
   for (int j = 0; j < per; ++j) {
     const int b = b0 + j;
@@ -225,11 +230,27 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
       const int sstart = __shfl_sync(0xFFFFFFFFu, start, src);
       const int srts = __shfl_sync(0xFFFFFFFFu, rts, src);
       const int sns = __shfl_sync(0xFFFFFFFFu, ns, src);
-      const int per_head = srts * sns;
+      // Row tiles last to first, so that a causal sequence's longest units go
+      // out first and the grid ends on short ones.  Alone, the class takes them
+      // across all KV heads (row tile, then head, then split); beside the other
+      // class, whose K/V stream through L2 meanwhile, one head at a time (head,
+      // then row tile, then split), which keeps fewer of its pages hot in L2.
+      const int per_head = srts * sns, per_tile = pp.hkv * sns;
       int4* dst = pp.work[sk] + (size_t)sstart * pp.hkv;
       for (int i = lane; i < per_head * pp.hkv; i += 32) {
-        const int hk = i / per_head, rem = i - hk * per_head;
-        dst[i] = make_int4(sb, rem / sns, hk | ((rem % sns) << 16), sns);
+        int hk, rt, s;
+        if (beside) {
+          hk = i / per_head;
+          const int rem = i - hk * per_head;
+          rt = srts - 1 - rem / sns;
+          s = rem % sns;
+        } else {
+          rt = srts - 1 - i / per_tile;
+          const int rem = i % per_tile;
+          hk = rem / sns;
+          s = rem % sns;
+        }
+        dst[i] = make_int4(sb, rt, hk | (s << 16), sns);
       }
     }
   }
