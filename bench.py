@@ -648,7 +648,9 @@ def time_workload(w: synth.Workload, args, dev, world: int, steps: int, warmup: 
 
         e2e_run(max(3, warmup // 4), True)
         torch.cuda.synchronize()
-        n_e2e = max(10, steps // 4)
+        # the first upload and the last read-back lie outside the overlap: enough
+        # steps that they weigh little against the steady state a serving loop runs in
+        n_e2e = max(40, steps // 2)
         barrier()
         a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(up_stream)
