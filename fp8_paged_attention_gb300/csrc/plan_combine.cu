@@ -84,13 +84,47 @@ __device__ __forceinline__ int seq_lq(const PlanParams& pp, int b) {
   return e - a;
 }
 
+// A sequence whose item list is long (a prefill-like sequence): its first item
+// slot, row tiles and splits, in class kc.
+struct LongList {
+  int b, kc, start, rts, ns;
+};
+constexpr int kLongQueue = 64;  // long lists the whole block writes; more go to their own warps
+
+// Item i of a long list.  Row tiles run last to first, so that a causal
+// sequence's longest units go out first and the grid ends on short ones.
+// Alone, the class takes them across all KV heads (row tile, then head, then
+// split); beside the other class, whose K/V stream through L2 meanwhile, one
+// head at a time (head, then row tile, then split), which keeps fewer of its
+// pages hot in L2.
+__device__ __forceinline__ void write_long_item(const PlanParams& pp, const LongList& l, int i, bool beside) {
+  int hk, rt, s;
+  if (beside) {
+    const int per_head = l.rts * l.ns;
+    hk = i / per_head;
+    const int rem = i - hk * per_head;
+    rt = l.rts - 1 - rem / l.ns;
+    s = rem % l.ns;
+  } else {
+    const int per_tile = pp.hkv * l.ns;
+    rt = l.rts - 1 - i / per_tile;
+    const int rem = i % per_tile;
+    hk = rem / l.ns;
+    s = rem % l.ns;
+  }
+  pp.work[l.kc][(size_t)l.start * pp.hkv + i] = make_int4(l.b, rt, hk | (s << 16), l.ns);
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
   static_assert(kPlanThreads == 32 * 32, "two-level warp scan");
   ptx::griddep_launch_dependents();  // the attention grid may start its prologue
   ptx::griddep_wait();               // inputs and the workspace belong to earlier kernels until they finish
   __shared__ int wsum[2][32];
   __shared__ long long wwork[2][32];
+  __shared__ LongList long_q[kLongQueue];
+  __shared__ int n_long;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (tid == 0) n_long = 0;  // published by the __syncthreads of the scans below
   const int per = (pp.batch + kPlanThreads - 1) / kPlanThreads;
   const int b0 = min(pp.batch, tid * per), b1 = min(pp.batch, b0 + per);
   int cnt[2] = {0, 0};
@@ -195,8 +229,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
       pp.counts[2 + k] = 0;  // the attention kernel's dynamic item counter
     }
   // Items of a sequence: (KV head, row tile, split), split fastest.  A thread
-  // writes its own sequences' short lists; a long list (a prefill sequence)
-  // is written by the whole warp, 32 items per round, in the order below.
+  // writes its own sequences' short lists; long lists (prefill sequences, in
+  // the order of write_long_item) are queued and written by the whole block
+  // once every thread has seen its sequences.
   const bool beside = total[0] > 0 && total[1] > 0;  // both classes run, side by side
   constexpr int kLongList = 64;
   for (int j = 0; j < per; ++j) {
@@ -223,36 +258,26 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams pp) {
         for (int rt = 0; rt < rts; ++rt)
           for (int s = 0; s < ns; ++s) *dst++ = make_int4(b, rt, hk | (s << 16), ns);
     }
-    for (unsigned lm = __ballot_sync(0xFFFFFFFFu, nitems > kLongList); lm; lm &= lm - 1) {
-      const int src = __ffs(lm) - 1;
-      const int sk = __shfl_sync(0xFFFFFFFFu, kc, src);
-      const int sb = __shfl_sync(0xFFFFFFFFu, b, src);
-      const int sstart = __shfl_sync(0xFFFFFFFFu, start, src);
-      const int srts = __shfl_sync(0xFFFFFFFFu, rts, src);
-      const int sns = __shfl_sync(0xFFFFFFFFu, ns, src);
-      // Row tiles last to first, so that a causal sequence's longest units go
-      // out first and the grid ends on short ones.  Alone, the class takes them
-      // across all KV heads (row tile, then head, then split); beside the other
-      // class, whose K/V stream through L2 meanwhile, one head at a time (head,
-      // then row tile, then split), which keeps fewer of its pages hot in L2.
-      const int per_head = srts * sns, per_tile = pp.hkv * sns;
-      int4* dst = pp.work[sk] + (size_t)sstart * pp.hkv;
-      for (int i = lane; i < per_head * pp.hkv; i += 32) {
-        int hk, rt, s;
-        if (beside) {
-          hk = i / per_head;
-          const int rem = i - hk * per_head;
-          rt = srts - 1 - rem / sns;
-          s = rem % sns;
-        } else {
-          rt = srts - 1 - i / per_tile;
-          const int rem = i % per_tile;
-          hk = rem / sns;
-          s = rem % sns;
-        }
-        dst[i] = make_int4(sb, rt, hk | (s << 16), sns);
-      }
+    // long lists: queued for the whole block, or written by the warp when the queue is full
+    const bool long_list = nitems > kLongList;
+    int qslot = -1;
+    if (long_list) {
+      qslot = atomicAdd(&n_long, 1);
+      if (qslot < kLongQueue) long_q[qslot] = LongList{b, kc, start, rts, ns};
     }
+    for (unsigned lm = __ballot_sync(0xFFFFFFFFu, long_list && qslot >= kLongQueue); lm; lm &= lm - 1) {
+      const int src = __ffs(lm) - 1;
+      const LongList l{__shfl_sync(0xFFFFFFFFu, b, src), __shfl_sync(0xFFFFFFFFu, kc, src),
+                       __shfl_sync(0xFFFFFFFFu, start, src), __shfl_sync(0xFFFFFFFFu, rts, src),
+                       __shfl_sync(0xFFFFFFFFu, ns, src)};
+      for (int i = lane; i < l.rts * l.ns * pp.hkv; i += 32) write_long_item(pp, l, i, beside);
+    }
+  }
+  __syncthreads();
+  const int nq = min(n_long, kLongQueue);
+  for (int q = 0; q < nq; ++q) {
+    const LongList l = long_q[q];
+    for (int i = tid; i < l.rts * l.ns * pp.hkv; i += kPlanThreads) write_long_item(pp, l, i, beside);
   }
 }
 
