@@ -14,21 +14,33 @@ namespace fp8pa {
 
 namespace {
 
-// 8 elements per thread when both pointers allow 16-byte / 8-byte accesses.
+// 8 elements per vector when both pointers allow 16-byte / 8-byte accesses; up
+// to kV grid-strided vectors per thread and pass, loaded before any converts
+// (kV = 1 for inputs that one pass of the grid covers: a short kernel's code
+// stays small).
+template <int kV>
 __global__ void quantize_q_vec8(const uint4* __restrict__ q, uint2* __restrict__ out, const float* __restrict__ qd,
                                 long long n8) {
   ptx::griddep_wait();
   const float d = *qd, y = __frcp_rn(d);
   const bool fast = quant::fast_ok(d);
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
-    const uint4 v = q[i];
-    uint2 c, f = make_uint2(1, 0);
-    if (fast) c = quant::fast8(v, y, -d, f);
-    // a vector with a flagged code (NaN / infinite inputs, overflow) takes the exact form
-    if (f.x | f.y)
-      c = make_uint2(quant::exact_pair(v.x, d) | (quant::exact_pair(v.y, d) << 16),
-                     quant::exact_pair(v.z, d) | (quant::exact_pair(v.w, d) << 16));
-    out[i] = c;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x; i0 < n8; i0 += kV * stride) {
+    uint4 v[kV];
+#pragma unroll
+    for (int k = 0; k < kV; ++k)
+      if (i0 + k * stride < n8) v[k] = q[i0 + k * stride];
+#pragma unroll
+    for (int k = 0; k < kV; ++k) {
+      if (i0 + k * stride >= n8) break;
+      uint2 c, f = make_uint2(1, 0);
+      if (fast) c = quant::fast8(v[k], y, -d, f);
+      // a vector with a flagged code (NaN / infinite inputs, overflow) takes the exact form
+      if (f.x | f.y)
+        c = make_uint2(quant::exact_pair(v[k].x, d) | (quant::exact_pair(v[k].y, d) << 16),
+                       quant::exact_pair(v[k].z, d) | (quant::exact_pair(v[k].w, d) << 16));
+      out[i0 + k * stride] = c;
+    }
   }
   // Let the next kernel (the forward's plan) launch only as this grid drains:
   // launched earlier, the attention grid behind it would take SM room from the
@@ -57,9 +69,11 @@ cudaError_t launch_quantize_q(const void* q_bf16, void* q_e4m3, const float* q_d
     const long long n8 = n / 8;
     if (n8 > 0) {
       const long long blocks = (n8 + 255) / 256;
-      cudaError_t e = launch_pdl(quantize_q_vec8, dim3((unsigned)(blocks < 4096 ? blocks : 4096)), dim3(256), 0, stream,
-                                 reinterpret_cast<const uint4*>(q_bf16), reinterpret_cast<uint2*>(q_e4m3), q_descale,
-                                 n8);
+      const dim3 grid((unsigned)(blocks < 4096 ? blocks : 4096));
+      const uint4* src = reinterpret_cast<const uint4*>(q_bf16);
+      uint2* dst = reinterpret_cast<uint2*>(q_e4m3);
+      cudaError_t e = blocks <= 4096 ? launch_pdl(quantize_q_vec8<1>, grid, dim3(256), 0, stream, src, dst, q_descale, n8)
+                                     : launch_pdl(quantize_q_vec8<4>, grid, dim3(256), 0, stream, src, dst, q_descale, n8);
       if (e != cudaSuccess) return e;
     }
     done = n8 * 8;
