@@ -39,3 +39,22 @@ def test_quantize_ragged_lengths_and_unaligned(n):
         assert np.array_equal(out[off:off + n].cpu().numpy(), want)
         if off == 0:
             assert out[n].item() == 0xAA   # no write past the end
+
+
+@pytest.mark.parametrize("descale", [3.7 / 448, 35.0 / 448])
+def test_quantize_input_larger_than_one_grid_pass_bit_exact(descale):
+    """An input larger than one pass of the quantizer's grid (4096 blocks x 256
+    threads x 8 elements), which loads four vectors per thread before
+    converting, with a partial last pass and a scalar tail (length not a
+    multiple of 8): every element, of random bit patterns (NaNs and
+    infinities included), against the oracle."""
+    import fp8_paged_attention_gb300 as fp8pa
+    n = 4096 * 256 * 8 * 2 + 8 * 12345 + 5
+    rng = np.random.default_rng(5)
+    bits = rng.integers(0, 65536, size=n, dtype=np.uint16)
+    q = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    d = torch.tensor([descale], dtype=torch.float32, device="cuda")
+    got = fp8pa.quantize_q_fp8(q, d).cpu().numpy()
+    want = oracle.quantize_q(bits, float(np.float32(descale)))
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(int(i), hex(int(bits[i])), hex(int(got[i])), hex(int(want[i]))) for i in bad[:10]]
