@@ -104,6 +104,16 @@ def test_decode_tiles_never_read_slots_before_the_window(d, hkv, fp8):
         check(w, out, lse, ref=ref)
 
 
+def test_plan_with_more_long_item_lists_than_its_queue():
+    """66 prefill sequences whose item lists are long (6 row tiles x 16 KV
+    heads = 96 items each): more than the plan's block-wide queue of 64 holds,
+    so the last lists are written by their own warps.  Every row against the
+    oracle."""
+    w = make("plan_overflow", [321] * 66, [321] * 66, 32, 16, 256, 31, True, True, seed=3)
+    out, lse = run_gpu(w)
+    check(w, out, lse)
+
+
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_attention_cases(case):
     name, lq, lk, hq, hkv, d, wl, causal, fp8 = case
