@@ -368,14 +368,17 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ replicas across ranks
 
-def hold_device(steps: int, host_us_per_step: float = 100.0):
-    """Enqueues a device-side wait of at least `steps * host_us_per_step` us on
-    the current stream just before a timed region.  The host then queues every
-    timed launch while the GPU waits, so a kernel shorter than its own host-side
-    submission does not sit idle inside its timed interval waiting for the
-    launch to arrive (torch's spin kernel, clock cycles at the highest SM clock;
-    it runs before the region's first event and is not part of any timing)."""
-    us = min(steps * host_us_per_step, 200000.0)
+def hold_device(steps: int, host_us_per_step: float = 100.0, margin_us: float = 100000.0):
+    """Enqueues a device-side wait of at least `steps * host_us_per_step +
+    margin_us` us on the current stream just before a timed region.  The host
+    then queues every timed launch while the GPU waits, so a kernel shorter than
+    its own host-side submission does not sit idle inside its timed interval
+    waiting for the launch to arrive; the margin absorbs a stall of the host
+    thread while it queues (one such stall of ~80 ms once stretched a 10 ms
+    region ninefold).  Torch's spin kernel, clock cycles at the highest SM
+    clock; it runs before the region's first event and is not part of any
+    timing."""
+    us = min(steps * host_us_per_step + margin_us, 600000.0)
     torch.cuda._sleep(int(us * 2070))
 
 
