@@ -5,10 +5,9 @@
 //
 // Token t goes to slot s = slot_mapping[t], i.e. row s % 64 of page s / 64 of
 // the [pages][64][Hkv][D] cache; a negative slot is a padding token.  Each
-// element is quantized like Q, by the rule E4M3_RNE_sat(fl32(x / descale)): the
-// correctly rounded fp32 quotient, then the hardware round-to-nearest-even
-// saturating conversion, a NaN quotient mapped to 0x7F with the input's sign
-// (the quotient is formed without a division, quant_e4m3.cuh).
+// element is quantized like Q: E4M3_RNE_sat(fl32(x / descale)), an IEEE fp32
+// division then the hardware round-to-nearest-even saturating conversion, a NaN
+// quotient mapped to 0x7F with the input's sign.
 //
 // The op is HBM-bound (2 bytes read, 1 written per element).  One unit is one
 // (token, tensor) row: Hkv * D contiguous bf16 elements in, the same number of
